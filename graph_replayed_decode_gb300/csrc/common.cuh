@@ -1,0 +1,115 @@
+// common.cuh -- shared device helpers of libeng: bf16 packing, warp reductions and thin inline-PTX
+// wrappers (warp-level bf16 MMA, ldmatrix, cp.async, programmatic dependent launch).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+typedef __nv_bfloat16 bf16;
+
+#define ENG_DEVICE __device__ __forceinline__
+
+// ------------------------------------------------------------------ status word bits (mirror eng.h)
+#define ST_BAD_BLOCK 1
+#define ST_BAD_POSITION 2
+#define ST_NAN 4
+#define ST_TIMEOUT 8
+
+ENG_DEVICE void set_status(int* status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------------ bf16 helpers
+ENG_DEVICE uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+ENG_DEVICE float2 unpack_bf16x2(uint32_t u) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
+  return __bfloat1622float2(v);
+}
+
+ENG_DEVICE float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+// ------------------------------------------------------------------ reductions (fixed xor trees)
+ENG_DEVICE float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+ENG_DEVICE float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------ loads
+// Streaming 16-byte load that bypasses L1 allocation (weights are read once per step).
+ENG_DEVICE uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+ENG_DEVICE uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+ENG_DEVICE void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src));
+}
+ENG_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+ENG_DEVICE void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N));
+}
+
+// ------------------------------------------------------------------ warp MMA (m16n8k16, bf16 in, f32 accumulate)
+// A: 16x16 row-major fragment (4 regs), B: 16x8 column fragment (2 regs), C/D: 16x8 f32 (4 regs).
+ENG_DEVICE void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+ENG_DEVICE void ldmatrix_x4(uint32_t r[4], const void* smem_row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(smem_row_addr)));
+}
+
+ENG_DEVICE void ldmatrix_x4_trans(uint32_t r[4], const void* smem_row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(smem_row_addr)));
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// Wait until the preceding kernel in the stream has completed and its writes are visible.  A no-op
+// when the kernel was launched without the programmatic-serialisation attribute.
+ENG_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel in the stream to begin launching (its own pdl_wait still orders its reads).
+ENG_DEVICE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// ------------------------------------------------------------------ packed weight layout
+// A weight matrix W[N][K] (row-major, N % 16 == 0, K % 32 == 0) is stored as tiles of 16 rows x 32
+// columns, tile (i, j) at ((i * K/32) + j) * 512 elements.  Inside a tile the 512 values are ordered
+// [k-step s (2)][lane (32)][8] so that one 16-byte load per lane yields that lane's m16n8k16 A
+// fragment for k-step s: with g = lane / 4, t = lane % 4, the 8 values are
+//   W[16i+g][32j+16s+2t+{0,1}], W[16i+g+8][..same..], W[16i+g][32j+16s+2t+8+{0,1}], W[16i+g+8][..same..].
+ENG_DEVICE size_t packed_offset(int row, int col, int K) {
+  const int i = row >> 4, r = row & 15;
+  const int j = col >> 5, kk = col & 31;
+  const int s = kk >> 4, kr = kk & 15;
+  const int g = r & 7, half = r >> 3;
+  const int hi8 = kr >> 3, t = (kr & 7) >> 1, lo = kr & 1;
+  const int lane = g * 4 + t;
+  const int e = hi8 * 4 + half * 2 + lo;
+  return ((size_t)i * (K >> 5) + j) * 512 + (size_t)s * 256 + lane * 8 + e;
+}

@@ -1,0 +1,990 @@
+// engine.cu -- host side of libeng: the C ABI of include/eng.h.
+//
+// Owns the fused device weights, the paged KV pool, the static step buffers (the only memory a captured
+// graph reads), the KV block pool policy and the per-step kernel sequence:
+//
+//   embed + RMSNorm -> per layer [ QKV GEMM (+bias) -> QK-norm + RoPE + KV write -> attention
+//   (prefill rows packed, decode rows one per request) -> o_proj GEMM + residual -> RMSNorm ->
+//   gate|up GEMM + SiLU*up -> down GEMM + residual -> RMSNorm (next layer) ] -> final RMSNorm at each
+//   request's last token -> LM head GEMM + greedy / Gumbel-max sampling.
+//
+// "33. Removing overhead", section "CUDA graphs for a changing batch": decode-only steps are padded to
+// the smallest captured bucket and replayed from static buffers; every host value a kernel grid depends
+// on is the bucket's, never the step's.  Section "Async scheduling" of the same page and "19. Fast
+// decode", section "Host synchronizations": the step never waits for the GPU -- inputs go through a
+// pinned staging ring whose slots are reused only after their copy has completed.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <map>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/eng.h"
+#include "kernels.h"
+
+using namespace grd;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+constexpr int kSlots = 4;  // pinned staging ring depth
+
+struct Layer {
+  bf16* qkv = nullptr;        // packed [(Hq + 2 Hkv) d][H]
+  float* qkv_bias = nullptr;  // [(Hq + 2 Hkv) d] or null
+  float* q_norm = nullptr;    // [d] or null
+  float* k_norm = nullptr;
+  bf16* o = nullptr;          // packed [H][Hq d]
+  bf16* gu = nullptr;         // packed [2I][H], gate/up rows interleaved per 16-row tile
+  bf16* down = nullptr;       // packed [H][I]
+  float* in_norm = nullptr;   // [H]
+  float* post_norm = nullptr; // [H]
+};
+
+// Word offsets of the step inputs inside one staging slot (host) and the device input region.
+struct InLayout {
+  size_t ids, pos, tok2req, cu, seq, last, invt, rng, wlog, items, bt, words;
+};
+
+struct GemmSite {
+  int N = 0, K = 0, RG = 1, S = 1, ktn = 0;
+  int* tickets = nullptr;
+};
+
+}  // namespace
+
+struct eng {
+  eng_config_t c{};
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  cudaStream_t cap_stream = nullptr;
+  std::vector<void*> allocations;
+  std::string err;
+
+  // weights
+  bf16* embed = nullptr;  // packed [V][H]
+  bf16* lm = nullptr;     // packed [V][H] (== embed when tied)
+  float* final_norm = nullptr;
+  std::vector<Layer> layers;
+  float* rope = nullptr;  // [max_pos][d/2][2]
+  int max_pos = 0;
+
+  // KV pool [L][2][NB + 1][Hkv][16][d]
+  bf16* kv = nullptr;
+  size_t kv_elems = 0;
+
+  // inputs
+  InLayout in{};
+  int* d_in = nullptr;
+  int* h_in[kSlots] = {};
+  cudaEvent_t ev[kSlots] = {};
+  int slot = 0;
+  int max_items = 0;
+
+  // activations and outputs
+  float* h = nullptr;      // [Tm][H]
+  bf16* y = nullptr;       // [Tm][H]
+  float* qkv = nullptr;    // [Tm][QKV]
+  bf16* q = nullptr;       // [Tm][Hq][d]
+  bf16* attn = nullptr;    // [Tm][Hq d]
+  bf16* act = nullptr;     // [Tm][I]
+  bf16* ylast = nullptr;   // [Rm][H]
+  float* logits = nullptr; // [Rm][V]
+  int* ids = nullptr;      // [Rm]
+  int* slots = nullptr;    // [Tm]
+  float* gemm_ws = nullptr;
+  float* attn_ws = nullptr;
+  int* attn_tickets = nullptr;
+  unsigned long long* best = nullptr;
+  int* done_counter = nullptr;
+  int* status = nullptr;
+  GemmSite g_qkv, g_o, g_gu, g_down, g_lm;
+  int split_blocks = 4, max_splits = 1;
+
+  // pool
+  std::deque<int> free_list;
+  std::vector<uint8_t> used;
+
+  // graphs
+  std::map<int, cudaGraphExec_t> graphs;
+  std::map<int, int> graph_launches;
+  bool eager_only = false;
+  bool pdl = false;
+  int launches = 0;
+  eng_step_info_t last{};
+};
+
+// ------------------------------------------------------------------ error helpers
+
+static int fail(eng_t* e, int code, const std::string& msg) {
+  if (e)
+    e->err = msg;
+  else
+    g_create_error = msg;
+  return code;
+}
+
+#define CUDA_OR_FAIL(e, call)                                                                        \
+  do {                                                                                               \
+    cudaError_t err_ = (call);                                                                       \
+    if (err_ != cudaSuccess)                                                                         \
+      return fail((e), ENG_ECUDA, std::string(#call) + ": " + cudaGetErrorString(err_));             \
+  } while (0)
+
+template <typename T>
+static int dev_alloc(eng_t* e, T** p, size_t count) {
+  void* v = nullptr;
+  const size_t bytes = std::max<size_t>(count * sizeof(T), 16);
+  cudaError_t r = cudaMalloc(&v, bytes);
+  if (r != cudaSuccess) return fail(e, ENG_ENOMEM, std::string("cudaMalloc failed: ") + cudaGetErrorString(r));
+  r = cudaMemset(v, 0, bytes);
+  if (r != cudaSuccess) return fail(e, ENG_ECUDA, std::string("cudaMemset failed: ") + cudaGetErrorString(r));
+  e->allocations.push_back(v);
+  *p = static_cast<T*>(v);
+  return ENG_OK;
+}
+
+#define TRY(x)                   \
+  do {                           \
+    int rc_ = (x);               \
+    if (rc_ != ENG_OK) return rc_; \
+  } while (0)
+
+// ------------------------------------------------------------------ config checks
+
+static std::string check_config(const eng_config_t& c) {
+  if (c.layers < 1 || c.hidden < 32 || c.q_heads < 1 || c.kv_heads < 1 || c.intermediate < 32 || c.vocab < 16)
+    return "non-positive model dimension";
+  if (c.head_dim != 64 && c.head_dim != 128) return "head_dim must be 64 or 128";
+  if (c.q_heads % c.kv_heads != 0) return "q_heads must be a multiple of kv_heads";
+  if (c.q_heads / c.kv_heads > 16) return "at most 16 query heads per KV head";
+  if (c.hidden % 32 || c.intermediate % 32 || (c.q_heads * c.head_dim) % 32) return "reduction widths must be multiples of 32";
+  if (c.vocab % 16) return "vocab must be a multiple of 16";
+  if (c.dtype != ENG_DTYPE_BF16) return "only ENG_DTYPE_BF16 weights are supported";
+  if (c.block_size != 16) return "block_size must be 16";
+  if (c.num_blocks < 1 || c.max_reqs < 1 || c.max_tokens < c.max_reqs || c.max_blocks_per_seq < 1)
+    return "bad engine capacity (num_blocks, max_reqs <= max_tokens, max_blocks_per_seq)";
+  if (!(c.rms_eps > 0.f) || !(c.rope_theta > 0.0)) return "rms_eps and rope_theta must be positive";
+  return "";
+}
+
+// ------------------------------------------------------------------ weight loading
+
+namespace {
+struct WeightMap {
+  std::unordered_map<std::string, const eng_tensor_t*> m;
+  const eng_tensor_t* get(const std::string& n) const {
+    auto it = m.find(n);
+    return it == m.end() ? nullptr : it->second;
+  }
+};
+}  // namespace
+
+// Copies `numel` bf16 values of tensor `t` to device memory at dst.
+static int copy_bf16(eng_t* e, const eng_tensor_t* t, bf16* dst, int64_t numel, const char* name) {
+  if (!t) return fail(e, ENG_EINVAL, std::string("missing weight ") + name);
+  if (t->numel != numel) return fail(e, ENG_EINVAL, std::string("wrong numel for ") + name);
+  if (t->dtype != ENG_DTYPE_BF16) return fail(e, ENG_EINVAL, std::string("expected bf16 for ") + name);
+  if (!t->data) return fail(e, ENG_EINVAL, std::string("null data for ") + name);
+  CUDA_OR_FAIL(e, cudaMemcpyAsync(dst, t->data, numel * 2, t->on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                                  e->stream));
+  return ENG_OK;
+}
+
+// Loads a 1-D weight (bf16 or f32) as f32 at dst; tmp is a bf16 scratch of at least numel values.
+static int load_f32(eng_t* e, const eng_tensor_t* t, float* dst, int64_t numel, bf16* tmp, const char* name) {
+  if (!t) return fail(e, ENG_EINVAL, std::string("missing weight ") + name);
+  if (t->numel != numel) return fail(e, ENG_EINVAL, std::string("wrong numel for ") + name);
+  if (!t->data) return fail(e, ENG_EINVAL, std::string("null data for ") + name);
+  const cudaMemcpyKind k = t->on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+  if (t->dtype == ENG_DTYPE_F32) {
+    CUDA_OR_FAIL(e, cudaMemcpyAsync(dst, t->data, numel * 4, k, e->stream));
+  } else if (t->dtype == ENG_DTYPE_BF16) {
+    CUDA_OR_FAIL(e, cudaMemcpyAsync(tmp, t->data, numel * 2, k, e->stream));
+    CUDA_OR_FAIL(e, launch_bf16_to_f32(tmp, dst, numel, e->stream));
+  } else {
+    return fail(e, ENG_EINVAL, std::string("unsupported dtype for ") + name);
+  }
+  return ENG_OK;
+}
+
+static int load_weights(eng_t* e, const eng_tensor_t* w, int32_t n) {
+  const eng_config_t& c = e->c;
+  WeightMap wm;
+  for (int i = 0; i < n; ++i) {
+    if (!w[i].name) return fail(e, ENG_EINVAL, "weight with null name");
+    wm.m[w[i].name] = &w[i];
+  }
+  const int H = c.hidden, d = c.head_dim, Hq = c.q_heads, Hkv = c.kv_heads, I = c.intermediate, V = c.vocab;
+  const int QKV = (Hq + 2 * Hkv) * d;
+  const size_t tmp_elems = std::max<size_t>({(size_t)V * H, (size_t)2 * I * H, (size_t)QKV * H, (size_t)H * Hq * d});
+  bf16* tmp = nullptr;
+  {
+    void* v = nullptr;
+    cudaError_t r = cudaMalloc(&v, tmp_elems * 2);
+    if (r != cudaSuccess) return fail(e, ENG_ENOMEM, "cudaMalloc of the load scratch failed");
+    tmp = static_cast<bf16*>(v);
+  }
+  auto done = [&](int rc) {
+    cudaStreamSynchronize(e->stream);
+    cudaFree(tmp);
+    return rc;
+  };
+  int rc;
+#define LW(x)              \
+  do {                     \
+    rc = (x);              \
+    if (rc != ENG_OK) return done(rc); \
+  } while (0)
+
+  LW(dev_alloc(e, &e->embed, (size_t)V * H));
+  LW(copy_bf16(e, wm.get("model.embed_tokens.weight"), tmp, (int64_t)V * H, "model.embed_tokens.weight"));
+  if (launch_pack(tmp, e->embed, V, H, 0, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+  if (c.tie_embeddings) {
+    e->lm = e->embed;
+  } else {
+    LW(dev_alloc(e, &e->lm, (size_t)V * H));
+    cudaStreamSynchronize(e->stream);
+    LW(copy_bf16(e, wm.get("lm_head.weight"), tmp, (int64_t)V * H, "lm_head.weight"));
+    if (launch_pack(tmp, e->lm, V, H, 0, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+  }
+  LW(dev_alloc(e, &e->final_norm, H));
+  cudaStreamSynchronize(e->stream);
+  LW(load_f32(e, wm.get("model.norm.weight"), e->final_norm, H, tmp, "model.norm.weight"));
+
+  e->layers.resize(c.layers);
+  for (int l = 0; l < c.layers; ++l) {
+    Layer& L = e->layers[l];
+    const std::string p = "model.layers." + std::to_string(l) + ".";
+    auto nm = [&](const char* s) { return p + s; };
+    cudaStreamSynchronize(e->stream);
+    // fused QKV: rows [q | k | v] ("33. Removing overhead", section "Fewer, larger matmuls")
+    LW(dev_alloc(e, &L.qkv, (size_t)QKV * H));
+    LW(copy_bf16(e, wm.get(nm("self_attn.q_proj.weight")), tmp, (int64_t)Hq * d * H, nm("self_attn.q_proj.weight").c_str()));
+    LW(copy_bf16(e, wm.get(nm("self_attn.k_proj.weight")), tmp + (size_t)Hq * d * H, (int64_t)Hkv * d * H,
+                 nm("self_attn.k_proj.weight").c_str()));
+    LW(copy_bf16(e, wm.get(nm("self_attn.v_proj.weight")), tmp + (size_t)(Hq + Hkv) * d * H, (int64_t)Hkv * d * H,
+                 nm("self_attn.v_proj.weight").c_str()));
+    if (launch_pack(tmp, L.qkv, QKV, H, 0, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+    if (c.qkv_bias) {
+      LW(dev_alloc(e, &L.qkv_bias, QKV));
+      cudaStreamSynchronize(e->stream);
+      LW(load_f32(e, wm.get(nm("self_attn.q_proj.bias")), L.qkv_bias, Hq * d, tmp, nm("self_attn.q_proj.bias").c_str()));
+      cudaStreamSynchronize(e->stream);
+      LW(load_f32(e, wm.get(nm("self_attn.k_proj.bias")), L.qkv_bias + Hq * d, Hkv * d, tmp,
+                  nm("self_attn.k_proj.bias").c_str()));
+      cudaStreamSynchronize(e->stream);
+      LW(load_f32(e, wm.get(nm("self_attn.v_proj.bias")), L.qkv_bias + (Hq + Hkv) * d, Hkv * d, tmp,
+                  nm("self_attn.v_proj.bias").c_str()));
+    }
+    if (c.qk_norm) {
+      LW(dev_alloc(e, &L.q_norm, d));
+      LW(dev_alloc(e, &L.k_norm, d));
+      cudaStreamSynchronize(e->stream);
+      LW(load_f32(e, wm.get(nm("self_attn.q_norm.weight")), L.q_norm, d, tmp, nm("self_attn.q_norm.weight").c_str()));
+      cudaStreamSynchronize(e->stream);
+      LW(load_f32(e, wm.get(nm("self_attn.k_norm.weight")), L.k_norm, d, tmp, nm("self_attn.k_norm.weight").c_str()));
+    }
+    cudaStreamSynchronize(e->stream);
+    LW(dev_alloc(e, &L.o, (size_t)H * Hq * d));
+    LW(copy_bf16(e, wm.get(nm("self_attn.o_proj.weight")), tmp, (int64_t)H * Hq * d, nm("self_attn.o_proj.weight").c_str()));
+    if (launch_pack(tmp, L.o, H, Hq * d, 0, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+    cudaStreamSynchronize(e->stream);
+    // fused gate|up, interleaved per 16-row tile for the SiLU epilogue
+    LW(dev_alloc(e, &L.gu, (size_t)2 * I * H));
+    LW(copy_bf16(e, wm.get(nm("mlp.gate_proj.weight")), tmp, (int64_t)I * H, nm("mlp.gate_proj.weight").c_str()));
+    LW(copy_bf16(e, wm.get(nm("mlp.up_proj.weight")), tmp + (size_t)I * H, (int64_t)I * H, nm("mlp.up_proj.weight").c_str()));
+    if (launch_pack(tmp, L.gu, 2 * I, H, I, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+    cudaStreamSynchronize(e->stream);
+    LW(dev_alloc(e, &L.down, (size_t)H * I));
+    LW(copy_bf16(e, wm.get(nm("mlp.down_proj.weight")), tmp, (int64_t)H * I, nm("mlp.down_proj.weight").c_str()));
+    if (launch_pack(tmp, L.down, H, I, 0, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+    LW(dev_alloc(e, &L.in_norm, H));
+    LW(dev_alloc(e, &L.post_norm, H));
+    cudaStreamSynchronize(e->stream);
+    LW(load_f32(e, wm.get(nm("input_layernorm.weight")), L.in_norm, H, tmp, nm("input_layernorm.weight").c_str()));
+    cudaStreamSynchronize(e->stream);
+    LW(load_f32(e, wm.get(nm("post_attention_layernorm.weight")), L.post_norm, H, tmp,
+                nm("post_attention_layernorm.weight").c_str()));
+  }
+#undef LW
+  if (cudaStreamSynchronize(e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "weight load failed"));
+  return done(ENG_OK);
+}
+
+// ------------------------------------------------------------------ buffers
+
+static int setup_buffers(eng_t* e) {
+  const eng_config_t& c = e->c;
+  const int Tm = c.max_tokens, Rm = c.max_reqs, H = c.hidden, d = c.head_dim;
+  const int QKV = (c.q_heads + 2 * c.kv_heads) * d;
+
+  // RoPE table in float64, stored as float32: angle = pos * theta^(-2i/d)
+  e->max_pos = c.max_blocks_per_seq * 16;
+  {
+    std::vector<float> tab((size_t)e->max_pos * d);
+    for (int pos = 0; pos < e->max_pos; ++pos)
+      for (int i = 0; i < d / 2; ++i) {
+        const double inv = std::pow(c.rope_theta, -2.0 * i / d);
+        const double ang = (double)pos * inv;
+        tab[((size_t)pos * (d / 2) + i) * 2] = (float)std::cos(ang);
+        tab[((size_t)pos * (d / 2) + i) * 2 + 1] = (float)std::sin(ang);
+      }
+    TRY(dev_alloc(e, &e->rope, tab.size()));
+    CUDA_OR_FAIL(e, cudaMemcpy(e->rope, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice));
+  }
+
+  e->kv_elems = (size_t)c.layers * 2 * (size_t)(c.num_blocks + 1) * c.kv_heads * 16 * d;
+  TRY(dev_alloc(e, &e->kv, e->kv_elems));
+
+  // input layout (int32 words); block tables last so a step copies only the rows it uses
+  e->max_items = Tm / 64 + Rm + 1;
+  InLayout& L = e->in;
+  size_t o = 0;
+  L.ids = o; o += Tm;
+  L.pos = o; o += Tm;
+  L.tok2req = o; o += Tm;
+  L.cu = o; o += Rm + 1;
+  L.seq = o; o += Rm;
+  L.last = o; o += Rm;
+  L.invt = o; o += Rm;
+  L.rng = o; o += 4;
+  L.wlog = o; o += 4;
+  o = (o + 3) & ~(size_t)3;
+  L.items = o; o += (size_t)4 * e->max_items;
+  L.bt = o; o += (size_t)Rm * c.max_blocks_per_seq;
+  L.words = o;
+  TRY(dev_alloc(e, &e->d_in, L.words));
+  for (int i = 0; i < kSlots; ++i) {
+    void* hp = nullptr;
+    if (cudaMallocHost(&hp, L.words * 4) != cudaSuccess) return fail(e, ENG_ENOMEM, "cudaMallocHost failed");
+    memset(hp, 0, L.words * 4);
+    e->h_in[i] = static_cast<int*>(hp);
+    CUDA_OR_FAIL(e, cudaEventCreateWithFlags(&e->ev[i], cudaEventDisableTiming));
+  }
+
+  TRY(dev_alloc(e, &e->h, (size_t)Tm * H));
+  TRY(dev_alloc(e, &e->y, (size_t)Tm * H));
+  TRY(dev_alloc(e, &e->qkv, (size_t)Tm * QKV));
+  TRY(dev_alloc(e, &e->q, (size_t)Tm * c.q_heads * d));
+  TRY(dev_alloc(e, &e->attn, (size_t)Tm * c.q_heads * d));
+  TRY(dev_alloc(e, &e->act, (size_t)Tm * c.intermediate));
+  TRY(dev_alloc(e, &e->ylast, (size_t)Rm * H));
+  TRY(dev_alloc(e, &e->logits, (size_t)Rm * c.vocab));
+  TRY(dev_alloc(e, &e->ids, Rm));
+  TRY(dev_alloc(e, &e->slots, Tm));
+  TRY(dev_alloc(e, &e->best, Rm));
+  TRY(dev_alloc(e, &e->done_counter, 4));
+  TRY(dev_alloc(e, &e->status, 4));
+
+  auto site = [&](GemmSite& s, int N, int K, int T) -> int {
+    s.N = N;
+    s.K = K;
+    gemm_plan(N, K, &s.RG, &s.S, &s.ktn);
+    return dev_alloc(e, &s.tickets, gemm_tickets(N, K, T) + 1);
+  };
+  TRY(site(e->g_qkv, QKV, H, Tm));
+  TRY(site(e->g_o, H, c.q_heads * d, Tm));
+  TRY(site(e->g_gu, 2 * c.intermediate, H, Tm));
+  TRY(site(e->g_down, H, c.intermediate, Tm));
+  TRY(site(e->g_lm, c.vocab, H, Rm));
+  size_t ws = 0;
+  ws = std::max(ws, gemm_ws_floats(QKV, H, Tm));
+  ws = std::max(ws, gemm_ws_floats(H, c.q_heads * d, Tm));
+  ws = std::max(ws, gemm_ws_floats(2 * c.intermediate, H, Tm));
+  ws = std::max(ws, gemm_ws_floats(H, c.intermediate, Tm));
+  ws = std::max(ws, gemm_ws_floats(c.vocab, H, Rm));
+  TRY(dev_alloc(e, &e->gemm_ws, ws + 4));
+
+  // decode attention splits: 16-key blocks per split chosen from the block-table width so that a row
+  // never needs more than 32 splits; fixed per engine, so eager and replayed steps agree bit for bit
+  e->split_blocks = std::max(4, (c.max_blocks_per_seq + 31) / 32);
+  e->max_splits = (c.max_blocks_per_seq + e->split_blocks - 1) / e->split_blocks;
+  TRY(dev_alloc(e, &e->attn_ws, attn_decode_ws_floats(Rm, c.q_heads, c.kv_heads, d, e->max_splits)));
+  TRY(dev_alloc(e, &e->attn_tickets, (size_t)Rm * c.kv_heads));
+
+  e->used.assign(c.num_blocks, 0);
+  e->free_list.clear();
+  for (int b = 0; b < c.num_blocks; ++b) e->free_list.push_back(b);
+  return ENG_OK;
+}
+
+// ------------------------------------------------------------------ the step's kernel sequence
+
+static cudaError_t gemm(eng_t* e, const GemmSite& s, const bf16* W, const bf16* X, int T, int epi, cudaStream_t st,
+                        float* out_f32 = nullptr, const float* bias = nullptr, float* resid = nullptr,
+                        bf16* out_bf16 = nullptr) {
+  GemmParams p{};
+  p.W = W;
+  p.X = X;
+  p.ldx = s.K;
+  p.T = T;
+  p.N = s.N;
+  p.K = s.K;
+  p.RG = s.RG;
+  p.S = s.S;
+  p.kt_per_split = s.ktn;
+  p.ws = e->gemm_ws;
+  p.tickets = s.tickets;
+  p.out_f32 = out_f32;
+  p.ldo = s.N;
+  p.bias = bias;
+  p.resid = resid;
+  p.out_bf16 = out_bf16;
+  const int* in = e->d_in;
+  p.logits = e->logits;
+  p.write_logits = in + e->in.wlog;
+  p.inv_temp = reinterpret_cast<const float*>(in + e->in.invt);
+  p.rng = reinterpret_cast<const uint32_t*>(in + e->in.rng);
+  p.best = e->best;
+  p.done_counter = e->done_counter;
+  p.out_ids = e->ids;
+  p.status = e->status;
+  LaunchOpts o;
+  o.pdl = e->pdl;
+  e->launches++;
+  return launch_gemm(p, epi, o, st);
+}
+
+// Enqueues one forward over T packed tokens of R requests; requests [0, P) go to the packed prefill
+// kernel (n_items work items), [P, R) to the decode kernel with `splits` splits per row.
+static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, int splits, cudaStream_t st) {
+  const eng_config_t& c = e->c;
+  const int H = c.hidden, d = c.head_dim, Hq = c.q_heads, Hkv = c.kv_heads;
+  const int* in = e->d_in;
+  const size_t plane = (size_t)(c.num_blocks + 1) * Hkv * 16 * d;
+  LaunchOpts o;
+  o.pdl = e->pdl;
+  cudaError_t r;
+
+  NormParams np{};
+  np.H = H;
+  np.V = c.vocab;
+  np.eps = c.rms_eps;
+  np.status = e->status;
+  np.rows = T;
+  np.h_out = e->h;
+  np.embed = e->embed;
+  np.ids = in + e->in.ids;
+  np.w = e->layers[0].in_norm;
+  np.y = e->y;
+  e->launches++;
+  if ((r = launch_rmsnorm(np, true, o, st)) != cudaSuccess) return r;
+
+  for (int l = 0; l < c.layers; ++l) {
+    const Layer& L = e->layers[l];
+    if (l > 0) {
+      NormParams n2{};
+      n2.h_in = e->h;
+      n2.w = L.in_norm;
+      n2.y = e->y;
+      n2.rows = T;
+      n2.H = H;
+      n2.V = c.vocab;
+      n2.eps = c.rms_eps;
+      n2.status = e->status;
+      e->launches++;
+      if ((r = launch_rmsnorm(n2, false, o, st)) != cudaSuccess) return r;
+    }
+    if ((r = gemm(e, e->g_qkv, L.qkv, e->y, T, EPI_STORE_F32, st, e->qkv, L.qkv_bias)) != cudaSuccess) return r;
+
+    bf16* kplane = e->kv + (size_t)l * 2 * plane;
+    bf16* vplane = kplane + plane;
+    RopeKvParams rp{};
+    rp.qkv = e->qkv;
+    rp.positions = in + e->in.pos;
+    rp.tok2req = in + e->in.tok2req;
+    rp.seq_lens = in + e->in.seq;
+    rp.bt = in + e->in.bt;
+    rp.mbs = c.max_blocks_per_seq;
+    rp.q_norm = L.q_norm;
+    rp.k_norm = L.k_norm;
+    rp.cos_sin = e->rope;
+    rp.max_pos = e->max_pos;
+    rp.q_out = e->q;
+    rp.k_pool = kplane;
+    rp.v_pool = vplane;
+    rp.slots = e->slots;
+    rp.T = T;
+    rp.Hq = Hq;
+    rp.Hkv = Hkv;
+    rp.d = d;
+    rp.NB = c.num_blocks;
+    rp.eps = c.rms_eps;
+    rp.status = e->status;
+    e->launches++;
+    if ((r = launch_rope_kv(rp, o, st)) != cudaSuccess) return r;
+
+    const float scale_log2 = 1.4426950408889634f / sqrtf((float)d);
+    if (P > 0) {
+      AttnPrefillParams ap{};
+      ap.q = e->q;
+      ap.k_pool = kplane;
+      ap.v_pool = vplane;
+      ap.bt = in + e->in.bt;
+      ap.mbs = c.max_blocks_per_seq;
+      ap.positions = in + e->in.pos;
+      ap.items = reinterpret_cast<const int4*>(in + e->in.items);
+      ap.n_items = n_items;
+      ap.out = e->attn;
+      ap.Hq = Hq;
+      ap.Hkv = Hkv;
+      ap.d = d;
+      ap.NB = c.num_blocks;
+      ap.scale_log2 = scale_log2;
+      ap.status = e->status;
+      e->launches++;
+      if ((r = launch_attn_prefill(ap, o, st)) != cudaSuccess) return r;
+    }
+    if (R > P) {
+      AttnDecodeParams dp{};
+      dp.q = e->q;
+      dp.k_pool = kplane;
+      dp.v_pool = vplane;
+      dp.bt = in + e->in.bt;
+      dp.mbs = c.max_blocks_per_seq;
+      dp.seq_lens = in + e->in.seq;
+      dp.cu = in + e->in.cu;
+      dp.r0 = P;
+      dp.rows = R - P;
+      dp.out = e->attn;
+      dp.ws = e->attn_ws;
+      dp.tickets = e->attn_tickets;
+      dp.Hq = Hq;
+      dp.Hkv = Hkv;
+      dp.d = d;
+      dp.NB = c.num_blocks;
+      dp.split_blocks = e->split_blocks;
+      dp.max_splits = splits;
+      dp.scale_log2 = scale_log2;
+      dp.status = e->status;
+      e->launches++;
+      if ((r = launch_attn_decode(dp, o, st)) != cudaSuccess) return r;
+    }
+    if ((r = gemm(e, e->g_o, L.o, e->attn, T, EPI_RESID, st, nullptr, nullptr, e->h)) != cudaSuccess) return r;
+
+    NormParams n3{};
+    n3.h_in = e->h;
+    n3.w = L.post_norm;
+    n3.y = e->y;
+    n3.rows = T;
+    n3.H = H;
+    n3.V = c.vocab;
+    n3.eps = c.rms_eps;
+    n3.status = e->status;
+    e->launches++;
+    if ((r = launch_rmsnorm(n3, false, o, st)) != cudaSuccess) return r;
+    if ((r = gemm(e, e->g_gu, L.gu, e->y, T, EPI_SILU, st, nullptr, nullptr, nullptr, e->act)) != cudaSuccess) return r;
+    if ((r = gemm(e, e->g_down, L.down, e->act, T, EPI_RESID, st, nullptr, nullptr, e->h)) != cudaSuccess) return r;
+  }
+
+  NormParams nf{};
+  nf.h_in = e->h;
+  nf.row_index = in + e->in.last;
+  nf.w = e->final_norm;
+  nf.y = e->ylast;
+  nf.rows = R;
+  nf.H = H;
+  nf.V = c.vocab;
+  nf.eps = c.rms_eps;
+  nf.status = e->status;
+  e->launches++;
+  if ((r = launch_rmsnorm(nf, false, o, st)) != cudaSuccess) return r;
+  return gemm(e, e->g_lm, e->lm, e->ylast, R, EPI_LMHEAD, st);
+}
+
+// ------------------------------------------------------------------ staging
+
+static float inv_temperature(float T) { return T == 0.f ? 0.f : 1.0f / T; }
+
+// Waits (rarely) for the copy that last used this staging slot, then returns it cleared.
+static int* take_slot(eng_t* e, int* slot_index) {
+  const int k = e->slot;
+  e->slot = (e->slot + 1) % kSlots;
+  cudaEventSynchronize(e->ev[k]);
+  *slot_index = k;
+  return e->h_in[k];
+}
+
+static int push_slot(eng_t* e, int k, size_t words) {
+  CUDA_OR_FAIL(e, cudaMemcpyAsync(e->d_in, e->h_in[k], words * 4, cudaMemcpyHostToDevice, e->stream));
+  CUDA_OR_FAIL(e, cudaEventRecord(e->ev[k], e->stream));
+  return ENG_OK;
+}
+
+// Fills a staging slot with a decode-only batch of `size` padding rows (capture and warm-up).
+static void stage_padding(eng_t* e, int* h, int size) {
+  const InLayout& L = e->in;
+  for (int i = 0; i < size; ++i) {
+    h[L.ids + i] = 0;
+    h[L.pos + i] = 0;
+    h[L.tok2req + i] = i;
+    h[L.seq + i] = 0;
+    h[L.last + i] = i;
+    reinterpret_cast<float*>(h)[L.invt + i] = 0.f;
+  }
+  for (int i = 0; i <= size; ++i) h[L.cu + i] = i;
+  h[L.rng + 0] = h[L.rng + 1] = h[L.rng + 2] = h[L.rng + 3] = 0;
+  h[L.wlog] = 0;
+}
+
+// ------------------------------------------------------------------ C ABI
+
+extern "C" {
+
+int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_weights, void* cuda_stream, eng_t** out) {
+  if (!out) return fail(nullptr, ENG_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!cfg || (!weights && n_weights > 0) || n_weights < 0) return fail(nullptr, ENG_EINVAL, "null config or weights");
+  const std::string why = check_config(*cfg);
+  if (!why.empty()) return fail(nullptr, ENG_EINVAL, why);
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0)
+    return fail(nullptr, ENG_ECUDA, "no CUDA device: the engine has no CPU path");
+  eng_t* e = new eng_t();
+  e->c = *cfg;
+  cudaGetDevice(&e->device);
+  int rc = ENG_OK;
+  if (cuda_stream) {
+    e->stream = static_cast<cudaStream_t>(cuda_stream);
+  } else {
+    if (cudaStreamCreateWithFlags(&e->stream, cudaStreamNonBlocking) != cudaSuccess) rc = ENG_ECUDA;
+    e->own_stream = true;
+  }
+  if (rc == ENG_OK && cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking) != cudaSuccess) rc = ENG_ECUDA;
+  if (rc == ENG_OK) rc = setup_buffers(e);
+  if (rc == ENG_OK) rc = load_weights(e, weights, n_weights);
+  if (rc == ENG_OK && cudaDeviceSynchronize() != cudaSuccess) rc = fail(e, ENG_ECUDA, "device error after load");
+  if (rc != ENG_OK) {
+    g_create_error = e->err.empty() ? g_create_error : e->err;
+    eng_destroy(e);
+    return rc;
+  }
+  *out = e;
+  return ENG_OK;
+}
+
+void eng_destroy(eng_t* e) {
+  if (!e) return;
+  if (e->stream) cudaStreamSynchronize(e->stream);
+  for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
+  for (int i = 0; i < kSlots; ++i) {
+    if (e->ev[i]) cudaEventDestroy(e->ev[i]);
+    if (e->h_in[i]) cudaFreeHost(e->h_in[i]);
+  }
+  for (void* p : e->allocations) cudaFree(p);
+  if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
+  if (e->own_stream && e->stream) cudaStreamDestroy(e->stream);
+  delete e;
+}
+
+const char* eng_last_error(const eng_t* e) { return e ? e->err.c_str() : g_create_error.c_str(); }
+
+void* eng_stream(const eng_t* e) { return e ? static_cast<void*>(e->stream) : nullptr; }
+
+int eng_set_eager(eng_t* e, int32_t eager) {
+  if (!e) return ENG_EINVAL;
+  e->eager_only = eager != 0;
+  return ENG_OK;
+}
+
+int eng_kv_pool(eng_t* e, void** dev_ptr, int64_t* bytes) {
+  if (!e || !dev_ptr || !bytes) return ENG_EINVAL;
+  *dev_ptr = e->kv;
+  *bytes = (int64_t)e->kv_elems * 2;
+  return ENG_OK;
+}
+
+int eng_debug_buffer(eng_t* e, const char* name, void** dev_ptr, int64_t* bytes) {
+  if (!e || !name || !dev_ptr || !bytes) return ENG_EINVAL;
+  const eng_config_t& c = e->c;
+  const std::string n(name);
+  if (n == "hidden") {
+    *dev_ptr = e->h;
+    *bytes = (int64_t)c.max_tokens * c.hidden * 4;
+  } else if (n == "slots") {
+    *dev_ptr = e->slots;
+    *bytes = (int64_t)c.max_tokens * 4;
+  } else if (n == "logits") {
+    *dev_ptr = e->logits;
+    *bytes = (int64_t)c.max_reqs * c.vocab * 4;
+  } else if (n == "ids") {
+    *dev_ptr = e->ids;
+    *bytes = (int64_t)c.max_reqs * 4;
+  } else {
+    return fail(e, ENG_EINVAL, "unknown debug buffer " + n);
+  }
+  return ENG_OK;
+}
+
+int eng_status(eng_t* e, int32_t reset) {
+  if (!e) return ENG_EINVAL;
+  CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+  int st = 0;
+  CUDA_OR_FAIL(e, cudaMemcpy(&st, e->status, 4, cudaMemcpyDeviceToHost));
+  if (reset) CUDA_OR_FAIL(e, cudaMemset(e->status, 0, 4));
+  return st;
+}
+
+int eng_pool_alloc(eng_t* e, int32_t n, int32_t* out_ids) {
+  if (!e || n < 0 || (n > 0 && !out_ids)) return e ? fail(e, ENG_EINVAL, "bad pool_alloc arguments") : ENG_EINVAL;
+  if ((size_t)n > e->free_list.size())
+    return fail(e, ENG_EPOOL, "KV pool exhausted: " + std::to_string(n) + " blocks requested, " +
+                                  std::to_string(e->free_list.size()) + " free");
+  for (int i = 0; i < n; ++i) {
+    const int b = e->free_list.front();
+    e->free_list.pop_front();
+    e->used[b] = 1;
+    out_ids[i] = b;
+  }
+  return ENG_OK;
+}
+
+int eng_pool_free(eng_t* e, const int32_t* ids, int32_t n) {
+  if (!e || n < 0 || (n > 0 && !ids)) return e ? fail(e, ENG_EINVAL, "bad pool_free arguments") : ENG_EINVAL;
+  std::vector<uint8_t> seen(e->c.num_blocks, 0);
+  for (int i = 0; i < n; ++i) {
+    const int b = ids[i];
+    if (b < 0 || b >= e->c.num_blocks || !e->used[b] || seen[b])
+      return fail(e, ENG_EINVAL, "block " + std::to_string(b) + " is not allocated");
+    seen[b] = 1;
+  }
+  for (int i = 0; i < n; ++i) {
+    e->used[ids[i]] = 0;
+    e->free_list.push_back(ids[i]);
+  }
+  return ENG_OK;
+}
+
+int32_t eng_pool_free_count(const eng_t* e) { return e ? (int32_t)e->free_list.size() : 0; }
+
+int eng_last_step_info(const eng_t* e, eng_step_info_t* info) {
+  if (!e || !info) return ENG_EINVAL;
+  *info = e->last;
+  return ENG_OK;
+}
+
+int eng_capture(eng_t* e, const int32_t* sizes, int32_t n) {
+  if (!e || !sizes || n < 1) return e ? fail(e, ENG_EINVAL, "bad capture sizes") : ENG_EINVAL;
+  std::vector<int> v(sizes, sizes + n);
+  std::sort(v.begin(), v.end());
+  for (size_t i = 0; i < v.size(); ++i) {
+    if (v[i] < 1 || v[i] > e->c.max_reqs) return fail(e, ENG_EINVAL, "capture size outside [1, max_reqs]");
+    if (i && v[i] == v[i - 1]) return fail(e, ENG_EINVAL, "duplicate capture size");
+  }
+  CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+  for (auto it = v.rbegin(); it != v.rend(); ++it) {  // largest first
+    const int size = *it;
+    if (e->graphs.count(size)) {
+      cudaGraphExecDestroy(e->graphs[size]);
+      e->graphs.erase(size);
+    }
+    int k;
+    int* h = take_slot(e, &k);
+    stage_padding(e, h, size);
+    TRY(push_slot(e, k, e->in.words));
+    // warm up on the engine stream (lazy attribute setup, first-touch), then record on a side stream
+    for (int w = 0; w < 2; ++w) {
+      e->launches = 0;
+      CUDA_OR_FAIL(e, enqueue_forward(e, size, size, 0, 0, e->max_splits, e->stream));
+    }
+    CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+    cudaGraph_t graph = nullptr;
+    CUDA_OR_FAIL(e, cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal));
+    e->launches = 0;
+    const cudaError_t le = enqueue_forward(e, size, size, 0, 0, e->max_splits, e->cap_stream);
+    const cudaError_t ce = cudaStreamEndCapture(e->cap_stream, &graph);
+    if (le != cudaSuccess || ce != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      return fail(e, ENG_ECUDA, std::string("graph capture failed: ") + cudaGetErrorString(le != cudaSuccess ? le : ce));
+    }
+    cudaGraphExec_t exec = nullptr;
+    const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) return fail(e, ENG_ECUDA, std::string("graph instantiate failed: ") + cudaGetErrorString(ie));
+    e->graphs[size] = exec;
+    e->graph_launches[size] = e->launches;
+  }
+  CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+  return ENG_OK;
+}
+
+int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_logits_dev) {
+  if (!e) return ENG_EINVAL;
+  if (!s || !out_ids_dev) return fail(e, ENG_EINVAL, "null step or out_ids");
+  const eng_config_t& c = e->c;
+  const int T = s->num_tokens, R = s->num_reqs, bs = s->bt_stride;
+  if (R < 1 || R > c.max_reqs) return fail(e, ENG_EINVAL, "num_reqs outside [1, max_reqs]");
+  if (T < R || T > c.max_tokens) return fail(e, ENG_EINVAL, "num_tokens outside [num_reqs, max_tokens]");
+  if (bs < 1 || bs > c.max_blocks_per_seq) return fail(e, ENG_EINVAL, "bt_stride outside [1, max_blocks_per_seq]");
+  if (!s->token_ids || !s->positions || !s->cu_seqlens || !s->block_tables || !s->seq_lens || !s->temperature)
+    return fail(e, ENG_EINVAL, "null step array");
+  const int32_t* cu = s->cu_seqlens;
+  if (cu[0] != 0 || cu[R] != T) return fail(e, ENG_EINVAL, "cu_seqlens must start at 0 and end at num_tokens");
+  int P = 0;
+  bool seen_decode = false;
+  for (int r = 0; r < R; ++r) {
+    const int ql = cu[r + 1] - cu[r];
+    if (ql < 1) return fail(e, ENG_EINVAL, "every request needs at least one token");
+    if (ql > 1) {
+      if (seen_decode) return fail(e, ENG_EINVAL, "multi-token (prefill) requests must precede single-token ones");
+      P = r + 1;
+    } else {
+      seen_decode = true;
+    }
+    const int sl = s->seq_lens[r];
+    if (sl < ql) return fail(e, ENG_EINVAL, "seq_len smaller than the request's token count");
+    if (sl > c.max_blocks_per_seq * 16)
+      return fail(e, ENG_ECAPACITY, "sequence of " + std::to_string(sl) + " positions exceeds the engine capacity of " +
+                                        std::to_string(c.max_blocks_per_seq * 16));
+    if ((sl + 15) / 16 > bs) return fail(e, ENG_EINVAL, "block table row shorter than the sequence");
+    for (int i = 0; i < ql; ++i) {
+      if (s->positions[cu[r] + i] != sl - ql + i)
+        return fail(e, ENG_EINVAL, "positions of a request must be consecutive and end at seq_len - 1");
+      const int id = s->token_ids[cu[r] + i];
+      if (id < 0 || id >= c.vocab) return fail(e, ENG_EINVAL, "token id outside [0, vocab)");
+    }
+    for (int b = 0; b < (sl + 15) / 16; ++b) {
+      const int blk = s->block_tables[(size_t)r * bs + b];
+      if (blk < 0 || blk >= c.num_blocks) return fail(e, ENG_EINVAL, "block id outside [0, num_blocks)");
+    }
+    const float tp = s->temperature[r];
+    if (!(tp >= 0.f) || !std::isfinite(tp)) return fail(e, ENG_EINVAL, "temperature must be finite and >= 0");
+  }
+
+  const bool decode_only = (T == R);
+  int bucket = 0;
+  if (decode_only && !e->eager_only) {
+    for (auto& kv : e->graphs)
+      if (kv.first >= R) {
+        bucket = kv.first;
+        break;
+      }
+  }
+  const bool replay = bucket > 0;
+  const int rows = replay ? bucket : R;  // rows staged (padding included)
+
+  int k;
+  int* h = take_slot(e, &k);
+  const InLayout& L = e->in;
+  float* hf = reinterpret_cast<float*>(h);
+  for (int t = 0; t < T; ++t) {
+    h[L.ids + t] = s->token_ids[t];
+    h[L.pos + t] = s->positions[t];
+  }
+  for (int r = 0; r < R; ++r) {
+    for (int t = cu[r]; t < cu[r + 1]; ++t) h[L.tok2req + t] = r;
+    h[L.cu + r] = cu[r];
+    h[L.seq + r] = s->seq_lens[r];
+    h[L.last + r] = cu[r + 1] - 1;
+    hf[L.invt + r] = inv_temperature(s->temperature[r]);
+    int* row = h + L.bt + (size_t)r * c.max_blocks_per_seq;
+    memcpy(row, s->block_tables + (size_t)r * bs, (size_t)bs * 4);
+    if (bs < c.max_blocks_per_seq) memset(row + bs, 0, (size_t)(c.max_blocks_per_seq - bs) * 4);
+  }
+  h[L.cu + R] = T;
+  for (int r = R; r < rows; ++r) {  // bucket padding: token 0, position 0, length 0
+    h[L.ids + r] = 0;
+    h[L.pos + r] = 0;
+    h[L.tok2req + r] = r;
+    h[L.cu + r + 1] = r + 1;
+    h[L.seq + r] = 0;
+    h[L.last + r] = r;
+    hf[L.invt + r] = 0.f;
+  }
+  h[L.rng + 0] = (int)(uint32_t)s->seed;
+  h[L.rng + 1] = (int)(uint32_t)(s->seed >> 32);
+  h[L.rng + 2] = (int)(uint32_t)s->offset;
+  h[L.rng + 3] = (int)(uint32_t)(s->offset >> 32);
+  h[L.wlog] = out_logits_dev ? 1 : 0;
+
+  // prefill work items: (request, first token, count <= 64)
+  int n_items = 0;
+  for (int r = 0; r < P; ++r)
+    for (int t0 = cu[r]; t0 < cu[r + 1]; t0 += 64) {
+      int* it = h + L.items + 4 * n_items;
+      it[0] = r;
+      it[1] = t0;
+      it[2] = std::min(64, cu[r + 1] - t0);
+      it[3] = 0;
+      ++n_items;
+    }
+  if (n_items > e->max_items) return fail(e, ENG_EINVAL, "too many prefill work items");
+
+  const size_t words = L.bt + (size_t)R * c.max_blocks_per_seq;
+  TRY(push_slot(e, k, words));
+
+  e->launches = 0;
+  if (replay) {
+    CUDA_OR_FAIL(e, cudaGraphLaunch(e->graphs[bucket], e->stream));
+    e->launches = e->graph_launches[bucket];
+  } else {
+    int max_blocks = 1;
+    for (int r = P; r < R; ++r) max_blocks = std::max(max_blocks, (s->seq_lens[r] + 15) / 16);
+    const int splits = (max_blocks + e->split_blocks - 1) / e->split_blocks;
+    CUDA_OR_FAIL(e, enqueue_forward(e, T, R, P, n_items, splits, e->stream));
+  }
+  CUDA_OR_FAIL(e, cudaMemcpyAsync(out_ids_dev, e->ids, (size_t)R * 4, cudaMemcpyDeviceToDevice, e->stream));
+  if (out_logits_dev)
+    CUDA_OR_FAIL(e, cudaMemcpyAsync(out_logits_dev, e->logits, (size_t)R * c.vocab * 4, cudaMemcpyDeviceToDevice,
+                                    e->stream));
+  e->last.replayed = replay ? 1 : 0;
+  e->last.bucket = rows;
+  e->last.launches = e->launches;
+  e->last.num_prefill = P;
+  e->last.h2d_bytes = (int64_t)words * 4;
+  return ENG_OK;
+}
+
+// ------------------------------------------------------------------ standalone kernels
+
+int eng_philox_uniforms(uint64_t seed, uint64_t offset, int32_t rows, int32_t vocab, float* out_dev, void* stream) {
+  if (rows < 0 || vocab < 0 || (!out_dev && rows * (int64_t)vocab > 0)) return ENG_EINVAL;
+  return launch_philox_uniforms(seed, offset, rows, vocab, out_dev, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ENG_OK
+             : ENG_ECUDA;
+}
+
+int eng_gumbel(const float* u_dev, float* g_dev, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!u_dev || !g_dev))) return ENG_EINVAL;
+  return launch_gumbel(u_dev, g_dev, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ENG_OK : ENG_ECUDA;
+}
+
+int eng_sample(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature, uint64_t seed,
+               uint64_t offset, int32_t* out_ids_dev, void* stream) {
+  if (rows < 0 || vocab < 1 || (rows > 0 && (!logits_dev || !temperature || !out_ids_dev))) return ENG_EINVAL;
+  if (rows == 0) return ENG_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // small per-call device block: [inv_temp rows][rng 4]
+  std::vector<uint32_t> hbuf((size_t)rows + 4);
+  for (int r = 0; r < rows; ++r) {
+    if (!(temperature[r] >= 0.f) || !std::isfinite(temperature[r])) return ENG_EINVAL;
+    const float it = inv_temperature(temperature[r]);
+    memcpy(&hbuf[r], &it, 4);
+  }
+  hbuf[rows + 0] = (uint32_t)seed;
+  hbuf[rows + 1] = (uint32_t)(seed >> 32);
+  hbuf[rows + 2] = (uint32_t)offset;
+  hbuf[rows + 3] = (uint32_t)(offset >> 32);
+  void* d = nullptr;
+  if (cudaMallocAsync(&d, hbuf.size() * 4, st) != cudaSuccess) return ENG_ENOMEM;
+  int rc = ENG_OK;
+  if (cudaMemcpyAsync(d, hbuf.data(), hbuf.size() * 4, cudaMemcpyHostToDevice, st) != cudaSuccess) rc = ENG_ECUDA;
+  const float* it = static_cast<const float*>(d);
+  const uint32_t* rng = static_cast<const uint32_t*>(d) + rows;
+  if (rc == ENG_OK && launch_sample(logits_dev, rows, vocab, it, rng, nullptr, out_ids_dev, nullptr, st) != cudaSuccess)
+    rc = ENG_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) rc = ENG_ECUDA;  // hbuf is pageable host memory
+  cudaFreeAsync(d, st);
+  return rc;
+}
+
+}  // extern "C"

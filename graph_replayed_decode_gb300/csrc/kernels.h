@@ -1,0 +1,144 @@
+// kernels.h -- internal launch interface between the engine (engine.cu) and the kernels.
+// Every launcher enqueues on `stream`, returns the launch's cudaError_t and never synchronises.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cuda_bf16.h>
+
+namespace grd {
+
+typedef __nv_bfloat16 bf16;
+
+// Launch options shared by all launchers: programmatic dependent launch on/off.
+struct LaunchOpts {
+  bool pdl = false;
+};
+
+// ------------------------------------------------------------------ weight packing (pack.cu)
+// dst (packed, see common.cuh) <- src row-major bf16 [N][K].  interleave_half: when > 0, the logical
+// rows are the concatenation [A (interleave_half rows); B (interleave_half rows)] and packed row tile i
+// holds A rows 8i..8i+7 then B rows 8i..8i+7 (gate|up for the fused SiLU epilogue).
+cudaError_t launch_pack(const bf16* src, bf16* dst, int N, int K, int interleave_half, cudaStream_t s);
+cudaError_t launch_bf16_to_f32(const bf16* src, float* dst, int64_t n, cudaStream_t s);
+
+// ------------------------------------------------------------------ norms (norm.cu)
+struct NormParams {
+  const float* h_in;     // residual rows [*, H] (ignored in embed mode)
+  float* h_out;          // embed mode: residual rows written here
+  const bf16* embed;     // embed mode: packed embedding [V][H]
+  const int* ids;        // embed mode: token ids [rows]
+  const int* row_index;  // optional gather: row i reads residual row row_index[i]
+  const float* w;        // norm weight [H]
+  bf16* y;               // output [rows][H]
+  int rows, H, V;
+  float eps;
+  int* status;
+};
+cudaError_t launch_rmsnorm(const NormParams& p, bool embed, const LaunchOpts& o, cudaStream_t s);
+
+// ------------------------------------------------------------------ skinny GEMM (gemm.cu)
+enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID = 1, EPI_SILU = 2, EPI_LMHEAD = 3 };
+
+struct GemmParams {
+  const bf16* W;   // packed [N][K]
+  const bf16* X;   // activations row-major [>= T][ldx] bf16
+  int ldx;
+  int T, N, K;
+  int RG;           // 16-row tiles per CTA (1, 2, 4, 8)
+  int S;            // k splits
+  int kt_per_split; // 32-column k tiles per split
+  float* ws;        // split-K partials
+  int* tickets;     // one per (row group, token chunk), zero between launches
+  // epilogues
+  float* out_f32;   // EPI_STORE_F32: out[t][n] (+ bias[n]), row stride ldo
+  int ldo;
+  const float* bias;
+  float* resid;     // EPI_RESID: resid[t][n] += v, row stride N
+  bf16* out_bf16;   // EPI_SILU: out[t][j] = silu(gate_j) * up_j, row stride N / 2
+  // EPI_LMHEAD: logits and sampling
+  float* logits;                // [T][N] when *write_logits != 0
+  const int* write_logits;      // device flag
+  const float* inv_temp;        // [T]; 0 = greedy
+  const uint32_t* rng;          // device [4]: seed_lo, seed_hi, offset_lo, offset_hi
+  unsigned long long* best;     // [T] packed (key, ~index), zero between launches
+  int* done_counter;            // counts finished CTAs, zero between launches
+  int* out_ids;                 // [T]
+  int* status;
+};
+// Picks RG / S / kt_per_split for an [N][K] weight (independent of T, so every token count computes
+// each output with the same summation order).
+void gemm_plan(int N, int K, int* RG, int* S, int* kt_per_split);
+size_t gemm_ws_floats(int N, int K, int T);
+int gemm_tickets(int N, int K, int T);
+cudaError_t launch_gemm(const GemmParams& p, int epi, const LaunchOpts& o, cudaStream_t s);
+
+// ------------------------------------------------------------------ QK-norm + RoPE + KV write (rope_kv.cu)
+struct RopeKvParams {
+  const float* qkv;       // [T][(Hq + 2 Hkv) d] projections (bias applied)
+  const int* positions;   // [T]
+  const int* tok2req;     // [T]
+  const int* seq_lens;    // [R]
+  const int* bt;          // [R][mbs]
+  int mbs;
+  const float* q_norm;    // [d] or null
+  const float* k_norm;    // [d] or null
+  const float* cos_sin;   // [max_pos][d/2][2] (cos, sin)
+  int max_pos;
+  bf16* q_out;            // [T][Hq][d]
+  bf16* k_pool;           // this layer's K plane [NB+1][Hkv][16][d]
+  bf16* v_pool;           // this layer's V plane
+  int* slots;             // [T] slot of each token, -1 for padding rows
+  int T, Hq, Hkv, d, NB;
+  float eps;
+  int* status;
+};
+cudaError_t launch_rope_kv(const RopeKvParams& p, const LaunchOpts& o, cudaStream_t s);
+
+// ------------------------------------------------------------------ attention (attn_decode.cu, attn_prefill.cu)
+struct AttnDecodeParams {
+  const bf16* q;          // [T][Hq][d]
+  const bf16* k_pool;     // layer K plane
+  const bf16* v_pool;     // layer V plane
+  const int* bt;          // [R][mbs]
+  int mbs;
+  const int* seq_lens;    // [R]
+  const int* cu;          // [R+1]: request r's query token is cu[r]
+  int r0;                 // first request handled (grid.x = rows)
+  int rows;
+  bf16* out;              // [T][Hq * d]
+  float* ws;              // split partials
+  int* tickets;           // [rows_max][Hkv]
+  int Hq, Hkv, d, NB;
+  int split_blocks;       // KV blocks per split
+  int max_splits;         // grid.z
+  float scale_log2;       // log2(e) / sqrt(d)
+  int* status;
+};
+size_t attn_decode_ws_floats(int rows, int Hq, int Hkv, int d, int max_splits);
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, cudaStream_t s);
+
+struct AttnPrefillParams {
+  const bf16* q;          // [T][Hq][d]
+  const bf16* k_pool;
+  const bf16* v_pool;
+  const int* bt;
+  int mbs;
+  const int* positions;   // [T]
+  const int4* items;      // work items: (request, first token, token count <= 64, unused)
+  int n_items;
+  bf16* out;              // [T][Hq * d]
+  int Hq, Hkv, d, NB;
+  float scale_log2;
+  int* status;
+};
+cudaError_t launch_attn_prefill(const AttnPrefillParams& p, const LaunchOpts& o, cudaStream_t s);
+
+// ------------------------------------------------------------------ sampler pieces (sample.cu)
+cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int vocab, float* out, cudaStream_t s);
+cudaError_t launch_gumbel(const float* u, float* g, int64_t n, cudaStream_t s);
+cudaError_t launch_sample(const float* logits, int rows, int vocab, const float* inv_temp, const uint32_t* rng,
+                          unsigned long long* best, int* out_ids, int* status, cudaStream_t s);
+
+}  // namespace grd

@@ -1,0 +1,82 @@
+// sample.cu -- standalone launches of the sampler arithmetic of sampling.cuh: the Philox uniforms, the
+// Gumbel transform and the greedy / Gumbel-max argmax over caller-provided logits.  The fused LM-head
+// epilogue (gemm.cu) uses the same device functions, so these launches let tests compare the GPU's
+// noise and log bit for bit with a CPU restatement.
+#include "common.cuh"
+#include "kernels.h"
+#include "sampling.cuh"
+
+namespace grd {
+
+__global__ void k_philox_uniforms(uint32_t s0, uint32_t s1, uint32_t o0, uint32_t o1, int rows, int vocab,
+                                  float* out) {
+  const int64_t n = (int64_t)rows * vocab;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / vocab), v = (int)(i % vocab);
+    out[i] = philox_uniform(s0, s1, o0, o1, (uint32_t)r, (uint32_t)v);
+  }
+}
+
+cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int vocab, float* out, cudaStream_t s) {
+  const int64_t n = (int64_t)rows * vocab;
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  k_philox_uniforms<<<(unsigned)blocks, 256, 0, s>>>((uint32_t)seed, (uint32_t)(seed >> 32), (uint32_t)offset,
+                                                      (uint32_t)(offset >> 32), rows, vocab, out);
+  return cudaGetLastError();
+}
+
+__global__ void k_gumbel(const float* u, float* g, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    g[i] = gumbel_from_uniform(u[i]);
+}
+
+cudaError_t launch_gumbel(const float* u, float* g, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  k_gumbel<<<(unsigned)blocks, 256, 0, s>>>(u, g, n);
+  return cudaGetLastError();
+}
+
+// One CTA per row: every thread scans a strided share of the vocabulary, then a fixed reduction tree.
+__global__ void __launch_bounds__(256) k_sample(const float* logits, int vocab, const float* inv_temp,
+                                                const uint32_t* rng_dev, int* out_ids, int* status) {
+  const int r = blockIdx.x;
+  const float it = inv_temp[r];
+  uint32_t rng[4] = {rng_dev[0], rng_dev[1], rng_dev[2], rng_dev[3]};
+  unsigned long long best = 0ull;
+  const float* z = logits + (size_t)r * vocab;
+  for (int v = threadIdx.x; v < vocab; v += blockDim.x) {
+    const float key = sample_key(z[v], it, rng, (uint32_t)r, (uint32_t)v);
+    if (key != key) {
+      set_status(status, ST_NAN);
+      continue;
+    }
+    const unsigned long long pk = pack_key_index(key, (uint32_t)v);
+    best = pk > best ? pk : best;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
+    best = x > best ? x : best;
+  }
+  __shared__ unsigned long long wb[8];
+  if ((threadIdx.x & 31) == 0) wb[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long b = 0ull;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) b = wb[w] > b ? wb[w] : b;
+    out_ids[r] = (int)unpack_index(b);
+  }
+}
+
+cudaError_t launch_sample(const float* logits, int rows, int vocab, const float* inv_temp, const uint32_t* rng,
+                          unsigned long long* /*best*/, int* out_ids, int* status, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  k_sample<<<rows, 256, 0, s>>>(logits, vocab, inv_temp, rng, out_ids, status);
+  return cudaGetLastError();
+}
+
+}  // namespace grd

@@ -1,0 +1,275 @@
+"""ctypes binding of libeng.so, one Python function per C entry point of include/eng.h.
+
+Argument marshalling only: every step of the forward runs in the library's CUDA
+kernels.  Loading fails loudly if the library has not been built (there is no
+CPU fallback).  Device pointers are plain integers (for example
+``torch.Tensor.data_ptr()``); host arrays are numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, Sequence
+
+import numpy as np
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeng.so")
+
+ENG_OK = 0
+ENG_EINVAL = -1
+ENG_ECAPACITY = -2
+ENG_ENOMEM = -3
+ENG_EPOOL = -4
+ENG_ECUDA = -5
+ENG_EDEVICE = -6
+ENG_ESTATE = -7
+
+ENG_STATUS_BAD_BLOCK = 1
+ENG_STATUS_BAD_POSITION = 2
+ENG_STATUS_NAN = 4
+ENG_STATUS_TIMEOUT = 8
+
+ENG_DTYPE_BF16 = 0
+ENG_DTYPE_F16 = 1
+ENG_DTYPE_F32 = 2
+
+
+class eng_config_t(ctypes.Structure):
+    _fields_ = [
+        ("layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("q_heads", ctypes.c_int32),
+        ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+        ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_double),
+        ("qk_norm", ctypes.c_int32), ("qkv_bias", ctypes.c_int32), ("tie_embeddings", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+        ("max_reqs", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+    ]
+
+
+class eng_tensor_t(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("data", ctypes.c_void_p), ("numel", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("on_device", ctypes.c_int32)]
+
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_F32P = ctypes.POINTER(ctypes.c_float)
+
+
+class eng_step_t(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_reqs", ctypes.c_int32), ("bt_stride", ctypes.c_int32),
+                ("token_ids", _I32P), ("positions", _I32P), ("cu_seqlens", _I32P), ("block_tables", _I32P),
+                ("seq_lens", _I32P), ("temperature", _F32P), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+
+
+class eng_step_info_t(ctypes.Structure):
+    _fields_ = [("replayed", ctypes.c_int32), ("bucket", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("num_prefill", ctypes.c_int32), ("h2d_bytes", ctypes.c_int64)]
+
+
+class EngError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+_lib = None
+
+# (name, restype, argtypes) of every entry point declared in include/eng.h
+SIGNATURES = [
+    ("eng_create", ctypes.c_int, [ctypes.POINTER(eng_config_t), ctypes.POINTER(eng_tensor_t), ctypes.c_int32,
+                                  ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
+    ("eng_capture", ctypes.c_int, [ctypes.c_void_p, _I32P, ctypes.c_int32]),
+    ("eng_step", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_t), ctypes.c_void_p, ctypes.c_void_p]),
+    ("eng_last_step_info", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_info_t)]),
+    ("eng_pool_alloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P]),
+    ("eng_pool_free", ctypes.c_int, [ctypes.c_void_p, _I32P, ctypes.c_int32]),
+    ("eng_pool_free_count", ctypes.c_int32, [ctypes.c_void_p]),
+    ("eng_status", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("eng_set_eager", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("eng_kv_pool", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int64)]),
+    ("eng_debug_buffer", ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_void_p),
+                                        ctypes.POINTER(ctypes.c_int64)]),
+    ("eng_stream", ctypes.c_void_p, [ctypes.c_void_p]),
+    ("eng_last_error", ctypes.c_char_p, [ctypes.c_void_p]),
+    ("eng_destroy", None, [ctypes.c_void_p]),
+    ("eng_philox_uniforms", ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_void_p, ctypes.c_void_p]),
+    ("eng_gumbel", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
+    ("eng_sample", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, _F32P, ctypes.c_uint64,
+                                  ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]),
+]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libeng.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built (python -m graph_replayed_decode_gb300.build); "
+                               "the engine has no CPU fallback")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(e, rc: int) -> int:
+    if rc < 0:
+        msg = lib().eng_last_error(e)
+        raise EngError(rc, msg.decode() if msg else "")
+    return rc
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr_i32(a: np.ndarray):
+    return a.ctypes.data_as(_I32P)
+
+
+# ------------------------------------------------------------------ marshalling helpers
+
+
+def make_config(shape, num_blocks: int, max_reqs: int, max_tokens: int, max_blocks_per_seq: int) -> eng_config_t:
+    """eng_config_t from a model shape (any object with the synth.ModelShape fields)."""
+    return eng_config_t(
+        layers=shape.layers, hidden=shape.hidden, q_heads=shape.q_heads, kv_heads=shape.kv_heads,
+        head_dim=shape.head_dim, intermediate=shape.intermediate, vocab=shape.vocab, rms_eps=shape.rms_eps,
+        rope_theta=shape.rope_theta, qk_norm=int(shape.qk_norm), qkv_bias=int(shape.qkv_bias),
+        tie_embeddings=int(shape.tie_embeddings), dtype=ENG_DTYPE_BF16, block_size=16, num_blocks=num_blocks,
+        max_reqs=max_reqs, max_tokens=max_tokens, max_blocks_per_seq=max_blocks_per_seq)
+
+
+class TensorList:
+    """eng_tensor_t array over host numpy arrays (bf16 as uint16 bits) that keeps them alive."""
+
+    def __init__(self, items: Iterable[tuple[str, np.ndarray]]):
+        self._keep = []
+        recs = []
+        for name, arr in items:
+            arr = np.ascontiguousarray(arr)
+            if arr.dtype == np.uint16:
+                dt = ENG_DTYPE_BF16
+            elif arr.dtype == np.float32:
+                dt = ENG_DTYPE_F32
+            else:
+                raise TypeError(f"{name}: weights are bf16 bits (uint16) or float32")
+            nm = name.encode()
+            self._keep += [arr, nm]
+            recs.append(eng_tensor_t(nm, arr.ctypes.data, arr.size, dt, 0))
+        self.array = (eng_tensor_t * len(recs))(*recs)
+        self.count = len(recs)
+
+
+class StepArrays:
+    """eng_step_t over host arrays (kept alive by this object)."""
+
+    def __init__(self, token_ids, positions, cu_seqlens, block_tables, seq_lens, temperature, seed: int = 0,
+                 offset: int = 0):
+        self.token_ids = _i32(token_ids)
+        self.positions = _i32(positions)
+        self.cu_seqlens = _i32(cu_seqlens)
+        bt = np.atleast_2d(_i32(block_tables))
+        self.block_tables = np.ascontiguousarray(bt)
+        self.seq_lens = _i32(seq_lens)
+        self.temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+        R = len(self.cu_seqlens) - 1
+        self.step = eng_step_t(
+            num_tokens=len(self.token_ids), num_reqs=R, bt_stride=self.block_tables.shape[1],
+            token_ids=_ptr_i32(self.token_ids), positions=_ptr_i32(self.positions),
+            cu_seqlens=_ptr_i32(self.cu_seqlens), block_tables=_ptr_i32(self.block_tables),
+            seq_lens=_ptr_i32(self.seq_lens), temperature=self.temperature.ctypes.data_as(_F32P),
+            seed=int(seed), offset=int(offset))
+
+
+# ------------------------------------------------------------------ entry points
+
+
+def eng_create(cfg: eng_config_t, weights: TensorList, cuda_stream: int | None = None) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    rc = lib().eng_create(ctypes.byref(cfg), weights.array, weights.count, cuda_stream, ctypes.byref(h))
+    _check(None, rc)
+    return h
+
+
+def eng_capture(e, sizes: Sequence[int]) -> None:
+    s = _i32(sizes)
+    _check(e, lib().eng_capture(e, _ptr_i32(s), len(s)))
+
+
+def eng_step(e, step: StepArrays, out_ids_dev: int, out_logits_dev: int | None = None) -> None:
+    _check(e, lib().eng_step(e, ctypes.byref(step.step), out_ids_dev, out_logits_dev))
+
+
+def eng_last_step_info(e) -> eng_step_info_t:
+    info = eng_step_info_t()
+    _check(e, lib().eng_last_step_info(e, ctypes.byref(info)))
+    return info
+
+
+def eng_pool_alloc(e, n: int) -> np.ndarray:
+    out = np.zeros(max(n, 1), dtype=np.int32)
+    _check(e, lib().eng_pool_alloc(e, n, _ptr_i32(out)))
+    return out[:n]
+
+
+def eng_pool_free(e, ids) -> None:
+    a = _i32(ids)
+    _check(e, lib().eng_pool_free(e, _ptr_i32(a), len(a)))
+
+
+def eng_pool_free_count(e) -> int:
+    return int(lib().eng_pool_free_count(e))
+
+
+def eng_status(e, reset: bool = False) -> int:
+    return _check(e, lib().eng_status(e, int(reset)))
+
+
+def eng_set_eager(e, eager: bool) -> None:
+    _check(e, lib().eng_set_eager(e, int(eager)))
+
+
+def eng_kv_pool(e) -> tuple[int, int]:
+    p = ctypes.c_void_p()
+    n = ctypes.c_int64()
+    _check(e, lib().eng_kv_pool(e, ctypes.byref(p), ctypes.byref(n)))
+    return int(p.value or 0), int(n.value)
+
+
+def eng_debug_buffer(e, name: str) -> tuple[int, int]:
+    p = ctypes.c_void_p()
+    n = ctypes.c_int64()
+    _check(e, lib().eng_debug_buffer(e, name.encode(), ctypes.byref(p), ctypes.byref(n)))
+    return int(p.value or 0), int(n.value)
+
+
+def eng_stream(e) -> int:
+    return int(lib().eng_stream(e) or 0)
+
+
+def eng_last_error(e=None) -> str:
+    m = lib().eng_last_error(e)
+    return m.decode() if m else ""
+
+
+def eng_destroy(e) -> None:
+    lib().eng_destroy(e)
+
+
+def eng_philox_uniforms(seed: int, offset: int, rows: int, vocab: int, out_dev: int, stream: int | None = None):
+    _check(None, lib().eng_philox_uniforms(seed, offset, rows, vocab, out_dev, stream))
+
+
+def eng_gumbel(u_dev: int, g_dev: int, n: int, stream: int | None = None):
+    _check(None, lib().eng_gumbel(u_dev, g_dev, n, stream))
+
+
+def eng_sample(logits_dev: int, rows: int, vocab: int, temperature, seed: int, offset: int, out_ids_dev: int,
+               stream: int | None = None):
+    t = np.ascontiguousarray(temperature, dtype=np.float32)
+    _check(None, lib().eng_sample(logits_dev, rows, vocab, t.ctypes.data_as(_F32P), seed, offset, out_ids_dev,
+                                  stream))

@@ -1,0 +1,257 @@
+/*
+ * eng.h -- C ABI of the GB300 fused serving step (libeng.so).
+ *
+ * One call of eng_step runs one serving step of a Qwen3/Qwen2.5-style dense
+ * decoder over one unpadded packed sequence: prefill chunks first, decode
+ * tokens last ("One forward per step", section "What changed").  Every step of
+ * the forward runs in this library's CUDA kernels (sm_103a): embedding gather,
+ * fused residual-add + RMSNorm, one concatenated QKV GEMM, per-head QK-RMSNorm,
+ * RoPE applied inside the paged KV-cache write, attention split inside the call
+ * (packed causal prefill kernel for chunk positions, one-row-per-request paged
+ * decode kernel for decode positions), output projection with residual, one
+ * concatenated gate|up GEMM with fused SiLU-and-mul, the down projection with
+ * residual, the final norm, the LM head and on-device greedy / Gumbel-max
+ * sampling.  The step makes no host synchronisation.  Decode-only steps are
+ * padded to the smallest captured batch size and replayed as one CUDA graph
+ * over static buffers ("33. Removing overhead: fusion, graphs and async
+ * scheduling", section "CUDA graphs for a changing batch").
+ *
+ * Conventions for every function below:
+ *   - returns ENG_OK (0) on success, a negative ENG_E* code otherwise; the
+ *     message of the last failure is available from eng_last_error;
+ *   - "host" pointers are ordinary CPU memory (pinned memory is faster but not
+ *     required); "device" pointers are CUDA global memory of the engine's GPU;
+ *   - an engine is bound to one CUDA stream and one GPU and is not thread-safe.
+ */
+#ifndef ENG_H
+#define ENG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ errors */
+#define ENG_OK 0
+#define ENG_EINVAL (-1)    /* bad argument, shape or request order (the pages raise ValueError) */
+#define ENG_ECAPACITY (-2) /* a position at or past max_blocks_per_seq * block_size ("19. Fast decode",
+                              StaticKVCache: prompt plus new tokens exceed the capacity) */
+#define ENG_ENOMEM (-3)    /* a device or pinned-host allocation failed (eng_create only) */
+#define ENG_EPOOL (-4)     /* the KV block pool has fewer free blocks than requested */
+#define ENG_ECUDA (-5)     /* a CUDA runtime call failed (no device, launch failure, ...) */
+#define ENG_EDEVICE (-6)   /* a kernel-side check failed; see eng_status */
+#define ENG_ESTATE (-7)    /* call not valid in the engine's current state */
+
+/* bits of the device status word (eng_status) */
+#define ENG_STATUS_BAD_BLOCK 1    /* a block-table entry outside [0, num_blocks): write redirected to scratch */
+#define ENG_STATUS_BAD_POSITION 2 /* a position outside the block table: write redirected to scratch */
+#define ENG_STATUS_NAN 4          /* a non-finite logit met the sampler */
+#define ENG_STATUS_TIMEOUT 8      /* a bounded wait inside a kernel gave up */
+
+/* ------------------------------------------------------------------ dtypes */
+#define ENG_DTYPE_BF16 0
+#define ENG_DTYPE_F16 1 /* reserved: not accepted yet */
+#define ENG_DTYPE_F32 2
+
+typedef struct eng eng_t;
+
+/*
+ * Model and engine shape.  Projection widths must be multiples of 16 (rows)
+ * and reduction widths multiples of 32: hidden, q_heads*head_dim and
+ * intermediate are multiples of 32, vocab a multiple of 16.  head_dim is 64 or
+ * 128; q_heads is a multiple of kv_heads with at most 16 query heads per KV
+ * head; block_size must be 16.  max_reqs bounds the requests of one step and
+ * the capture sizes; max_tokens bounds the packed tokens of one step;
+ * max_blocks_per_seq bounds a block-table row (positions < max_blocks_per_seq * 16).
+ */
+typedef struct {
+  int32_t layers, hidden, q_heads, kv_heads, head_dim, intermediate, vocab;
+  float rms_eps;     /* RMSNorm epsilon, also used by the QK-norms */
+  double rope_theta; /* RoPE base: inv_freq_i = theta^(-2i/head_dim) */
+  int32_t qk_norm;   /* 1: per-head RMSNorm of q and k before RoPE (Qwen3) */
+  int32_t qkv_bias;  /* 1: q/k/v projections carry a bias (Qwen2.5) */
+  int32_t tie_embeddings; /* 1: the LM head is the embedding matrix */
+  int32_t dtype;          /* ENG_DTYPE_BF16 */
+  int32_t block_size, num_blocks, max_reqs, max_tokens, max_blocks_per_seq;
+} eng_config_t;
+
+/*
+ * One weight tensor, named as in Hugging Face Qwen checkpoints:
+ *   model.embed_tokens.weight [vocab, hidden]
+ *   model.layers.{i}.input_layernorm.weight [hidden]
+ *   model.layers.{i}.self_attn.{q,k,v}_proj.weight [out, hidden] (+ .bias when qkv_bias)
+ *   model.layers.{i}.self_attn.{q,k}_norm.weight [head_dim] (when qk_norm)
+ *   model.layers.{i}.self_attn.o_proj.weight [hidden, q_heads*head_dim]
+ *   model.layers.{i}.post_attention_layernorm.weight [hidden]
+ *   model.layers.{i}.mlp.{gate,up}_proj.weight [intermediate, hidden]
+ *   model.layers.{i}.mlp.down_proj.weight [hidden, intermediate]
+ *   model.norm.weight [hidden]
+ *   lm_head.weight [vocab, hidden] (only when tie_embeddings == 0)
+ * Row-major, dtype ENG_DTYPE_BF16 (or ENG_DTYPE_F32 for norm weights and
+ * biases).  on_device = 1 if `data` is a device pointer of the engine's GPU.
+ */
+typedef struct {
+  const char* name;
+  const void* data;
+  int64_t numel;
+  int32_t dtype;
+  int32_t on_device;
+} eng_tensor_t;
+
+/*
+ * One packed step, all arrays in host memory, read before eng_step returns:
+ *   token_ids[num_tokens], positions[num_tokens]: absolute position of each token;
+ *   cu_seqlens[num_reqs + 1]: request r owns tokens cu_seqlens[r] .. cu_seqlens[r+1]-1
+ *     (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[num_reqs] = num_tokens,
+ *     every request at least one token, requests with several tokens first);
+ *   block_tables[num_reqs * bt_stride]: row r lists request r's KV blocks in order
+ *     (bt_stride <= max_blocks_per_seq columns; unused entries are ignored);
+ *   seq_lens[num_reqs]: keys visible to request r's last query = its position + 1;
+ *   temperature[num_reqs]: 0 selects greedy argmax, > 0 Gumbel-max at that temperature;
+ *   seed, offset: Philox key and counter words of this step's Gumbel noise.
+ * A request's positions must be consecutive and end at seq_lens[r] - 1.
+ */
+typedef struct {
+  int32_t num_tokens, num_reqs, bt_stride;
+  const int32_t* token_ids;
+  const int32_t* positions;
+  const int32_t* cu_seqlens;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const float* temperature;
+  uint64_t seed, offset;
+} eng_step_t;
+
+/* What the last eng_step did (for tests and benchmarks). */
+typedef struct {
+  int32_t replayed;     /* 1: a captured graph was replayed; 0: kernels were launched eagerly */
+  int32_t bucket;       /* capture size replayed (or num_reqs when eager) */
+  int32_t launches;     /* kernels launched (the graph's kernel count when replayed) */
+  int32_t num_prefill;  /* requests routed to the packed prefill attention kernel */
+  int64_t h2d_bytes;    /* bytes copied host -> device by the step */
+} eng_step_info_t;
+
+/*
+ * eng_create -- allocate an engine and load fused weights.
+ * ("33. Removing overhead", section "Fewer, larger matmuls": Q/K/V and gate/up
+ * are concatenated once at load time.)  The weights are copied and re-laid out
+ * into the engine's own device memory, so the caller may free its tensors on
+ * return.  Allocates the paged KV pool [layers][2][num_blocks + 1][kv_heads][16][head_dim]
+ * bf16 (the extra block is the scratch block; the pool is zero-filled) and all
+ * static step buffers.  cuda_stream: the cudaStream_t to run on, or NULL for a
+ * stream the engine creates.  Errors: ENG_EINVAL (config, missing/mis-sized
+ * weight), ENG_ENOMEM, ENG_ECUDA.  *out is NULL on failure.
+ */
+int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_weights, void* cuda_stream,
+               eng_t** out);
+
+/*
+ * eng_capture -- record one CUDA graph per batch size, largest first, all
+ * sharing the engine's single set of static buffers ("33. Removing overhead",
+ * GraphRunner.capture; "(7) Graph Mode", section 4.1).  Every row of a capture
+ * is a padding row (slot redirected to the scratch block, sequence length 0),
+ * so capture writes only the scratch block of the KV pool.  sizes[n]: distinct
+ * values in [1, max_reqs].  Synchronises the stream.  Errors: ENG_EINVAL, ENG_ECUDA.
+ */
+int eng_capture(eng_t* e, const int32_t* sizes, int32_t n);
+
+/*
+ * eng_step -- run one packed step and write one sampled token id per request.
+ * Decode-only steps (every request one token) with num_reqs <= the largest
+ * captured size replay the smallest captured graph >= num_reqs, with rows
+ * num_reqs.. padded (token 0, position 0, sequence length 0); every other step
+ * runs the same kernels eagerly ("33. Removing overhead", GraphRunner.can_run).
+ * out_ids_dev: device int32[num_reqs]; out_logits_dev: device float[num_reqs][vocab]
+ * or NULL.  Both are written in stream order; eng_step returns without waiting
+ * for the GPU, so synchronise the stream before reading them.  The request's
+ * sampled id comes from its last packed token.  Errors: ENG_EINVAL (shapes,
+ * order, block ids out of range), ENG_ECAPACITY, ENG_ECUDA.
+ */
+int eng_step(eng_t* e, const eng_step_t* step, int32_t* out_ids_dev, float* out_logits_dev);
+
+/* eng_last_step_info -- what the last successful eng_step did. */
+int eng_last_step_info(const eng_t* e, eng_step_info_t* info);
+
+/*
+ * eng_pool_alloc / eng_pool_free -- the paged KV block pool ("One forward per
+ * step": a pool of fixed-size blocks, blocks reserved when a request is
+ * admitted).  The free list starts as 0..num_blocks-1; allocation takes from
+ * the front, freeing appends to the back.  The scratch block (num_blocks) is
+ * never handed out.  alloc: out_ids[n] host; ENG_EPOOL if fewer than n are
+ * free (nothing allocated).  free: ENG_EINVAL if an id is not allocated
+ * (nothing freed).
+ */
+int eng_pool_alloc(eng_t* e, int32_t n, int32_t* out_ids);
+int eng_pool_free(eng_t* e, const int32_t* ids, int32_t n);
+int32_t eng_pool_free_count(const eng_t* e);
+
+/*
+ * eng_status -- synchronise the stream and return the device status word
+ * (ENG_STATUS_* bits, 0 = clean), or a negative ENG_E* code if the stream
+ * holds a CUDA error.  reset != 0 clears the word afterwards.
+ */
+int eng_status(eng_t* e, int32_t reset);
+
+/* eng_set_eager -- 1: never replay graphs (debugging; "(7) Graph Mode", section 6: disable graphs when debugging). */
+int eng_set_eager(eng_t* e, int32_t eager);
+
+/*
+ * eng_kv_pool -- device address and size of the paged KV pool, laid out as
+ * bf16 [layers][2 (K, V)][num_blocks + 1][kv_heads][16][head_dim].  Lets a
+ * caller pre-fill context K/V for synthetic workloads or inspect the cache.
+ */
+int eng_kv_pool(eng_t* e, void** dev_ptr, int64_t* bytes);
+
+/*
+ * eng_debug_buffer -- device address and byte size of a named static buffer
+ * holding the last step's intermediate values: "hidden" (float [max_tokens][hidden],
+ * residual stream after the last layer), "slots" (int32 [max_tokens], KV slot
+ * of each packed token, -1 for padding rows), "logits" (float [max_reqs][vocab]),
+ * "ids" (int32 [max_reqs]).  Read-only for the caller.
+ */
+int eng_debug_buffer(eng_t* e, const char* name, void** dev_ptr, int64_t* bytes);
+
+/* eng_stream -- the cudaStream_t the engine runs on. */
+void* eng_stream(const eng_t* e);
+
+/* eng_last_error -- message of the last failure on this engine (or of the last failed eng_create if e is NULL). */
+const char* eng_last_error(const eng_t* e);
+
+/* eng_destroy -- free every resource of the engine (synchronises its stream).  NULL is a no-op. */
+void eng_destroy(eng_t* e);
+
+/* ------------------------------------------------------------------
+ * Standalone kernels, for unit tests of the device arithmetic.
+ * ------------------------------------------------------------------ */
+
+/*
+ * eng_philox_uniforms -- the sampler's uniforms ("19. Fast decode", section
+ * "Sampling without the CPU") for rows x vocab entries: out[r][v] =
+ * (2 * (x >> 9) + 1) * 2^-24 with x word (v & 3) of Philox4x32-10 under key
+ * (seed_lo, seed_hi) at counter (v >> 2, r, offset_lo, offset_hi).
+ * out_dev: device float[rows][vocab].  stream: cudaStream_t or NULL (legacy default stream).
+ */
+int eng_philox_uniforms(uint64_t seed, uint64_t offset, int32_t rows, int32_t vocab, float* out_dev, void* stream);
+
+/*
+ * eng_gumbel -- g[i] = -ln(-ln u[i]) with the sampler's own float32 logarithm
+ * (correctly rounded +, -, *, / only).  u_dev, g_dev: device float[n]; u in (0, 1).
+ */
+int eng_gumbel(const float* u_dev, float* g_dev, int64_t n, void* stream);
+
+/*
+ * eng_sample -- the sampler on caller logits: out_ids[r] = argmax_v of
+ * logits[r][v] (temperature 0) or of logits[r][v] * (1/T_r) + g[r][v] with the
+ * Gumbel noise of eng_philox_uniforms / eng_gumbel; ties go to the lowest index.
+ * logits_dev: device float[rows][vocab]; temperature: host float[rows];
+ * out_ids_dev: device int32[rows].
+ */
+int eng_sample(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature, uint64_t seed,
+               uint64_t offset, int32_t* out_ids_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENG_H */

@@ -1,0 +1,255 @@
+"""End-to-end parity on the tiny two-layer decoder: one packed prefill step then graph-replayed decode.
+
+Workload: 4 requests with 16-token uniform-random prompts, block size 16, one packed prefill step followed
+by 15 pure-decode steps (16 sampled tokens per request), greedy; and the same with Gumbel-max sampling.
+Both sides consume the GPU's sampled ids (teacher forcing).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+from harness import GpuEngine, block_table, check_logits_and_ids
+
+pytestmark = pytest.mark.gpu
+
+S = synth.shape("tiny")
+NB, MBS = 64, 8
+
+
+@pytest.fixture(scope="module")
+def weights():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return synth.make_weights(S, seed=0)
+
+
+def _engine(weights, stream=None):
+    return GpuEngine(S, weights, num_blocks=NB, max_reqs=8, max_tokens=128, max_blocks_per_seq=MBS, stream=stream)
+
+
+def run_tiny(weights, temps, capture=True, steps=16, seed=5):
+    g = _engine(weights)
+    try:
+        if capture:
+            g.capture([1, 2, 4, 8])
+        pool = oracle.BlockPool(NB)
+        cache = oracle.PagedCache(S, NB)
+        model = oracle.OracleModel(S, weights)
+        R, P = 4, 16
+        prompts = [synth.prompt_ids(P, S.vocab, r) for r in range(R)]
+        blocks = []
+        for r in range(R):
+            got = g.alloc(oracle.blocks_needed(P + steps))
+            want = pool.alloc(oracle.blocks_needed(P + steps))
+            np.testing.assert_array_equal(got, want)                 # block tables bit-exact
+            blocks.append(list(got))
+            cache.set_block_table(r, got)
+        bt = block_table(blocks, MBS)
+        temps = np.asarray(temps, dtype=np.float32)
+
+        from graph_replayed_decode_gb300.eng import StepArrays
+        ids = np.concatenate(prompts)
+        pos = np.concatenate([np.arange(P)] * R)
+        cu = np.arange(R + 1) * P
+        errs = []
+        for k in range(steps):
+            seq = np.array([pos[cu[r + 1] - 1] + 1 for r in range(R)])
+            st = StepArrays(ids, pos, cu, bt, seq, temps, seed=seed, offset=k)
+            gid, glog = g.step(st)
+            info = g.info()
+            assert info.replayed == int(capture and k > 0)
+            olog = oracle.forward_step(model, cache, ids, pos, cu)
+            errs.append(check_logits_and_ids(glog, gid, olog, temps, seed, k))
+            # slots of this step: bit-exact against the oracle's slot mapping
+            import torch
+            sp, _ = g.eng.eng_debug_buffer(g.h, "slots")
+            from harness import device_view
+            slots = device_view(sp, 4 * len(ids), torch.int32).cpu().numpy()
+            want_slots = [cache.slot(int(np.searchsorted(cu, t, side="right") - 1), int(pos[t])) for t in range(len(ids))]
+            np.testing.assert_array_equal(slots, want_slots)
+            ids = gid.copy()
+            pos = np.array([pos[cu[r + 1] - 1] + 1 for r in range(R)])
+            cu = np.arange(R + 1)
+        assert g.status() == 0
+        return errs
+    finally:
+        g.close()
+
+
+def test_tiny_greedy_prefill_then_graph_decode(weights):
+    errs = run_tiny(weights, [0.0] * 4)
+    assert max(errs) <= 3e-2
+
+
+def test_tiny_gumbel_prefill_then_graph_decode(weights):
+    errs = run_tiny(weights, [1.0, 0.7, 0.0, 1.3])
+    assert max(errs) <= 3e-2
+
+
+def test_tiny_eager_only(weights):
+    run_tiny(weights, [0.0, 1.0, 0.0, 0.5], capture=False, steps=4)
+
+
+def _decode_batch(g, weights, R, ctx=37, seed=0):
+    """R decode rows over synthetic contexts; returns StepArrays."""
+    from graph_replayed_decode_gb300.eng import StepArrays
+    blocks = []
+    for r in range(R):
+        b = g.alloc(oracle.blocks_needed(ctx + 1))
+        blocks.append(list(b))
+        for l in range(S.layers):
+            g.fill_context(l, b, synth.kv_context(S, l, r, ctx))
+    bt = block_table(blocks, MBS)
+    ids = synth.decode_ids(R, S.vocab, 0)
+    pos = np.full(R, ctx)
+    return StepArrays(ids, pos, np.arange(R + 1), bt, pos + 1, np.array([0.0, 1.0, 0.7, 0.0, 2.0][:R] * 2)[:R],
+                      seed=seed, offset=3)
+
+
+def test_graph_replay_equals_eager_bit_exact_and_padding_is_harmless(weights):
+    g = _engine(weights)
+    try:
+        st = _decode_batch(g, weights, 3)
+        ids_e, log_e = g.step(st)                        # eager (nothing captured yet)
+        assert g.info().replayed == 0
+        g.capture([4, 8])
+        ids_g, log_g = g.step(st)                        # replayed in bucket 4 with one padding row
+        info = g.info()
+        assert info.replayed == 1 and info.bucket == 4
+        np.testing.assert_array_equal(ids_g, ids_e)
+        np.testing.assert_array_equal(log_g.view(np.uint32), log_e.view(np.uint32))
+        assert np.isfinite(log_g).all()
+        assert g.status() == 0
+    finally:
+        g.close()
+
+
+def test_capture_writes_only_the_scratch_block(weights):
+    import torch
+    g = _engine(weights)
+    try:
+        _decode_batch(g, weights, 2)
+        before = g.kv_pool().clone()
+        g.capture([1, 2, 4, 8])
+        after = g.kv_pool()
+        torch.cuda.synchronize()
+        assert torch.equal(before[:, :, :NB], after[:, :, :NB])
+    finally:
+        g.close()
+
+
+def test_freed_block_poisoning_leaves_outputs_unchanged(weights):
+    import torch
+    g = _engine(weights)
+    try:
+        g.capture([4])
+        st = _decode_batch(g, weights, 3, ctx=29)
+        ids0, log0 = g.step(st)
+        used = set(int(b) for b in st.block_tables.reshape(-1) if b)
+        used |= {int(st.block_tables[0, 0])}
+        pool = g.kv_pool()
+        nan_bits = 0x7FC0
+        free = [b for b in range(NB + 1) if b not in used]
+        pool[:, :, torch.as_tensor(free, device="cuda")] = nan_bits
+        # poison the tails of the last blocks too (positions past each row's length)
+        for r in range(3):
+            last = int(st.block_tables[r, (29 + 1 - 1) // 16])
+            pool[:, :, last, :, (30 % 16):, :] = nan_bits
+        ids1, log1 = g.step(st)
+        np.testing.assert_array_equal(ids1, ids0)
+        np.testing.assert_array_equal(log1.view(np.uint32), log0.view(np.uint32))
+    finally:
+        g.close()
+
+
+def test_mixed_step_prefill_chunks_and_decode_rows(weights):
+    """A packed step with two prompt chunks (one resuming after an earlier chunk) and three decode rows."""
+    from graph_replayed_decode_gb300.eng import StepArrays
+    g = _engine(weights)
+    try:
+        model = oracle.OracleModel(S, weights)
+        cache = oracle.PagedCache(S, NB)
+        blocks = [list(g.alloc(n)) for n in (3, 2, 2, 2, 3)]
+        for r, b in enumerate(blocks):
+            cache.set_block_table(r, b)
+        bt = block_table(blocks, MBS)
+        # request 0: first chunk of 20 prompt tokens, then a second chunk of 9 (positions 20..28)
+        p0 = synth.prompt_ids(29, S.vocab, 10)
+        first = StepArrays(p0[:20], np.arange(20), [0, 20], bt[:1], [20], [0.0])
+        gid, glog = g.step(first)
+        olog = oracle.forward_step(model, cache, p0[:20], np.arange(20), [0, 20])
+        check_logits_and_ids(glog, gid, olog, [0.0], 0, 0)
+        # decode rows 2..4 with synthetic contexts of 17, 5, 31 keys
+        ctxs = [17, 5, 31]
+        for j, ctx in enumerate(ctxs):
+            r = 2 + j
+            for l in range(S.layers):
+                kv = synth.kv_context(S, l, 100 + r, ctx)
+                g.fill_context(l, blocks[r], kv)
+                from oracle.model import widen_bf16
+                K = np.swapaxes(widen_bf16(kv[0]), 0, 1)
+                V = np.swapaxes(widen_bf16(kv[1]), 0, 1)
+                cache.write(l, r, np.arange(ctx), K, V)
+        p1 = synth.prompt_ids(11, S.vocab, 11)
+        dec = synth.decode_ids(3, S.vocab, 4)
+        ids = np.concatenate([p0[20:], p1, dec])
+        pos = np.concatenate([np.arange(20, 29), np.arange(11), np.array(ctxs)])
+        cu = np.array([0, 9, 20, 21, 22, 23])
+        seq = np.array([29, 11, 18, 6, 32])
+        temps = np.array([0.0, 0.9, 0.0, 1.0, 0.0], dtype=np.float32)
+        st = StepArrays(ids, pos, cu, bt, seq, temps, seed=1, offset=2)
+        gid, glog = g.step(st)
+        assert g.info().num_prefill == 2
+        olog = oracle.forward_step(model, cache, ids, pos, cu)
+        check_logits_and_ids(glog, gid, olog, temps, 1, 2)
+        assert g.status() == 0
+    finally:
+        g.close()
+
+
+def test_step_does_not_wait_for_the_gpu(weights):
+    """eng_step returns while earlier work on its stream is still running (no host sync in the step)."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    stream = torch.cuda.Stream()
+    g = _engine(weights, stream=stream)
+    try:
+        g.capture([4])
+        st = _decode_batch(g, weights, 4)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(200_000_000)               # keep the stream busy for a while
+        eng.eng_step(g.h, st, g.ids_dev.data_ptr(), None)
+        assert not stream.query(), "eng_step waited for the stream"
+        stream.synchronize()
+    finally:
+        g.close()
+
+
+def test_host_validation_errors(weights):
+    from graph_replayed_decode_gb300 import eng
+    from graph_replayed_decode_gb300.eng import StepArrays
+    g = _engine(weights)
+    try:
+        b = list(g.alloc(2))
+        bt = block_table([b, b], MBS)
+        with pytest.raises(eng.EngError) as ei:    # decode row before a prefill chunk
+            g.step(StepArrays([1, 2, 3], [5, 0, 1], [0, 1, 3], bt, [6, 2], [0, 0]))
+        assert ei.value.code == eng.ENG_EINVAL
+        with pytest.raises(eng.EngError) as ei:    # position past the capacity
+            bt_wide = np.zeros((1, MBS), dtype=np.int32)
+            g.step(StepArrays([1], [MBS * 16], [0, 1], bt_wide, [MBS * 16 + 1], [0]))
+        assert ei.value.code == eng.ENG_ECAPACITY
+        with pytest.raises(eng.EngError) as ei:    # block id out of range
+            g.step(StepArrays([1], [3], [0, 1], np.array([[NB + 5]]), [4], [0]))
+        assert ei.value.code == eng.ENG_EINVAL
+        with pytest.raises(eng.EngError) as ei:    # pool exhaustion
+            g.alloc(NB)
+        assert ei.value.code == eng.ENG_EPOOL
+        with pytest.raises(eng.EngError):
+            eng.eng_pool_free(g.h, [NB - 1])
+        assert g.status() == 0
+    finally:
+        g.close()
