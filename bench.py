@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Decode throughput of the graph-replayed fused serving step on GB300.
+
+Default workload (one GPU): a Qwen3-0.6B-shaped decoder (28 layers, hidden 1024, 16 Q / 8 KV heads,
+head_dim 128, QK-norm, intermediate 3072, vocab 151936, tied embeddings, random bf16 weights ~N(0, 0.02)),
+batch 1, a 512-token prompt prefilled eagerly into a paged cache (block 16), then pure-decode steps replayed
+from the captured bucket-1 CUDA graph with Gumbel-max sampling at temperature 0.8 (capture sizes
+1, 2, 4, 8, 16, 32, 64).  One step = one whole forward of the decode batch (embedding, 28 layers, final
+norm, LM head, sampling, in-place advance of the next step's inputs).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line (rank 0).  `value` is decode tokens/s with inputs resident on the device (eng_decode:
+back-to-back graph replays); `e2e` is the same metric through eng_step with host inputs copied in and the
+sampled ids read back every step.  With --gpus N > 1 (torchrun) every rank runs an independent replica.
+`--impl reference` times the CPU oracle on the same workload (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from graph_replayed_decode_gb300 import roofline  # noqa: E402
+
+METRIC = "decode tokens/s and step ms at 1 GB300; achieved fraction of HBM step roofline"
+CAPTURE_SIZES = [1, 2, 4, 8, 16, 32, 64]
+
+WORKLOADS = {
+    # the metric's headline configuration
+    "qwen3_0p6b_b1": dict(shape="qwen3_0p6b", batch=1, contexts=[512], temperature=0.8, prefill=True,
+                          text="Qwen3-0.6B-shaped decoder, batch 1 pure decode after a 512-token prefill, "
+                               "paged cache (block 16), Gumbel-max T=0.8, graph-replayed (bucket 1)"),
+    "qwen3_0p6b_b32": dict(shape="qwen3_0p6b", batch=32, contexts=None, temperature=1.0, prefill=False,
+                           text="Qwen3-0.6B-shaped decoder, batch 32 pure decode, contexts drawn from "
+                                "{16,64,256,1024,4096} (seed 0, synthetic KV), Gumbel-max T=1.0, bucket 32"),
+    "dense_8b_b64": dict(shape="dense_8b", batch=64, contexts=[2048] * 64, temperature=0.7, prefill=False,
+                         text="8B-shaped dense decoder, batch 64 pure decode at context 2048 (synthetic KV), "
+                              "Gumbel-max T=0.7, bucket 64"),
+}
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def workload_contexts(wl: dict) -> list[int]:
+    if wl["contexts"] is not None:
+        return list(wl["contexts"])
+    return [int(x) for x in synth.context_lengths(wl["batch"], (16, 64, 256, 1024, 4096), key=0, seed=0)]
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the CPU oracle (baseline / reference arm)
+
+
+def oracle_decode_rate(wl: dict, budget_s: float, max_steps: int | None = None, warmup: int = 0) -> dict:
+    """Time the CPU oracle (float64 numpy, as it stands) on decode steps of the workload.
+
+    Setup (untimed): widened weights and each request's context filled with the same synthetic K/V
+    recipe as the GPU's synthetic contexts (the 512-token prompt's cache for the batch-1 workload).
+    Steps run until `budget_s` of measured time or `max_steps` steps.
+    """
+    import oracle
+    s = synth.shape(wl["shape"])
+    w = synth.make_weights(s, seed=0)
+    model = oracle.OracleModel(s, w)
+    B = wl["batch"]
+    ctxs = workload_contexts(wl)
+    rows = list(range(min(B, 4)))                  # a bounded sample of the batch: rows are independent
+    room = (max_steps or 512) + warmup + 2
+    cap = {r: ctxs[r] + room for r in rows}
+    cache = oracle.ContiguousCache(s, cap)
+    for r in rows:
+        for l in range(s.layers):
+            kv = synth.kv_context(s, l, r, ctxs[r])
+            cache.keys[(l, r)][:, :ctxs[r], :] = oracle.widen_bf16(kv[0])
+            cache.values[(l, r)][:, :ctxs[r], :] = oracle.widen_bf16(kv[1])
+    ids = synth.decode_ids(len(rows), s.vocab, 0)
+    pos = np.array([ctxs[r] for r in rows])
+    temps = np.full(len(rows), wl["temperature"], dtype=np.float32)
+    model.get("model.embed_tokens.weight")
+    done, t_meas, k = 0, 0.0, 0
+    while True:
+        t0 = time.perf_counter()
+        z = oracle.forward_step(model, cache, ids, pos, np.arange(len(rows) + 1), request_keys=rows)
+        ids = oracle.sample(z.astype(np.float32), temps, 0, k)
+        dt = time.perf_counter() - t0
+        pos = pos + 1
+        k += 1
+        if k > warmup:
+            done += 1
+            t_meas += dt
+        if max_steps is not None and done >= max_steps:
+            break
+        if max_steps is None and ((t_meas >= budget_s and done >= 2) or k + 1 >= room):
+            break
+    tokens = done * len(rows)
+    return {"value": tokens / t_meas, "steps": done, "rows": len(rows), "seconds": t_meas,
+            "cores": os.cpu_count() or 1}
+
+
+# ------------------------------------------------------------------ our arm
+
+
+class _CudaArray:
+    def __init__(self, ptr: int, n: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i2", "data": (ptr, False), "version": 3,
+                                         "strides": None}
+
+
+def fill_synthetic_kv(h, s, nb: int, blocks, ctxs) -> None:
+    """Write each request's synthetic context K/V (synth.kv_context, bf16) into the engine's paged pool."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    ptr, nbytes = eng.eng_kv_pool(h)
+    pool = torch.as_tensor(_CudaArray(ptr, nbytes // 2), device="cuda").view(s.layers, 2, nb + 1, s.kv_heads, 16,
+                                                                             s.head_dim)
+    for r, (b, ctx) in enumerate(zip(blocks, ctxs)):
+        pos = torch.arange(ctx, device="cuda")
+        bt = torch.as_tensor(np.asarray(b, dtype=np.int64), device="cuda")
+        for l in range(s.layers):
+            x = torch.from_numpy(synth.kv_context(s, l, r, ctx).view(np.int16)).to("cuda")
+            pool[l, :, bt[pos // 16], :, pos % 16, :] = x.permute(2, 0, 1, 3)
+    torch.cuda.synchronize()
+
+
+def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+    torch.cuda.set_device(local_rank)
+    from graph_replayed_decode_gb300 import build, eng
+    if not os.path.exists(eng.LIB_PATH):
+        if rank == 0:
+            build.build()
+        if world > 1:
+            torch.distributed.barrier()
+    s = synth.shape(wl["shape"])
+    B = wl["batch"]
+    ctxs = workload_contexts(wl)
+    K, W = args.steps, args.warmup
+    extra = 1 + W + K + 1 + args.steps + 8          # first step, warmup, timed, profile, e2e
+    mbs = -(-(max(ctxs) + extra) // 16)
+    need = [-(-(c + extra) // 16) for c in ctxs]
+    nb = sum(need) + 8
+    max_tokens = max(512 if wl["prefill"] else 64, 64)
+
+    weights = synth.make_weights(s, seed=0, cache=False)
+    stream = torch.cuda.Stream()
+    h = eng.eng_create(eng.make_config(s, nb, 64, max_tokens, mbs), eng.TensorList(weights.items()),
+                       stream.cuda_stream)
+    del weights
+    ids_dev = torch.zeros(64, dtype=torch.int32, device="cuda")
+    temps = np.full(B, wl["temperature"], dtype=np.float32)
+    blocks = [eng.eng_pool_alloc(h, n) for n in need]
+    bt = np.zeros((B, mbs), dtype=np.int32)
+    for r, b in enumerate(blocks):
+        bt[r, :len(b)] = b
+    out = {}
+    # ---- context: a real eager prefill (batch 1) or synthetic K/V written into the pool
+    if wl["prefill"]:
+        assert B == 1
+        prompt = synth.prompt_ids(ctxs[0], s.vocab, 0)
+        st = eng.StepArrays(prompt, np.arange(ctxs[0]), [0, ctxs[0]], bt, [ctxs[0]], temps, seed=0, offset=0)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            eng.eng_step(h, st, ids_dev.data_ptr(), None)
+            e1.record()
+        torch.cuda.synchronize()
+        out["prefill_ms"] = e0.elapsed_time(e1)
+        first = ids_dev[:1].cpu().numpy()
+    else:
+        fill_synthetic_kv(h, s, nb, blocks, ctxs)
+        first = synth.decode_ids(B, s.vocab, 0)
+    eng.eng_capture(h, CAPTURE_SIZES)
+
+    pos = np.array(ctxs, dtype=np.int32)
+    st = eng.StepArrays(first, pos, np.arange(B + 1), bt, pos + 1, temps, seed=0, offset=1)
+    eng.eng_step(h, st, ids_dev.data_ptr(), None)           # first decode step (host inputs)
+    launches_per_step = eng.eng_last_step_info(h).launches
+    ring = torch.zeros((max(K, W, 1), B), dtype=torch.int32, device="cuda")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    eng.eng_decode(h, W, ring.data_ptr())                     # warm-up replays
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
+    with torch.cuda.stream(stream):
+        e0.record()
+        eng.eng_decode(h, K, ring.data_ptr())
+        e1.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    t_dev = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        torch.distributed.barrier()
+    seq_timed = [c + 1 + W + k + 1 for c in ctxs for k in range(K)]    # keys seen by each timed step's rows
+
+    # ---- per-kernel timing of one more step (CUDA events around every launch on the engine stream)
+    prof = eng.eng_profile(h)
+
+    # ---- end to end: eng_step with host inputs and a device->host read of the sampled ids every step
+    pinned = torch.zeros(B, dtype=torch.int32).pin_memory()
+    ids_h = ring[K - 1].cpu().numpy() if K > 0 else first
+    pos = pos + 1 + W + K + 1
+    torch.cuda.synchronize()
+    h2d = 0
+    t0 = time.perf_counter()
+    for k in range(K):
+        st = eng.StepArrays(ids_h, pos, np.arange(B + 1), bt, pos + 1, temps, seed=0, offset=10_000 + k)
+        eng.eng_step(h, st, ids_dev.data_ptr(), None)
+        with torch.cuda.stream(stream):
+            pinned.copy_(ids_dev[:B], non_blocking=True)
+        stream.synchronize()
+        ids_h = pinned.numpy().copy()
+        pos = pos + 1
+        h2d = eng.eng_last_step_info(h).h2d_bytes
+    t_e2e = time.perf_counter() - t0
+    clk = clocks.stop()
+    status = eng.eng_status(h, True)
+    eng.eng_destroy(h)
+
+    # ---- max over ranks
+    times = np.array([t_dev, t_e2e], dtype=np.float64)
+    if world > 1:
+        tt = torch.from_numpy(times).cuda()
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        times = tt.cpu().numpy()
+    t_dev, t_e2e = float(times[0]), float(times[1])
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    bw = peaks["hbm_gbs"] * 1e9
+    mean_seq = float(np.mean(seq_timed))
+    step_b = roofline.step_bytes(s, B, [mean_seq] * B)
+    t_roof = step_b / bw
+    step_s = t_dev / K
+    # dominant kernel kind by total time of the profiled step
+    agg: dict[str, list] = {}
+    for kind, ms, nbytes in prof:
+        a = agg.setdefault(kind, [0, 0.0, 0])
+        a[0] += 1
+        a[1] += ms
+        a[2] += nbytes
+    dom = max(agg.items(), key=lambda kv: kv[1][1])
+    dk, (dn, dms, dbytes) = dom
+    achieved = (dbytes / dn) / (dms / dn / 1e3) / 1e9
+    traffic = load_traffic(wl_name=args.workload, kind=dk)
+    result = {
+        "metric": METRIC,
+        "value": world * B * K / t_dev,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": step_s * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl["text"], "batch": B, "context_start": ctxs if B <= 4 else "seeded draw",
+                   "temperature": wl["temperature"], "capture_sizes": CAPTURE_SIZES,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {roofline.weight_bytes(s) / 1e9:.3f} GB of weights read per step"},
+        "step_roofline": {"bytes_per_step": int(step_b), "t_roof_ms": t_roof * 1e3, "frac": t_roof / step_s,
+                          "peak_gbs": peaks["hbm_gbs"], "of": peaks["source"]},
+        "roofline": {"kernel": dk, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "launches_per_step": dn,
+                     "share_of_step": dms / sum(a[1] for a in agg.values()), "of": peaks["source"]},
+        "kernels": {k: {"launches": v[0], "ms": round(v[1], 4), "gbs": round(v[2] / (v[1] / 1e3) / 1e9, 1)}
+                    for k, v in sorted(agg.items(), key=lambda kv: -kv[1][1])},
+        "e2e": {"value": world * B * K / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": 4 * B},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if "prefill_ms" in out:
+        result["prefill_ms"] = out["prefill_ms"]
+    if world == 1 and not args.no_cpu_baseline:
+        cb = oracle_decode_rate(wl, budget_s=args.cpu_seconds, warmup=1)
+        result["cpu_baseline"] = {"value": cb["value"], "unit": "tokens/s", "cores": cb["cores"], "kind": "oracle",
+                                  "sample": f"{cb['steps']} decode steps x {cb['rows']} row(s) of this workload "
+                                            f"(float64 numpy oracle, synthetic context), {cb['seconds']:.1f} s"}
+    return result
+
+
+def load_traffic(wl_name: str, kind: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    entry = d.get(wl_name, {}).get(kind)
+    if not entry or entry.get("sources_hash") != sources_hash():
+        return None
+    return entry.get("bytes_per_launch")
+
+
+def sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "graph_replayed_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_0p6b_b1")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    wl = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        r = oracle_decode_rate(wl, budget_s=0.0, max_steps=args.steps, warmup=max(args.warmup, 1))
+        line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["seconds"] / max(r["steps"], 1) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": wl["text"] + " (CPU oracle on a bounded sample)"},
+                "cpu_baseline": {"value": r["value"], "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
+                                 "sample": f"{r['steps']} timed decode steps x {r['rows']} row(s), float64 numpy"},
+                "e2e": {"value": r["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, wl, rank, world, local_rank)
+    if res is not None:
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -18,6 +18,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <deque>
 #include <map>
@@ -50,7 +51,7 @@ struct Layer {
 
 // Word offsets of the step inputs inside one staging slot (host) and the device input region.
 struct InLayout {
-  size_t ids, pos, tok2req, cu, seq, last, invt, rng, wlog, items, bt, words;
+  size_t ids, pos, tok2req, cu, seq, last, invt, rng, wlog, step, items, bt, words;
 };
 
 struct GemmSite {
@@ -108,6 +109,18 @@ struct eng {
   int* status = nullptr;
   GemmSite g_qkv, g_o, g_gu, g_down, g_lm;
   int split_blocks = 4, max_splits = 1;
+  int* ring = nullptr;  // [ring_cap][bucket] ids recorded by the advance kernel
+  int ring_cap = 1024;
+
+  // the decode batch that eng_decode continues (host mirror of its lengths)
+  int dec_R = 0, dec_rows = 0, dec_bt_stride = 0;
+  std::vector<int> dec_seq;
+
+  // per-launch event timing (eng_profile)
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_ev;
+  std::vector<int> prof_kind;
+  std::vector<int64_t> prof_bytes;
 
   // pool
   std::deque<int> free_list;
@@ -357,7 +370,8 @@ static int setup_buffers(eng_t* e) {
   L.last = o; o += Rm;
   L.invt = o; o += Rm;
   L.rng = o; o += 4;
-  L.wlog = o; o += 4;
+  L.wlog = o; o += 2;
+  L.step = o; o += 2;
   o = (o + 3) & ~(size_t)3;
   L.items = o; o += (size_t)4 * e->max_items;
   L.bt = o; o += (size_t)Rm * c.max_blocks_per_seq;
@@ -384,6 +398,7 @@ static int setup_buffers(eng_t* e) {
   TRY(dev_alloc(e, &e->best, Rm));
   TRY(dev_alloc(e, &e->done_counter, 4));
   TRY(dev_alloc(e, &e->status, 4));
+  TRY(dev_alloc(e, &e->ring, (size_t)e->ring_cap * Rm));
 
   auto site = [&](GemmSite& s, int N, int K, int T) -> int {
     s.N = N;
@@ -419,9 +434,32 @@ static int setup_buffers(eng_t* e) {
 
 // ------------------------------------------------------------------ the step's kernel sequence
 
-static cudaError_t gemm(eng_t* e, const GemmSite& s, const bf16* W, const bf16* X, int T, int epi, cudaStream_t st,
-                        float* out_f32 = nullptr, const float* bias = nullptr, float* resid = nullptr,
-                        bf16* out_bf16 = nullptr) {
+// Event pair around one launch when eng_profile is collecting (no-op otherwise).
+static void prof_begin(eng_t* e, cudaStream_t st, int kind, int64_t bytes) {
+  if (!e->prof_on) return;
+  const size_t i = e->prof_kind.size();
+  if (2 * i + 2 > e->prof_ev.size()) return;
+  cudaEventRecord(e->prof_ev[2 * i], st);
+  e->prof_kind.push_back(kind);
+  e->prof_bytes.push_back(bytes);
+}
+static void prof_end(eng_t* e, cudaStream_t st) {
+  if (!e->prof_on || e->prof_kind.empty()) return;
+  cudaEventRecord(e->prof_ev[2 * (e->prof_kind.size() - 1) + 1], st);
+}
+
+static int64_t gemm_bytes(const GemmSite& s, int T, int epi) {
+  int64_t b = (int64_t)s.N * s.K * 2 + (int64_t)T * s.K * 2;  // weights once + activations in
+  if (epi == EPI_STORE_F32) b += (int64_t)T * s.N * 4;
+  if (epi == EPI_RESID) b += (int64_t)T * s.N * 8;            // residual read + write
+  if (epi == EPI_SILU) b += (int64_t)T * (s.N / 2) * 2;
+  if (epi == EPI_LMHEAD) b += (int64_t)T * 4;
+  return b;
+}
+
+static cudaError_t gemm(eng_t* e, const GemmSite& s, const bf16* W, const bf16* X, int T, int epi, int kind,
+                        cudaStream_t st, float* out_f32 = nullptr, const float* bias = nullptr,
+                        float* resid = nullptr, bf16* out_bf16 = nullptr) {
   GemmParams p{};
   p.W = W;
   p.X = X;
@@ -451,16 +489,26 @@ static cudaError_t gemm(eng_t* e, const GemmSite& s, const bf16* W, const bf16* 
   LaunchOpts o;
   o.pdl = e->pdl;
   e->launches++;
-  return launch_gemm(p, epi, o, st);
+  prof_begin(e, st, kind, gemm_bytes(s, T, epi));
+  const cudaError_t r = launch_gemm(p, epi, o, st);
+  prof_end(e, st);
+  return r;
 }
 
 // Enqueues one forward over T packed tokens of R requests; requests [0, P) go to the packed prefill
-// kernel (n_items work items), [P, R) to the decode kernel with `splits` splits per row.
-static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, int splits, cudaStream_t st) {
+// kernel (n_items work items), [P, R) to the decode kernel with `splits` splits per row.  With
+// `advance`, a decode-only step ends by feeding its sampled ids back as the next inputs (advance.cu).
+static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, int splits, bool advance,
+                                   cudaStream_t st) {
   const eng_config_t& c = e->c;
   const int H = c.hidden, d = c.head_dim, Hq = c.q_heads, Hkv = c.kv_heads;
-  const int* in = e->d_in;
+  const int QKV = (Hq + 2 * Hkv) * d;
+  int* in = e->d_in;
   const size_t plane = (size_t)(c.num_blocks + 1) * Hkv * 16 * d;
+  const int64_t kv_tok = (int64_t)2 * Hkv * d * 2;  // K and V bytes of one position in one layer
+  int64_t kv_read = 0;                              // decode rows' K/V bytes per layer (profiling only)
+  if (e->prof_on)
+    for (int v : e->dec_seq) kv_read += (int64_t)v * kv_tok;
   LaunchOpts o;
   o.pdl = e->pdl;
   cudaError_t r;
@@ -477,24 +525,31 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
   np.w = e->layers[0].in_norm;
   np.y = e->y;
   e->launches++;
-  if ((r = launch_rmsnorm(np, true, o, st)) != cudaSuccess) return r;
+  prof_begin(e, st, ENG_K_EMBED_NORM, (int64_t)T * H * (2 + 4 + 2));
+  r = launch_rmsnorm(np, true, o, st);
+  prof_end(e, st);
+  if (r != cudaSuccess) return r;
 
   for (int l = 0; l < c.layers; ++l) {
     const Layer& L = e->layers[l];
+    NormParams nn{};
+    nn.h_in = e->h;
+    nn.y = e->y;
+    nn.rows = T;
+    nn.H = H;
+    nn.V = c.vocab;
+    nn.eps = c.rms_eps;
+    nn.status = e->status;
     if (l > 0) {
-      NormParams n2{};
-      n2.h_in = e->h;
-      n2.w = L.in_norm;
-      n2.y = e->y;
-      n2.rows = T;
-      n2.H = H;
-      n2.V = c.vocab;
-      n2.eps = c.rms_eps;
-      n2.status = e->status;
+      nn.w = L.in_norm;
       e->launches++;
-      if ((r = launch_rmsnorm(n2, false, o, st)) != cudaSuccess) return r;
+      prof_begin(e, st, ENG_K_NORM, (int64_t)T * H * (4 + 2));
+      r = launch_rmsnorm(nn, false, o, st);
+      prof_end(e, st);
+      if (r != cudaSuccess) return r;
     }
-    if ((r = gemm(e, e->g_qkv, L.qkv, e->y, T, EPI_STORE_F32, st, e->qkv, L.qkv_bias)) != cudaSuccess) return r;
+    if ((r = gemm(e, e->g_qkv, L.qkv, e->y, T, EPI_STORE_F32, ENG_K_GEMM_QKV, st, e->qkv, L.qkv_bias)) != cudaSuccess)
+      return r;
 
     bf16* kplane = e->kv + (size_t)l * 2 * plane;
     bf16* vplane = kplane + plane;
@@ -521,7 +576,10 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     rp.eps = c.rms_eps;
     rp.status = e->status;
     e->launches++;
-    if ((r = launch_rope_kv(rp, o, st)) != cudaSuccess) return r;
+    prof_begin(e, st, ENG_K_ROPE_KV, (int64_t)T * (QKV * 4 + Hq * d * 2) + (int64_t)T * kv_tok);
+    r = launch_rope_kv(rp, o, st);
+    prof_end(e, st);
+    if (r != cudaSuccess) return r;
 
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)d);
     if (P > 0) {
@@ -542,7 +600,10 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       ap.scale_log2 = scale_log2;
       ap.status = e->status;
       e->launches++;
-      if ((r = launch_attn_prefill(ap, o, st)) != cudaSuccess) return r;
+      prof_begin(e, st, ENG_K_ATTN_PREFILL, 0);
+      r = launch_attn_prefill(ap, o, st);
+      prof_end(e, st);
+      if (r != cudaSuccess) return r;
     }
     if (R > P) {
       AttnDecodeParams dp{};
@@ -567,23 +628,25 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       dp.scale_log2 = scale_log2;
       dp.status = e->status;
       e->launches++;
-      if ((r = launch_attn_decode(dp, o, st)) != cudaSuccess) return r;
+      prof_begin(e, st, ENG_K_ATTN_DECODE, kv_read + (int64_t)(R - P) * Hq * d * 4);
+      r = launch_attn_decode(dp, o, st);
+      prof_end(e, st);
+      if (r != cudaSuccess) return r;
     }
-    if ((r = gemm(e, e->g_o, L.o, e->attn, T, EPI_RESID, st, nullptr, nullptr, e->h)) != cudaSuccess) return r;
-
-    NormParams n3{};
-    n3.h_in = e->h;
-    n3.w = L.post_norm;
-    n3.y = e->y;
-    n3.rows = T;
-    n3.H = H;
-    n3.V = c.vocab;
-    n3.eps = c.rms_eps;
-    n3.status = e->status;
+    if ((r = gemm(e, e->g_o, L.o, e->attn, T, EPI_RESID, ENG_K_GEMM_O, st, nullptr, nullptr, e->h)) != cudaSuccess)
+      return r;
+    nn.w = L.post_norm;
     e->launches++;
-    if ((r = launch_rmsnorm(n3, false, o, st)) != cudaSuccess) return r;
-    if ((r = gemm(e, e->g_gu, L.gu, e->y, T, EPI_SILU, st, nullptr, nullptr, nullptr, e->act)) != cudaSuccess) return r;
-    if ((r = gemm(e, e->g_down, L.down, e->act, T, EPI_RESID, st, nullptr, nullptr, e->h)) != cudaSuccess) return r;
+    prof_begin(e, st, ENG_K_NORM, (int64_t)T * H * (4 + 2));
+    r = launch_rmsnorm(nn, false, o, st);
+    prof_end(e, st);
+    if (r != cudaSuccess) return r;
+    if ((r = gemm(e, e->g_gu, L.gu, e->y, T, EPI_SILU, ENG_K_GEMM_GATE_UP, st, nullptr, nullptr, nullptr, e->act)) !=
+        cudaSuccess)
+      return r;
+    if ((r = gemm(e, e->g_down, L.down, e->act, T, EPI_RESID, ENG_K_GEMM_DOWN, st, nullptr, nullptr, e->h)) !=
+        cudaSuccess)
+      return r;
   }
 
   NormParams nf{};
@@ -597,8 +660,33 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
   nf.eps = c.rms_eps;
   nf.status = e->status;
   e->launches++;
-  if ((r = launch_rmsnorm(nf, false, o, st)) != cudaSuccess) return r;
-  return gemm(e, e->g_lm, e->lm, e->ylast, R, EPI_LMHEAD, st);
+  prof_begin(e, st, ENG_K_NORM, (int64_t)R * H * (4 + 2));
+  r = launch_rmsnorm(nf, false, o, st);
+  prof_end(e, st);
+  if (r != cudaSuccess) return r;
+  if ((r = gemm(e, e->g_lm, e->lm, e->ylast, R, EPI_LMHEAD, ENG_K_LM_HEAD, st)) != cudaSuccess) return r;
+
+  if (advance) {
+    AdvanceParams ad{};
+    ad.sampled = e->ids;
+    ad.ids = in + e->in.ids;
+    ad.pos = in + e->in.pos;
+    ad.seq = in + e->in.seq;
+    ad.rng = reinterpret_cast<uint32_t*>(in + e->in.rng);
+    ad.step = in + e->in.step;
+    ad.ring = e->ring;
+    ad.ring_cap = e->ring_cap;
+    ad.rows = R;
+    ad.vocab = c.vocab;
+    ad.max_pos = e->max_pos;
+    ad.status = e->status;
+    e->launches++;
+    prof_begin(e, st, ENG_K_ADVANCE, (int64_t)R * 16);
+    r = launch_advance(ad, o, st);
+    prof_end(e, st);
+    if (r != cudaSuccess) return r;
+  }
+  return cudaSuccess;
 }
 
 // ------------------------------------------------------------------ staging
@@ -651,6 +739,11 @@ int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_w
     return fail(nullptr, ENG_ECUDA, "no CUDA device: the engine has no CPU path");
   eng_t* e = new eng_t();
   e->c = *cfg;
+  {
+    // programmatic dependent launch between the step's kernels (ENG_PDL=0 turns it off for comparison)
+    const char* v = getenv("ENG_PDL");
+    e->pdl = !(v && v[0] == '0');
+  }
   cudaGetDevice(&e->device);
   int rc = ENG_OK;
   if (cuda_stream) {
@@ -676,6 +769,7 @@ void eng_destroy(eng_t* e) {
   if (!e) return;
   if (e->stream) cudaStreamSynchronize(e->stream);
   for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
+  for (cudaEvent_t ev : e->prof_ev) cudaEventDestroy(ev);
   for (int i = 0; i < kSlots; ++i) {
     if (e->ev[i]) cudaEventDestroy(e->ev[i]);
     if (e->h_in[i]) cudaFreeHost(e->h_in[i]);
@@ -794,13 +888,13 @@ int eng_capture(eng_t* e, const int32_t* sizes, int32_t n) {
     // warm up on the engine stream (lazy attribute setup, first-touch), then record on a side stream
     for (int w = 0; w < 2; ++w) {
       e->launches = 0;
-      CUDA_OR_FAIL(e, enqueue_forward(e, size, size, 0, 0, e->max_splits, e->stream));
+      CUDA_OR_FAIL(e, enqueue_forward(e, size, size, 0, 0, e->max_splits, true, e->stream));
     }
     CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
     cudaGraph_t graph = nullptr;
     CUDA_OR_FAIL(e, cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal));
     e->launches = 0;
-    const cudaError_t le = enqueue_forward(e, size, size, 0, 0, e->max_splits, e->cap_stream);
+    const cudaError_t le = enqueue_forward(e, size, size, 0, 0, e->max_splits, true, e->cap_stream);
     const cudaError_t ce = cudaStreamEndCapture(e->cap_stream, &graph);
     if (le != cudaSuccess || ce != cudaSuccess) {
       if (graph) cudaGraphDestroy(graph);
@@ -930,7 +1024,7 @@ int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_log
     int max_blocks = 1;
     for (int r = P; r < R; ++r) max_blocks = std::max(max_blocks, (s->seq_lens[r] + 15) / 16);
     const int splits = (max_blocks + e->split_blocks - 1) / e->split_blocks;
-    CUDA_OR_FAIL(e, enqueue_forward(e, T, R, P, n_items, splits, e->stream));
+    CUDA_OR_FAIL(e, enqueue_forward(e, T, R, P, n_items, splits, decode_only, e->stream));
   }
   CUDA_OR_FAIL(e, cudaMemcpyAsync(out_ids_dev, e->ids, (size_t)R * 4, cudaMemcpyDeviceToDevice, e->stream));
   if (out_logits_dev)
@@ -941,6 +1035,93 @@ int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_log
   e->last.launches = e->launches;
   e->last.num_prefill = P;
   e->last.h2d_bytes = (int64_t)words * 4;
+  // the device inputs now hold the next decode step of this batch (advanced in place)
+  if (decode_only) {
+    e->dec_R = R;
+    e->dec_rows = rows;
+    e->dec_bt_stride = bs;
+    e->dec_seq.assign(s->seq_lens, s->seq_lens + R);
+    for (int& v : e->dec_seq) v += 1;
+  } else {
+    e->dec_R = 0;
+  }
+  return ENG_OK;
+}
+
+static int decode_capacity_check(eng_t* e, int n) {
+  if (e->dec_R == 0) return fail(e, ENG_ESTATE, "no decode batch to continue: the last eng_step was not decode-only");
+  int mx = 0;
+  for (int v : e->dec_seq) mx = std::max(mx, v);
+  const int limit = std::min(e->dec_bt_stride, e->c.max_blocks_per_seq) * 16;
+  if (mx + n - 1 > limit)
+    return fail(e, ENG_ECAPACITY, "decoding " + std::to_string(n) + " more steps needs " + std::to_string(mx + n - 1) +
+                                      " positions; the block tables hold " + std::to_string(limit));
+  return ENG_OK;
+}
+
+int eng_decode(eng_t* e, int32_t n_steps, int32_t* out_ids_dev) {
+  if (!e) return ENG_EINVAL;
+  if (n_steps < 0 || (n_steps > 0 && !out_ids_dev)) return fail(e, ENG_EINVAL, "bad eng_decode arguments");
+  if (n_steps == 0) return ENG_OK;
+  TRY(decode_capacity_check(e, n_steps));
+  const int R = e->dec_R, rows = e->dec_rows;
+  auto it = e->graphs.find(rows);
+  const bool replay = !e->eager_only && it != e->graphs.end();
+  int* step_word = e->d_in + e->in.step;
+  int done = 0;
+  while (done < n_steps) {
+    const int chunk = std::min(n_steps - done, e->ring_cap);
+    CUDA_OR_FAIL(e, cudaMemsetAsync(step_word, 0, 4, e->stream));
+    for (int i = 0; i < chunk; ++i) {
+      if (replay) {
+        CUDA_OR_FAIL(e, cudaGraphLaunch(it->second, e->stream));
+      } else {
+        e->launches = 0;
+        CUDA_OR_FAIL(e, enqueue_forward(e, rows, rows, 0, 0, e->max_splits, true, e->stream));
+      }
+    }
+    CUDA_OR_FAIL(e, cudaMemcpy2DAsync(out_ids_dev + (size_t)done * R, (size_t)R * 4, e->ring, (size_t)rows * 4,
+                                      (size_t)R * 4, chunk, cudaMemcpyDeviceToDevice, e->stream));
+    done += chunk;
+  }
+  for (int& v : e->dec_seq) v += n_steps;
+  e->last.replayed = replay ? 1 : 0;
+  e->last.bucket = rows;
+  e->last.launches = replay ? e->graph_launches[rows] : e->launches;
+  e->last.num_prefill = 0;
+  e->last.h2d_bytes = 0;
+  return ENG_OK;
+}
+
+int eng_profile(eng_t* e, int32_t capacity, int32_t* kinds, float* ms, int64_t* bytes, int32_t* count) {
+  if (!e) return ENG_EINVAL;
+  if (capacity < 1 || !kinds || !ms || !bytes || !count) return fail(e, ENG_EINVAL, "bad eng_profile arguments");
+  TRY(decode_capacity_check(e, 1));
+  const int rows = e->dec_rows;
+  while ((int)e->prof_ev.size() < 2 * capacity) {
+    cudaEvent_t ev;
+    CUDA_OR_FAIL(e, cudaEventCreate(&ev));
+    e->prof_ev.push_back(ev);
+  }
+  e->prof_kind.clear();
+  e->prof_bytes.clear();
+  e->prof_on = true;
+  e->launches = 0;
+  const cudaError_t r = enqueue_forward(e, rows, rows, 0, 0, e->max_splits, true, e->stream);
+  e->prof_on = false;
+  CUDA_OR_FAIL(e, r);
+  CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+  const int n = (int)e->prof_kind.size();
+  if (n > capacity) return fail(e, ENG_EINVAL, "eng_profile capacity too small");
+  for (int i = 0; i < n; ++i) {
+    float t = 0.f;
+    CUDA_OR_FAIL(e, cudaEventElapsedTime(&t, e->prof_ev[2 * i], e->prof_ev[2 * i + 1]));
+    kinds[i] = e->prof_kind[i];
+    ms[i] = t;
+    bytes[i] = e->prof_bytes[i];
+  }
+  *count = n;
+  for (int& v : e->dec_seq) v += 1;
   return ENG_OK;
 }
 

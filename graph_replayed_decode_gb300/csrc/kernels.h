@@ -135,6 +135,20 @@ struct AttnPrefillParams {
 };
 cudaError_t launch_attn_prefill(const AttnPrefillParams& p, const LaunchOpts& o, cudaStream_t s);
 
+// ------------------------------------------------------------------ decode advance (advance.cu)
+struct AdvanceParams {
+  const int* sampled;  // [rows] ids sampled by this step
+  int* ids;            // static inputs, advanced in place
+  int* pos;
+  int* seq;
+  uint32_t* rng;       // [4]: seed_lo, seed_hi, offset_lo, offset_hi (offset += 1)
+  int* step;           // ring write index
+  int* ring;           // [ring_cap][rows]
+  int ring_cap, rows, vocab, max_pos;
+  int* status;
+};
+cudaError_t launch_advance(const AdvanceParams& p, const LaunchOpts& o, cudaStream_t s);
+
 // ------------------------------------------------------------------ sampler pieces (sample.cu)
 cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int vocab, float* out, cudaStream_t s);
 cudaError_t launch_gumbel(const float* u, float* g, int64_t n, cudaStream_t s);

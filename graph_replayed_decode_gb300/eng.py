@@ -80,6 +80,9 @@ SIGNATURES = [
     ("eng_capture", ctypes.c_int, [ctypes.c_void_p, _I32P, ctypes.c_int32]),
     ("eng_step", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_t), ctypes.c_void_p, ctypes.c_void_p]),
     ("eng_last_step_info", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_info_t)]),
+    ("eng_decode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    ("eng_profile", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P, _F32P, ctypes.POINTER(ctypes.c_int64),
+                                   _I32P]),
     ("eng_pool_alloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P]),
     ("eng_pool_free", ctypes.c_int, [ctypes.c_void_p, _I32P, ctypes.c_int32]),
     ("eng_pool_free_count", ctypes.c_int32, [ctypes.c_void_p]),
@@ -208,6 +211,26 @@ def eng_last_step_info(e) -> eng_step_info_t:
     info = eng_step_info_t()
     _check(e, lib().eng_last_step_info(e, ctypes.byref(info)))
     return info
+
+
+def eng_decode(e, n_steps: int, out_ids_dev: int) -> None:
+    _check(e, lib().eng_decode(e, n_steps, out_ids_dev))
+
+
+KERNEL_KINDS = ["embed_norm", "norm", "gemm_qkv", "rope_kv", "attn_decode", "attn_prefill", "gemm_o",
+                "gemm_gate_up", "gemm_down", "lm_head", "advance"]
+
+
+def eng_profile(e, capacity: int = 4096):
+    """Per-launch (kind name, ms, algorithmic bytes) of one further decode step."""
+    kinds = np.zeros(capacity, dtype=np.int32)
+    ms = np.zeros(capacity, dtype=np.float32)
+    nbytes = np.zeros(capacity, dtype=np.int64)
+    n = ctypes.c_int32()
+    _check(e, lib().eng_profile(e, capacity, _ptr_i32(kinds), ms.ctypes.data_as(_F32P),
+                                nbytes.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), ctypes.byref(n)))
+    k = n.value
+    return [(KERNEL_KINDS[kinds[i]], float(ms[i]), int(nbytes[i])) for i in range(k)]
 
 
 def eng_pool_alloc(e, n: int) -> np.ndarray:

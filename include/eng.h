@@ -170,8 +170,46 @@ int eng_capture(eng_t* e, const int32_t* sizes, int32_t n);
  */
 int eng_step(eng_t* e, const eng_step_t* step, int32_t* out_ids_dev, float* out_logits_dev);
 
-/* eng_last_step_info -- what the last successful eng_step did. */
+/* eng_last_step_info -- what the last successful eng_step (or eng_decode) did. */
 int eng_last_step_info(const eng_t* e, eng_step_info_t* info);
+
+/*
+ * eng_decode -- run n_steps further pure-decode steps entirely on the device, continuing the batch of
+ * the last eng_step, which must have been decode-only.  "19. Fast decode", section "Static shapes and a
+ * static cache" and the fast decoder's step: run, sample, record, advance -- every step reads only
+ * static device buffers, so no host value depends on the GPU's results.  After each step a request's
+ * sampled id becomes its next input token, its position and sequence length grow by one, and the
+ * Philox offset grows by one.  Each step replays the captured graph of the last step's bucket (or runs
+ * eagerly when none applies), so its kernels and results are those of eng_step.
+ * out_ids_dev: device int32[n_steps][num_reqs], step-major, written in stream order; the call returns
+ * without waiting for the GPU.  The caller must already hold the KV blocks of the new positions in the
+ * block tables it passed to eng_step.  Errors: ENG_ESTATE (no decode batch to continue), ENG_ECAPACITY
+ * (a sequence would outgrow its block-table row or max_blocks_per_seq * 16), ENG_EINVAL, ENG_ECUDA.
+ */
+int eng_decode(eng_t* e, int32_t n_steps, int32_t* out_ids_dev);
+
+/* Kernel kinds reported by eng_profile. */
+#define ENG_K_EMBED_NORM 0
+#define ENG_K_NORM 1
+#define ENG_K_GEMM_QKV 2
+#define ENG_K_ROPE_KV 3
+#define ENG_K_ATTN_DECODE 4
+#define ENG_K_ATTN_PREFILL 5
+#define ENG_K_GEMM_O 6
+#define ENG_K_GEMM_GATE_UP 7
+#define ENG_K_GEMM_DOWN 8
+#define ENG_K_LM_HEAD 9
+#define ENG_K_ADVANCE 10
+
+/*
+ * eng_profile -- time every kernel of one further decode step of the current batch (as eng_decode with
+ * n_steps = 1, launched eagerly on the engine's stream) with a CUDA event pair around each launch, and
+ * report per launch its kind (ENG_K_*), duration in milliseconds and algorithmic HBM bytes (weights
+ * read once, activations in and out, K/V read over the rows' current lengths and written at the new
+ * position).  kinds/ms/bytes: host arrays of `capacity` entries; *count receives the launch count.
+ * Synchronises the stream.  Errors: ENG_ESTATE (no decode batch), ENG_EINVAL (capacity too small).
+ */
+int eng_profile(eng_t* e, int32_t capacity, int32_t* kinds, float* ms, int64_t* bytes, int32_t* count);
 
 /*
  * eng_pool_alloc / eng_pool_free -- the paged KV block pool ("One forward per

@@ -253,3 +253,40 @@ def test_host_validation_errors(weights):
         assert g.status() == 0
     finally:
         g.close()
+
+
+def test_device_decode_loop_equals_host_driven_steps(weights):
+    """eng_decode (sampled ids fed back on the device) == eng_step with the ids read back each step."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    from graph_replayed_decode_gb300.eng import StepArrays
+    g = _engine(weights)
+    try:
+        g.capture([4, 8])
+        st = _decode_batch(g, weights, 3, ctx=20)
+        ids0, _ = g.step(st)
+        n = 6
+        ring = torch.zeros((n, 3), dtype=torch.int32, device="cuda")
+        eng.eng_decode(g.h, n, ring.data_ptr())
+        torch.cuda.synchronize()
+        assert g.info().replayed == 1
+        dev = np.concatenate([ids0[None], ring.cpu().numpy()])
+        ids, pos = st.token_ids.copy(), st.positions.copy()
+        host = []
+        for k in range(n + 1):
+            s2 = StepArrays(ids, pos, np.arange(4), st.block_tables, pos + 1, st.temperature, seed=st.step.seed,
+                            offset=st.step.offset + k)
+            ids, _ = g.step(s2, want_logits=False)
+            host.append(ids.copy())
+            pos = pos + 1
+        np.testing.assert_array_equal(dev, np.stack(host))
+        prof = eng.eng_profile(g.h)
+        kinds = [k for k, _, _ in prof]
+        assert kinds.count("attn_decode") == S.layers and kinds[-1] == "advance" and kinds[-2] == "lm_head"
+        assert all(ms > 0 for _, ms, _ in prof)
+        with pytest.raises(eng.EngError) as ei:          # past the block tables' capacity
+            eng.eng_decode(g.h, 200, ring.data_ptr())
+        assert ei.value.code == eng.ENG_ECAPACITY
+        assert g.status() == 0
+    finally:
+        g.close()
