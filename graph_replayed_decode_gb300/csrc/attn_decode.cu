@@ -30,7 +30,6 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   const int G = p.Hq / p.Hkv;
   const int h0 = kvh * G;
 
-  pdl_wait();
   const int r = p.r0 + row;
   const int sl = p.seq_lens[r];
   const int tok = p.cu[r];
@@ -42,6 +41,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   }
   const int nsplit = min((nblk + p.split_blocks - 1) / p.split_blocks, p.max_splits);
   if (sl <= 0) {  // padding row: zeros
+    pdl_wait();
     if (split == 0)
       for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
     return;
@@ -52,18 +52,6 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
 
   extern __shared__ __align__(16) uint8_t smem[];
   bf16* wbuf = reinterpret_cast<bf16*>(smem) + warp * (4 * TILE);  // 2 stages x (K, V)
-
-  // Q fragments: rows = the G query heads (rows >= G are zero), k = head dimension
-  uint32_t qa[KS][4];
-  const bf16* qb = p.q + (size_t)tok * p.Hq * D + (size_t)h0 * D;
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    const int d0 = ks * 16 + 2 * t;
-    qa[ks][0] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0) : 0u;
-    qa[ks][1] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0) : 0u;
-    qa[ks][2] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0 + 8) : 0u;
-    qa[ks][3] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0 + 8) : 0u;
-  }
 
   float o[D / 8][4];
 #pragma unroll
@@ -92,7 +80,24 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
 
   int b = b_begin + warp;
   int stage = 0;
-  if (b < b_end) issue(b, 0);
+  // context blocks already in the pool can be fetched before the preceding kernel finishes; the block that
+  // holds this step's new token (the last one) is written by that kernel
+  const bool early = b < b_end && b != nblk - 1;
+  if (early) issue(b, 0);
+  pdl_wait();
+  if (b < b_end && !early) issue(b, 0);
+  // Q fragments: rows = the G query heads (rows >= G are zero), k = head dimension
+  uint32_t qa[KS][4];
+  const bf16* qb = p.q + (size_t)tok * p.Hq * D + (size_t)h0 * D;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    const int d0 = ks * 16 + 2 * t;
+    qa[ks][0] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0) : 0u;
+    qa[ks][1] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0) : 0u;
+    qa[ks][2] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0 + 8) : 0u;
+    qa[ks][3] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0 + 8) : 0u;
+  }
+
   for (; b < b_end; b += 4) {
     if (b + 4 < b_end) {
       issue(b + 4, stage ^ 1);
@@ -250,18 +255,33 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   if (!s_last) return;
   __threadfence();
   const float* base = p.ws + ((size_t)row * p.Hkv + kvh) * p.max_splits * (size_t)G * (D + 2);
+  // split weights exp2(M_s - M) and the total L per head row, all loads in flight at once
+  float* sw = reinterpret_cast<float*>(smem);   // [nsplit][G] weights
+  float* sm = sw + p.max_splits * G;            // [G] merged max, then [G] 1 / L
+  for (int i = threadIdx.x; i < nsplit * G; i += blockDim.x) {
+    const int sp = i / G, hr = i - sp * G;
+    sw[i] = __ldcg(base + ((size_t)sp * G + hr) * (D + 2) + D);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int hr = threadIdx.x;
+    float M = -INFINITY;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, sw[sp * G + hr]);
+    float L = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float w = exp2f(sw[sp * G + hr] - M);
+      sw[sp * G + hr] = w;
+      L += __ldcg(base + ((size_t)sp * G + hr) * (D + 2) + D + 1) * w;
+    }
+    sm[hr] = 1.f / L;
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int hr = i / D, dd = i - hr * D;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(base + ((size_t)sp * G + hr) * (D + 2) + D));
-    float L = 0.f, O = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float* q_ = base + ((size_t)sp * G + hr) * (D + 2);
-      const float sc_ = exp2f(__ldcg(q_ + D) - M);
-      L += __ldcg(q_ + D + 1) * sc_;
-      O += __ldcg(q_ + dd) * sc_;
-    }
-    out[hr * D + dd] = __float2bfloat16_rn(O / L);
+    float O = 0.f;
+#pragma unroll 8
+    for (int sp = 0; sp < nsplit; ++sp) O += __ldcg(base + ((size_t)sp * G + hr) * (D + 2) + dd) * sw[sp * G + hr];
+    out[hr * D + dd] = __float2bfloat16_rn(O * sm[hr]);
   }
 }
 

@@ -55,8 +55,8 @@ struct InLayout {
 };
 
 struct GemmSite {
-  int N = 0, K = 0, RG = 1, S = 1, ktn = 0;
-  int* tickets = nullptr;
+  int N = 0, K = 0, RG = 1, S = 1, ktn = 0, rg_fixed = 0;
+  int groups() const { return N / 16 / RG; }
 };
 
 }  // namespace
@@ -93,7 +93,8 @@ struct eng {
   // activations and outputs
   float* h = nullptr;      // [Tm][H]
   bf16* y = nullptr;       // [Tm][H]
-  float* qkv = nullptr;    // [Tm][QKV]
+  float* sq = nullptr;     // [Tm][sq_stride] per-token partial sums of squares of the residual
+  int sq_stride = 1;
   bf16* q = nullptr;       // [Tm][Hq][d]
   bf16* attn = nullptr;    // [Tm][Hq d]
   bf16* act = nullptr;     // [Tm][I]
@@ -101,7 +102,6 @@ struct eng {
   float* logits = nullptr; // [Rm][V]
   int* ids = nullptr;      // [Rm]
   int* slots = nullptr;    // [Tm]
-  float* gemm_ws = nullptr;
   float* attn_ws = nullptr;
   int* attn_tickets = nullptr;
   unsigned long long* best = nullptr;
@@ -387,7 +387,6 @@ static int setup_buffers(eng_t* e) {
 
   TRY(dev_alloc(e, &e->h, (size_t)Tm * H));
   TRY(dev_alloc(e, &e->y, (size_t)Tm * H));
-  TRY(dev_alloc(e, &e->qkv, (size_t)Tm * QKV));
   TRY(dev_alloc(e, &e->q, (size_t)Tm * c.q_heads * d));
   TRY(dev_alloc(e, &e->attn, (size_t)Tm * c.q_heads * d));
   TRY(dev_alloc(e, &e->act, (size_t)Tm * c.intermediate));
@@ -400,24 +399,20 @@ static int setup_buffers(eng_t* e) {
   TRY(dev_alloc(e, &e->status, 4));
   TRY(dev_alloc(e, &e->ring, (size_t)e->ring_cap * Rm));
 
-  auto site = [&](GemmSite& s, int N, int K, int T) -> int {
+  auto site = [&](GemmSite& s, int N, int K, int rg_fixed, int /*T*/) -> int {
     s.N = N;
     s.K = K;
-    gemm_plan(N, K, &s.RG, &s.S, &s.ktn);
-    return dev_alloc(e, &s.tickets, gemm_tickets(N, K, T) + 1);
+    s.rg_fixed = rg_fixed;
+    gemm_plan(N, K, rg_fixed, &s.RG, &s.S, &s.ktn);
+    return ENG_OK;
   };
-  TRY(site(e->g_qkv, QKV, H, Tm));
-  TRY(site(e->g_o, H, c.q_heads * d, Tm));
-  TRY(site(e->g_gu, 2 * c.intermediate, H, Tm));
-  TRY(site(e->g_down, H, c.intermediate, Tm));
-  TRY(site(e->g_lm, c.vocab, H, Rm));
-  size_t ws = 0;
-  ws = std::max(ws, gemm_ws_floats(QKV, H, Tm));
-  ws = std::max(ws, gemm_ws_floats(H, c.q_heads * d, Tm));
-  ws = std::max(ws, gemm_ws_floats(2 * c.intermediate, H, Tm));
-  ws = std::max(ws, gemm_ws_floats(H, c.intermediate, Tm));
-  ws = std::max(ws, gemm_ws_floats(c.vocab, H, Rm));
-  TRY(dev_alloc(e, &e->gemm_ws, ws + 4));
+  TRY(site(e->g_qkv, QKV, H, d / 16, Tm));  // a CTA owns one whole head (QK-norm and RoPE in the epilogue)
+  TRY(site(e->g_o, H, c.q_heads * d, 0, Tm));
+  TRY(site(e->g_gu, 2 * c.intermediate, H, 0, Tm));
+  TRY(site(e->g_down, H, c.intermediate, 0, Tm));
+  TRY(site(e->g_lm, c.vocab, H, 0, Rm));
+  e->sq_stride = std::max(e->g_o.groups(), e->g_down.groups());
+  TRY(dev_alloc(e, &e->sq, (size_t)Tm * e->sq_stride));
 
   // decode attention splits: 16-key blocks per split chosen from the block-table width so that a row
   // never needs more than 32 splits; fixed per engine, so eager and replayed steps agree bit for bit
@@ -448,21 +443,20 @@ static void prof_end(eng_t* e, cudaStream_t st) {
   cudaEventRecord(e->prof_ev[2 * (e->prof_kind.size() - 1) + 1], st);
 }
 
-static int64_t gemm_bytes(const GemmSite& s, int T, int epi) {
-  int64_t b = (int64_t)s.N * s.K * 2 + (int64_t)T * s.K * 2;  // weights once + activations in
+static int64_t gemm_bytes(const GemmSite& s, int T, int epi, bool norm_in) {
+  int64_t b = (int64_t)s.N * s.K * 2;                          // weights once
+  b += norm_in ? (int64_t)T * s.K * 4 : (int64_t)T * s.K * 2;   // activations in (fp32 residual or bf16)
   if (epi == EPI_STORE_F32) b += (int64_t)T * s.N * 4;
-  if (epi == EPI_RESID) b += (int64_t)T * s.N * 8;            // residual read + write
+  if (epi == EPI_RESID) b += (int64_t)T * s.N * 8;              // residual read + write
   if (epi == EPI_SILU) b += (int64_t)T * (s.N / 2) * 2;
   if (epi == EPI_LMHEAD) b += (int64_t)T * 4;
   return b;
 }
 
-static cudaError_t gemm(eng_t* e, const GemmSite& s, const bf16* W, const bf16* X, int T, int epi, int kind,
-                        cudaStream_t st, float* out_f32 = nullptr, const float* bias = nullptr,
-                        float* resid = nullptr, bf16* out_bf16 = nullptr) {
+// Parameters shared by every GEMM launch of the engine.
+static GemmParams gemm_params(eng_t* e, const GemmSite& s, const bf16* W, int T) {
   GemmParams p{};
   p.W = W;
-  p.X = X;
   p.ldx = s.K;
   p.T = T;
   p.N = s.N;
@@ -470,14 +464,10 @@ static cudaError_t gemm(eng_t* e, const GemmSite& s, const bf16* W, const bf16* 
   p.RG = s.RG;
   p.S = s.S;
   p.kt_per_split = s.ktn;
-  p.ws = e->gemm_ws;
-  p.tickets = s.tickets;
-  p.out_f32 = out_f32;
   p.ldo = s.N;
-  p.bias = bias;
-  p.resid = resid;
-  p.out_bf16 = out_bf16;
-  const int* in = e->d_in;
+  p.eps = e->c.rms_eps;
+  p.sq_stride = e->sq_stride;
+  int* in = e->d_in;
   p.logits = e->logits;
   p.write_logits = in + e->in.wlog;
   p.inv_temp = reinterpret_cast<const float*>(in + e->in.invt);
@@ -486,11 +476,16 @@ static cudaError_t gemm(eng_t* e, const GemmSite& s, const bf16* W, const bf16* 
   p.done_counter = e->done_counter;
   p.out_ids = e->ids;
   p.status = e->status;
+  return p;
+}
+
+static cudaError_t gemm_launch(eng_t* e, const GemmParams& p, const GemmSite& s, int epi, bool norm_in, int kind,
+                               cudaStream_t st) {
   LaunchOpts o;
   o.pdl = e->pdl;
   e->launches++;
-  prof_begin(e, st, kind, gemm_bytes(s, T, epi));
-  const cudaError_t r = launch_gemm(p, epi, o, st);
+  prof_begin(e, st, kind, gemm_bytes(s, p.T, epi, norm_in));
+  const cudaError_t r = launch_gemm(p, epi, norm_in, o, st);
   prof_end(e, st);
   return r;
 }
@@ -502,7 +497,6 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
                                    cudaStream_t st) {
   const eng_config_t& c = e->c;
   const int H = c.hidden, d = c.head_dim, Hq = c.q_heads, Hkv = c.kv_heads;
-  const int QKV = (Hq + 2 * Hkv) * d;
   int* in = e->d_in;
   const size_t plane = (size_t)(c.num_blocks + 1) * Hkv * 16 * d;
   const int64_t kv_tok = (int64_t)2 * Hkv * d * 2;  // K and V bytes of one position in one layer
@@ -513,74 +507,55 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
   o.pdl = e->pdl;
   cudaError_t r;
 
-  NormParams np{};
-  np.H = H;
-  np.V = c.vocab;
-  np.eps = c.rms_eps;
-  np.status = e->status;
-  np.rows = T;
-  np.h_out = e->h;
-  np.embed = e->embed;
-  np.ids = in + e->in.ids;
-  np.w = e->layers[0].in_norm;
-  np.y = e->y;
+  EmbedParams ep{};
+  ep.embed = e->embed;
+  ep.ids = in + e->in.ids;
+  ep.h_out = e->h;
+  ep.sq_out = e->sq;
+  ep.sq_stride = e->sq_stride;
+  ep.rows = T;
+  ep.H = H;
+  ep.V = c.vocab;
+  ep.status = e->status;
   e->launches++;
-  prof_begin(e, st, ENG_K_EMBED_NORM, (int64_t)T * H * (2 + 4 + 2));
-  r = launch_rmsnorm(np, true, o, st);
+  prof_begin(e, st, ENG_K_EMBED_NORM, (int64_t)T * H * (2 + 4));
+  r = launch_embed(ep, o, st);
   prof_end(e, st);
   if (r != cudaSuccess) return r;
+  int sq_parts = 1;  // producers of the residual's partial sums: embed (1), then o_proj / down row groups
 
   for (int l = 0; l < c.layers; ++l) {
     const Layer& L = e->layers[l];
-    NormParams nn{};
-    nn.h_in = e->h;
-    nn.y = e->y;
-    nn.rows = T;
-    nn.H = H;
-    nn.V = c.vocab;
-    nn.eps = c.rms_eps;
-    nn.status = e->status;
-    if (l > 0) {
-      nn.w = L.in_norm;
-      e->launches++;
-      prof_begin(e, st, ENG_K_NORM, (int64_t)T * H * (4 + 2));
-      r = launch_rmsnorm(nn, false, o, st);
-      prof_end(e, st);
-      if (r != cudaSuccess) return r;
-    }
-    if ((r = gemm(e, e->g_qkv, L.qkv, e->y, T, EPI_STORE_F32, ENG_K_GEMM_QKV, st, e->qkv, L.qkv_bias)) != cudaSuccess)
-      return r;
-
     bf16* kplane = e->kv + (size_t)l * 2 * plane;
     bf16* vplane = kplane + plane;
-    RopeKvParams rp{};
-    rp.qkv = e->qkv;
-    rp.positions = in + e->in.pos;
-    rp.tok2req = in + e->in.tok2req;
-    rp.seq_lens = in + e->in.seq;
-    rp.bt = in + e->in.bt;
-    rp.mbs = c.max_blocks_per_seq;
-    rp.q_norm = L.q_norm;
-    rp.k_norm = L.k_norm;
-    rp.cos_sin = e->rope;
-    rp.max_pos = e->max_pos;
-    rp.q_out = e->q;
-    rp.k_pool = kplane;
-    rp.v_pool = vplane;
-    rp.slots = e->slots;
-    rp.T = T;
-    rp.Hq = Hq;
-    rp.Hkv = Hkv;
-    rp.d = d;
-    rp.NB = c.num_blocks;
-    rp.eps = c.rms_eps;
-    rp.status = e->status;
-    e->launches++;
-    prof_begin(e, st, ENG_K_ROPE_KV, (int64_t)T * (QKV * 4 + Hq * d * 2) + (int64_t)T * kv_tok);
-    r = launch_rope_kv(rp, o, st);
-    prof_end(e, st);
-    if (r != cudaSuccess) return r;
 
+    // ---- input RMSNorm + fused QKV projection + QK-norm + RoPE + paged KV write
+    GemmParams q = gemm_params(e, e->g_qkv, L.qkv, T);
+    q.h_in = e->h;
+    q.norm_w = L.in_norm;
+    q.sq_in = e->sq;
+    q.sq_parts = sq_parts;
+    q.bias = L.qkv_bias;
+    q.positions = in + e->in.pos;
+    q.tok2req = in + e->in.tok2req;
+    q.seq_lens = in + e->in.seq;
+    q.bt = in + e->in.bt;
+    q.mbs = c.max_blocks_per_seq;
+    q.q_norm = L.q_norm;
+    q.k_norm = L.k_norm;
+    q.cos_sin = e->rope;
+    q.max_pos = e->max_pos;
+    q.q_out = e->q;
+    q.k_pool = kplane;
+    q.v_pool = vplane;
+    q.slots = e->slots;
+    q.Hq = Hq;
+    q.Hkv = Hkv;
+    q.d = d;
+    q.NB = c.num_blocks;
+    if ((r = gemm_launch(e, q, e->g_qkv, EPI_QKV_ROPE, true, ENG_K_GEMM_QKV, st)) != cudaSuccess) return r;
+
+    // ---- attention, split by kind inside the step
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)d);
     if (P > 0) {
       AttnPrefillParams ap{};
@@ -633,38 +608,41 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       prof_end(e, st);
       if (r != cudaSuccess) return r;
     }
-    if ((r = gemm(e, e->g_o, L.o, e->attn, T, EPI_RESID, ENG_K_GEMM_O, st, nullptr, nullptr, e->h)) != cudaSuccess)
-      return r;
-    nn.w = L.post_norm;
-    e->launches++;
-    prof_begin(e, st, ENG_K_NORM, (int64_t)T * H * (4 + 2));
-    r = launch_rmsnorm(nn, false, o, st);
-    prof_end(e, st);
-    if (r != cudaSuccess) return r;
-    if ((r = gemm(e, e->g_gu, L.gu, e->y, T, EPI_SILU, ENG_K_GEMM_GATE_UP, st, nullptr, nullptr, nullptr, e->act)) !=
-        cudaSuccess)
-      return r;
-    if ((r = gemm(e, e->g_down, L.down, e->act, T, EPI_RESID, ENG_K_GEMM_DOWN, st, nullptr, nullptr, e->h)) !=
-        cudaSuccess)
-      return r;
+
+    // ---- output projection + residual (+ sums of squares for the next norm)
+    GemmParams po = gemm_params(e, e->g_o, L.o, T);
+    po.X = e->attn;
+    po.resid = e->h;
+    po.sq_out = e->sq;
+    if ((r = gemm_launch(e, po, e->g_o, EPI_RESID, false, ENG_K_GEMM_O, st)) != cudaSuccess) return r;
+    sq_parts = e->g_o.groups();
+
+    // ---- post-attention RMSNorm + fused gate|up projection + SiLU * up
+    GemmParams pg = gemm_params(e, e->g_gu, L.gu, T);
+    pg.h_in = e->h;
+    pg.norm_w = L.post_norm;
+    pg.sq_in = e->sq;
+    pg.sq_parts = sq_parts;
+    pg.out_bf16 = e->act;
+    if ((r = gemm_launch(e, pg, e->g_gu, EPI_SILU, true, ENG_K_GEMM_GATE_UP, st)) != cudaSuccess) return r;
+
+    // ---- down projection + residual
+    GemmParams pd = gemm_params(e, e->g_down, L.down, T);
+    pd.X = e->act;
+    pd.resid = e->h;
+    pd.sq_out = e->sq;
+    if ((r = gemm_launch(e, pd, e->g_down, EPI_RESID, false, ENG_K_GEMM_DOWN, st)) != cudaSuccess) return r;
+    sq_parts = e->g_down.groups();
   }
 
-  NormParams nf{};
-  nf.h_in = e->h;
-  nf.row_index = in + e->in.last;
-  nf.w = e->final_norm;
-  nf.y = e->ylast;
-  nf.rows = R;
-  nf.H = H;
-  nf.V = c.vocab;
-  nf.eps = c.rms_eps;
-  nf.status = e->status;
-  e->launches++;
-  prof_begin(e, st, ENG_K_NORM, (int64_t)R * H * (4 + 2));
-  r = launch_rmsnorm(nf, false, o, st);
-  prof_end(e, st);
-  if (r != cudaSuccess) return r;
-  if ((r = gemm(e, e->g_lm, e->lm, e->ylast, R, EPI_LMHEAD, ENG_K_LM_HEAD, st)) != cudaSuccess) return r;
+  // ---- final RMSNorm at each request's last token + LM head + sampling
+  GemmParams pl = gemm_params(e, e->g_lm, e->lm, R);
+  pl.h_in = e->h;
+  pl.norm_w = e->final_norm;
+  pl.sq_in = e->sq;
+  pl.sq_parts = sq_parts;
+  pl.x_rows = in + e->in.last;
+  if ((r = gemm_launch(e, pl, e->g_lm, EPI_LMHEAD, true, ENG_K_LM_HEAD, st)) != cudaSuccess) return r;
 
   if (advance) {
     AdvanceParams ad{};

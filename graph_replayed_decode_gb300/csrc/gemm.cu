@@ -1,37 +1,97 @@
 // gemm.cu -- skinny GEMM Y[T][N] = X[T][K] . W[N][K]^T for the decode-sized projections, with the
-// step's elementwise work fused into its epilogue.
+// step's norms and elementwise work fused into its prologue and epilogue.
 //
 // Shapes: T is the packed token count of the step (1..64 in decode, larger in prefill, handled in
 // 64-token chunks), N the output width, K the reduction width.  "33. Removing overhead", section "Fewer,
-// larger matmuls": Q/K/V and gate/up are each one matmul over a concatenated matrix; the same section
-// lists fusing SiLU-and-mul, RoPE, and the LM head with sampling into the producing kernels.
+// larger matmuls": Q/K/V and gate/up are each one matmul over a concatenated matrix; add_norm does the
+// residual add and the next norm in one memory pass; and the fusions production engines use -- SiLU-and-mul,
+// RoPE inside the KV write, the LM head with sampling -- save a pass over memory and a launch each.
 //
-// Design (HBM-bound at decode sizes):
-//   * W is pre-packed in m16n8k16 fragment order (common.cuh), so each lane streams its A fragments
-//     with 16-byte loads straight from HBM -- every byte of W is read exactly once per chunk;
-//   * X is staged through shared memory in 512-column pieces and read with ldmatrix;
-//   * a CTA owns RG 16-row tiles and one of S K-ranges; its 8 warps split the K-range, reduce through
-//     shared memory in a fixed order, and when S > 1 the last CTA of a row group (atomic ticket, no
-//     waiting) adds the S partials in split order -- so results are deterministic and do not depend
-//     on T, which makes graph replay and eager execution bit-identical;
-//   * epilogues: fp32 store (+bias), residual add into the fp32 stream, SiLU(gate)*up on row-interleaved
-//     gate|up tiles, and the LM head: logits (optional) plus a per-token running (key, index) maximum
-//     for greedy / Gumbel-max sampling, finished by the last CTA.
+// At decode sizes the kernel is bound by the latency of its dependent memory round trips, not by
+// bandwidth, so the design minimises the work left after the previous kernel finishes:
+//   * W is pre-packed in m16n8k16 fragment order (common.cuh).  Before waiting for its inputs
+//     (griddepcontrol.wait) every warp loads its first k-tiles' A fragments into registers and the CTA
+//     asks L2 to prefetch the rest of its slice, so weight streaming overlaps the preceding kernel;
+//   * X is staged through shared memory (in one piece when it fits) and read with ldmatrix.  With a norm
+//     prologue X = RMSNorm(h) * w is computed from the fp32 residual h and the per-token partial sums of
+//     squares its producer wrote (EPI_RESID), a warp per token, so no norm kernel runs;
+//   * a CTA owns RG 16-row tiles and one of S K-ranges; its 8 warps split the K-range and sum in a fixed
+//     order; the S CTAs of a row group form a thread-block cluster and add their tiles through distributed
+//     shared memory, always in split order (each CTA finishing every S-th token) -- deterministic and
+//     independent of T, so graph replay and eager execution are bit-identical;
+//   * epilogues run over the finished [16 RG rows x tokens] tile in shared memory:
+//       EPI_STORE_F32  out = Y (+bias)
+//       EPI_RESID      h += Y, plus each token's sum of h^2 over this CTA's rows (for the next norm)
+//       EPI_SILU       out = silu(gate) * up on row-interleaved gate|up tiles
+//       EPI_QKV_ROPE   the CTA's rows are whole heads: +bias, per-head QK-RMSNorm, rotate-half RoPE, and the
+//                      paged KV write (q heads -> q buffer, k/v heads -> pool slot of the token)
+//       EPI_LMHEAD     logits (optional) and a per-token (key, index) maximum for greedy / Gumbel-max
+//                      sampling; the last CTA turns the maxima into token ids.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "sampling.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace grd {
 
-static constexpr int kPieceTiles = 16;  // k-tiles (x32 columns) of X staged per piece
+static constexpr int kPieceTiles = 16;          // k-tiles (x32 columns) per X piece when X does not fit whole
+static constexpr int kPre = 4;                  // k-tiles per warp loaded into registers before waiting
+static constexpr size_t kWholeXBytes = 64 * 1024;
+static constexpr int kMaxClusterDev = 8;        // largest split-K cluster
+static constexpr int kCsTokens = 8;             // tokens whose RoPE row is staged before the wait
 
-template <int NT, int EPI>
+ENG_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Shared-memory plan of one launch (host and device agree on it).
+struct GemmSmem {
+  int piece;       // k-tiles of X staged per piece
+  size_t x_bytes;  // X staging
+  size_t red_bytes;
+  size_t ts_bytes;
+  size_t total;
+};
+
+__host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn) {
+  GemmSmem m;
+  const size_t whole = (size_t)NT * 8 * (ktn * 32 + 8) * 2;
+  m.piece = whole <= kWholeXBytes ? ktn : (ktn < kPieceTiles ? ktn : kPieceTiles);
+  m.x_bytes = (size_t)NT * 8 * (m.piece * 32 + 8) * 2;
+  m.red_bytes = (size_t)8 * NT * 32 * 16;
+  m.ts_bytes = (size_t)16 * RG * (NT * 8 + 1) * 4;
+  const size_t tail = m.red_bytes + m.ts_bytes;
+  m.total = m.x_bytes > tail ? m.x_bytes : tail;
+  return m;
+}
+
+template <int NT>
+ENG_DEVICE void mma_tile(float (&acc)[NT][4], const uint4& a0, const uint4& a1, const bf16* xs, int xstride, int kt,
+                         int lane) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    uint32_t b[4];
+    const int m = lane >> 3;
+    ldmatrix_x4(b, xs + (nt * 8 + (lane & 7)) * xstride + kt * 32 + (m >> 1) * 16 + (m & 1) * 8);
+    mma_bf16(acc[nt], a0.x, a0.y, a0.z, a0.w, b[0], b[1]);
+    mma_bf16(acc[nt], a1.x, a1.y, a1.z, a1.w, b[2], b[3]);
+  }
+}
+
+template <int NT, int EPI, bool NORM_IN>
 __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float s_rstd[64];
+  __shared__ int s_flag;
+  __shared__ int s_slot[64];           // EPI_QKV_ROPE: KV slot of each finished token (-1 padding, -2 bad)
+  __shared__ int s_pos[64];            //               and its position
+  __shared__ float s_cs[kCsTokens][128];  //          and its RoPE row (cos, sin pairs) for the first tokens
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
   const int rgi = blockIdx.x, split = blockIdx.y, chunk = blockIdx.z;
-  const int nRG = gridDim.x;
+  const int S = p.S;
   const int n0 = chunk * 64;
   const int KT = p.K >> 5;
   const int ktn = p.kt_per_split;
@@ -39,33 +99,141 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
   const int RG = p.RG, KG = 8 / RG;
   const int rt = warp % RG, kg = warp / RG;
   const int row_tile = rgi * RG + rt;
+  const int ntok = min(NT * 8, p.T - n0);  // valid tokens of this chunk
+  const GemmSmem sm = gemm_smem(NT, RG, ktn);
 
+  // ---- before waiting: weights do not depend on the preceding kernel
+  const uint4* wp = reinterpret_cast<const uint4*>(p.W) + ((size_t)row_tile * KT + kt0) * 64 + lane;
+  const int pn0 = min(sm.piece, ktn);
+  uint4 pre[kPre][2];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int kt = kg + u * KG;
+    if (kt < pn0) {
+      pre[u][0] = ld_stream16(wp + (size_t)kt * 64);
+      pre[u][1] = ld_stream16(wp + (size_t)kt * 64 + 32);
+    } else {
+      pre[u][0] = pre[u][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (threadIdx.x < RG && ktn > kPre * KG)
+    prefetch_l2(p.W + ((size_t)(rgi * RG + threadIdx.x) * KT + kt0) * 512, (uint32_t)ktn * 1024u);
+
+  // tokens this CTA finishes: split, split + S, ... (all of them when S == 1)
+  const int tok_first = S > 1 ? split : 0;
+  const int tok_step = S;
+  const int nown = tok_first < ntok ? (ntok - tok_first + tok_step - 1) / tok_step : 0;
+  if (EPI == EPI_QKV_ROPE) {
+    // step inputs (positions, lengths, block tables) are final before the step's first kernel: resolve
+    // each token's KV slot and fetch its RoPE row while the preceding kernel still runs
+    if (threadIdx.x < nown) {
+      const int tkn = n0 + tok_first + threadIdx.x * tok_step;
+      const int rq = p.tok2req[tkn];
+      const int pos = p.positions[tkn];
+      int slot = -1;
+      if (p.seq_lens[rq] != 0) {
+        if (pos < 0 || (pos >> 4) >= p.mbs || pos >= p.max_pos) {
+          slot = -2;
+        } else {
+          const int bb = p.bt[(size_t)rq * p.mbs + (pos >> 4)];
+          slot = (bb < 0 || bb >= p.NB) ? -3 : bb * 16 + (pos & 15);
+        }
+      }
+      s_slot[threadIdx.x] = slot;
+      s_pos[threadIdx.x] = (pos < 0 || pos >= p.max_pos) ? 0 : pos;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < min(nown, kCsTokens) * p.d; i += 256) {
+      const int k = i / p.d, j = i - k * p.d;
+      s_cs[k][j] = p.cos_sin[(size_t)s_pos[k] * p.d + j];
+    }
+  }
+  float4 wn_pre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  const int cpr0 = pn0 * 4;
+  const bool reg_stage = NORM_IN && ntok * cpr0 <= 256;  // one 8-column chunk of X per thread
+  if (reg_stage && threadIdx.x < ntok * cpr0) {
+    const float4* wn = reinterpret_cast<const float4*>(p.norm_w + kt0 * 32 + (threadIdx.x % cpr0) * 8);
+    wn_pre[0] = wn[0];
+    wn_pre[1] = wn[1];
+  }
+  pdl_trigger();
   pdl_wait();
+  float4 h_pre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  if (reg_stage && threadIdx.x < ntok * cpr0) {  // in flight together with the partial sums below
+    const int r = threadIdx.x / cpr0;
+    const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
+    const float4* hp = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K + kt0 * 32 + (threadIdx.x % cpr0) * 8);
+    h_pre[0] = hp[0];
+    h_pre[1] = hp[1];
+  }
+
+  if (NORM_IN) {  // 1 / rms of each staged token, from its producer's partial sums of squares
+    for (int r = warp; r < NT * 8; r += 8) {
+      float ss = 0.f;
+      if (r < ntok) {
+        const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
+        const float* part = p.sq_in + (size_t)src * p.sq_stride;
+        for (int j = lane; j < p.sq_parts; j += 32) ss += part[j];
+        ss = warp_sum(ss);
+      }
+      if (lane == 0) s_rstd[r] = r < ntok ? rsqrtf(ss / (float)p.K + p.eps) : 0.f;
+    }
+    __syncthreads();
+  }
 
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
   bf16* xs = reinterpret_cast<bf16*>(smem);
-  const uint4* wp = reinterpret_cast<const uint4*>(p.W) + ((size_t)row_tile * KT + kt0) * 64 + lane;
-
-  for (int pc = 0; pc < ktn; pc += kPieceTiles) {
-    const int pn = min(kPieceTiles, ktn - pc);
+  for (int pc = 0; pc < ktn; pc += sm.piece) {
+    const int pn = min(sm.piece, ktn - pc);
     const int xstride = pn * 32 + 8;
     const int cpr = pn * 4;  // 16-byte chunks per staged row
     if (pc > 0) __syncthreads();
     for (int i = threadIdx.x; i < NT * 8 * cpr; i += 256) {
       const int r = i / cpr, c = i - r * cpr;
-      const int tok = n0 + r;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (tok < p.T)
-        v = *reinterpret_cast<const uint4*>(p.X + (size_t)tok * p.ldx + (size_t)(kt0 + pc) * 32 + c * 8);
+      if (reg_stage && pc == 0) {
+        if (r < ntok) {
+          const float rs = s_rstd[r];
+          const float4 a = h_pre[0], b = h_pre[1], wa = wn_pre[0], wb = wn_pre[1];
+          v.x = pack_bf16x2(a.x * rs * wa.x, a.y * rs * wa.y);
+          v.y = pack_bf16x2(a.z * rs * wa.z, a.w * rs * wa.w);
+          v.z = pack_bf16x2(b.x * rs * wb.x, b.y * rs * wb.y);
+          v.w = pack_bf16x2(b.z * rs * wb.z, b.w * rs * wb.w);
+        }
+      } else if (r < ntok) {
+        const int col = (kt0 + pc) * 32 + c * 8;
+        if (NORM_IN) {
+          const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
+          const float4* hp = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K + col);
+          const float4* wn = reinterpret_cast<const float4*>(p.norm_w + col);
+          const float4 a = hp[0], b = hp[1], wa = wn[0], wb = wn[1];
+          const float rs = s_rstd[r];
+          v.x = pack_bf16x2(a.x * rs * wa.x, a.y * rs * wa.y);
+          v.y = pack_bf16x2(a.z * rs * wa.z, a.w * rs * wa.w);
+          v.z = pack_bf16x2(b.x * rs * wb.x, b.y * rs * wb.y);
+          v.w = pack_bf16x2(b.z * rs * wb.z, b.w * rs * wb.w);
+        } else {
+          v = *reinterpret_cast<const uint4*>(p.X + (size_t)(n0 + r) * p.ldx + col);
+        }
+      }
       *reinterpret_cast<uint4*>(xs + r * xstride + c * 8) = v;
     }
     __syncthreads();
 
+    int first = kg;
+    if (pc == 0) {  // the fragments loaded before waiting
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        const int kt = kg + u * KG;
+        if (kt < pn) mma_tile<NT>(acc, pre[u][0], pre[u][1], xs, xstride, kt, lane);
+      }
+      first = kg + kPre * KG;
+    }
     constexpr int U = 4;
-    for (int base = kg; base < pn; base += KG * U) {
+    for (int base = first; base < pn; base += KG * U) {
       uint4 a[U][2];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -80,162 +248,177 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int kt = base + u * KG;
-        if (kt < pn) {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            uint32_t b[4];
-            const int m = lane >> 3;
-            const bf16* addr = xs + (nt * 8 + (lane & 7)) * xstride + kt * 32 + (m >> 1) * 16 + (m & 1) * 8;
-            ldmatrix_x4(b, addr);
-            mma_bf16(acc[nt], a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w, b[0], b[1]);
-            mma_bf16(acc[nt], a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w, b[2], b[3]);
-          }
-        }
+        if (kt < pn) mma_tile<NT>(acc, a[u][0], a[u][1], xs, xstride, kt, lane);
       }
     }
   }
-  pdl_trigger();
 
-  // ---- reduce the KG warps of each row tile, in warp order
+  // ---- this CTA's tile: sum the KG warps of each row tile in warp order
   __syncthreads();
   float4* red = reinterpret_cast<float4*>(smem);
-  if (KG > 1) {
+  float* ts = reinterpret_cast<float*>(smem + sm.red_bytes);
+  constexpr int TS = NT * 8 + 1;  // token stride (padded)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-    __syncthreads();
-    if (kg == 0) {
-      for (int j = 1; j < KG; ++j) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float4 v = red[((j * RG + rt) * NT + nt) * 32 + lane];
-          acc[nt][0] += v.x;
-          acc[nt][1] += v.y;
-          acc[nt][2] += v.z;
-          acc[nt][3] += v.w;
-        }
-      }
+  for (int nt = 0; nt < NT; ++nt)
+    red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+  __syncthreads();
+  for (int i = threadIdx.x; i < RG * NT * 32; i += 256) {
+    const int ln = i & 31, nt = (i >> 5) % NT, r_t = (i >> 5) / NT;
+    float4 v = red[((0 * RG + r_t) * NT + nt) * 32 + ln];
+    for (int j = 1; j < KG; ++j) {
+      const float4 w = red[((j * RG + r_t) * NT + nt) * 32 + ln];
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
     }
+    const int r0 = r_t * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
+    ts[r0 * TS + c0] = v.x;
+    ts[r0 * TS + c0 + 1] = v.y;
+    ts[(r0 + 8) * TS + c0] = v.z;
+    ts[(r0 + 8) * TS + c0 + 1] = v.w;
+  }
+  __syncthreads();
+  const int rows = 16 * RG;
+  const int row0 = rgi * rows;
+
+  // ---- split-K across the cluster: CTA `split` finishes tokens split, split + S, ... (sum in split order)
+  cg::cluster_group cluster = cg::this_cluster();
+  if (S > 1) {
+    const float* peer[kMaxClusterDev];
+#pragma unroll
+    for (int sp = 0; sp < kMaxClusterDev; ++sp) peer[sp] = cluster.map_shared_rank(ts, sp < S ? sp : 0);
+    cluster.sync();
+    for (int i = threadIdx.x; i < rows * nown; i += 256) {
+      const int k = i / rows, r = i - k * rows;
+      const int idx = r * TS + tok_first + k * tok_step;
+      float v[kMaxClusterDev];
+#pragma unroll
+      for (int sp = 0; sp < kMaxClusterDev; ++sp) v[sp] = sp < S ? peer[sp][idx] : 0.f;
+      float sum = v[0];
+#pragma unroll
+      for (int sp = 1; sp < kMaxClusterDev; ++sp)
+        if (sp < S) sum += v[sp];
+      ts[idx] = sum;
+    }
+    __syncthreads();
   }
 
-  // ---- split-K: the last CTA of the row group adds the S partials in split order
-  __shared__ int s_flag;
-  bool finalize = true;
-  if (p.S > 1) {
-    const size_t group = (size_t)chunk * nRG + rgi;
-    if (kg == 0) {
-      float4* dst = reinterpret_cast<float4*>(p.ws) + ((group * p.S + split) * RG + rt) * NT * 32 + lane;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) __stcg(dst + nt * 32, make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]));
+  if (EPI == EPI_STORE_F32) {
+    for (int i = threadIdx.x; i < rows * nown; i += 256) {
+      const int k = i / rows, r = i - k * rows;
+      const int tok = tok_first + k * tok_step;
+      p.out_f32[(size_t)(n0 + tok) * p.ldo + row0 + r] = ts[r * TS + tok] + (p.bias ? p.bias[row0 + r] : 0.f);
     }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const int old = atomicAdd(p.tickets + group, 1);
-      s_flag = (old == p.S - 1);
-      if (s_flag) p.tickets[group] = 0;
+  } else if (EPI == EPI_RESID) {
+    // h += Y and this CTA's share of each token's sum of squares (lanes over rows, warps over tokens)
+    for (int k = warp; k < nown; k += 8) {
+      const int tok = tok_first + k * tok_step;
+      float* hrow = p.resid + (size_t)(n0 + tok) * p.N + row0;
+      float ss = 0.f;
+      for (int r = lane; r < rows; r += 32) {
+        const float v = hrow[r] + ts[r * TS + tok];
+        hrow[r] = v;
+        ss += v * v;
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) p.sq_out[(size_t)(n0 + tok) * p.sq_stride + rgi] = ss;
     }
-    __syncthreads();
-    finalize = s_flag != 0;
-    if (finalize) {
-      __threadfence();
-      if (kg == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-        for (int sp = 0; sp < p.S; ++sp) {
-          const float4* src = reinterpret_cast<const float4*>(p.ws) + ((group * p.S + sp) * RG + rt) * NT * 32 + lane;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float4 v = __ldcg(src + nt * 32);
-            acc[nt][0] += v.x;
-            acc[nt][1] += v.y;
-            acc[nt][2] += v.z;
-            acc[nt][3] += v.w;
-          }
+  } else if (EPI == EPI_SILU) {
+    const int I = p.N >> 1;
+    const int half = rows >> 1;  // gate rows j: tile row r < 8 of each 16-row tile; up rows: r + 8
+    for (int i = threadIdx.x; i < half * nown; i += 256) {
+      const int k = i / half, jj = i - k * half;
+      const int tok = tok_first + k * tok_step;
+      const int r = (jj >> 3) * 16 + (jj & 7);
+      const float ga = ts[r * TS + tok], up = ts[(r + 8) * TS + tok];
+      p.out_bf16[(size_t)(n0 + tok) * I + (row0 >> 1) + jj] = __float2bfloat16_rn(ga / (1.f + expf(-ga)) * up);
+    }
+  } else if (EPI == EPI_QKV_ROPE) {
+    const int D = p.d;
+    const int E = D / 32;
+    const int nheads_cta = rows / D;
+    for (int item = warp; item < nown * nheads_cta; item += 8) {
+      const int k = item / nheads_cta, hc = item - k * nheads_cta;
+      const int tok = tok_first + k * tok_step;
+      const int head = (row0 / D) + hc;
+      const int tkn = n0 + tok;
+      const int rbase = hc * D;
+      const int slot = s_slot[k];
+      int blk = p.NB, off = 0;
+      if (slot >= 0) {
+        blk = slot >> 4;
+        off = slot & 15;
+      }
+      if (head == 0 && lane == 0) {
+        p.slots[tkn] = slot >= 0 ? slot : -1;
+        if (slot < -1) set_status(p.status, slot == -2 ? ST_BAD_POSITION : ST_BAD_BLOCK);
+      }
+      float x[4];
+      for (int e = 0; e < E; ++e) {
+        const int r = rbase + lane * E + e;
+        x[e] = ts[r * TS + tok] + (p.bias ? p.bias[row0 + r] : 0.f);
+      }
+      const bool is_q = head < p.Hq;
+      const bool is_k = !is_q && head < p.Hq + p.Hkv;
+      if (is_q || is_k) {
+        const float* nw = is_q ? p.q_norm : p.k_norm;
+        if (nw) {
+          float ss = 0.f;
+          for (int e = 0; e < E; ++e) ss += x[e] * x[e];
+          ss = warp_sum(ss);
+          const float rs = rsqrtf(ss / (float)D + p.eps);
+          for (int e = 0; e < E; ++e) x[e] = x[e] * rs * nw[lane * E + e];
+        }
+        // rotate-half RoPE: element i < D/2 pairs with i + D/2, held by lane ^ 16
+        const float* cs = k < kCsTokens ? s_cs[k] : p.cos_sin + (size_t)s_pos[k] * D;  // [D/2][2]
+        float y[4];
+        for (int e = 0; e < E; ++e) {
+          const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+          const int ii = (lane & 15) * E + e;
+          const float c = cs[2 * ii], sn = cs[2 * ii + 1];
+          y[e] = (lane < 16) ? (x[e] * c - other * sn) : (x[e] * c + other * sn);
+        }
+        for (int e = 0; e < E; ++e) x[e] = y[e];
+      }
+      bf16* dst;
+      if (is_q) {
+        dst = p.q_out + ((size_t)tkn * p.Hq + head) * D;
+      } else {
+        const int kvh = is_k ? head - p.Hq : head - p.Hq - p.Hkv;
+        bf16* plane = is_k ? p.k_pool : p.v_pool;
+        dst = plane + (((size_t)blk * p.Hkv + kvh) * 16 + off) * D;
+      }
+      for (int e = 0; e < E; e += 2)
+        *reinterpret_cast<uint32_t*>(dst + lane * E + e) = pack_bf16x2(x[e], x[e + 1]);
+    }
+  } else if (EPI == EPI_LMHEAD) {
+    const bool wl = *p.write_logits != 0;
+    const uint32_t rng[4] = {p.rng[0], p.rng[1], p.rng[2], p.rng[3]};
+    for (int k = warp; k < nown; k += 8) {
+      const int tok = tok_first + k * tok_step;
+      const int tkn = n0 + tok;
+      const float it = p.inv_temp[tkn];
+      unsigned long long best = 0ull;
+      for (int r = lane; r < rows; r += 32) {
+        const int v = row0 + r;
+        const float z = ts[r * TS + tok];
+        if (wl) p.logits[(size_t)tkn * p.N + v] = z;
+        const float key = sample_key(z, it, rng, (uint32_t)tkn, (uint32_t)v);
+        if (key != key) {
+          set_status(p.status, ST_NAN);
+        } else {
+          const unsigned long long pk = pack_key_index(key, (uint32_t)v);
+          best = pk > best ? pk : best;
         }
       }
-    }
-  }
-
-  // ---- epilogue
-  if (finalize && kg == 0) {
-    const int row0 = row_tile * 16 + g;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int tok0 = n0 + nt * 8 + 2 * t;
-      if (EPI == EPI_STORE_F32) {
-        const float b0 = p.bias ? p.bias[row0] : 0.f;
-        const float b8 = p.bias ? p.bias[row0 + 8] : 0.f;
-        if (tok0 < p.T) {
-          p.out_f32[(size_t)tok0 * p.ldo + row0] = acc[nt][0] + b0;
-          p.out_f32[(size_t)tok0 * p.ldo + row0 + 8] = acc[nt][2] + b8;
-        }
-        if (tok0 + 1 < p.T) {
-          p.out_f32[(size_t)(tok0 + 1) * p.ldo + row0] = acc[nt][1] + b0;
-          p.out_f32[(size_t)(tok0 + 1) * p.ldo + row0 + 8] = acc[nt][3] + b8;
-        }
-      } else if (EPI == EPI_RESID) {
-        if (tok0 < p.T) {
-          p.resid[(size_t)tok0 * p.N + row0] += acc[nt][0];
-          p.resid[(size_t)tok0 * p.N + row0 + 8] += acc[nt][2];
-        }
-        if (tok0 + 1 < p.T) {
-          p.resid[(size_t)(tok0 + 1) * p.N + row0] += acc[nt][1];
-          p.resid[(size_t)(tok0 + 1) * p.N + row0 + 8] += acc[nt][3];
-        }
-      } else if (EPI == EPI_SILU) {
-        const int j = row_tile * 8 + g;  // gate row j sits at tile row g, up row j at tile row g + 8
-        const int I = p.N >> 1;
-        if (tok0 < p.T) {
-          const float ga = acc[nt][0], up = acc[nt][2];
-          p.out_bf16[(size_t)tok0 * I + j] = __float2bfloat16_rn(ga / (1.f + expf(-ga)) * up);
-        }
-        if (tok0 + 1 < p.T) {
-          const float ga = acc[nt][1], up = acc[nt][3];
-          p.out_bf16[(size_t)(tok0 + 1) * I + j] = __float2bfloat16_rn(ga / (1.f + expf(-ga)) * up);
-        }
-      } else if (EPI == EPI_LMHEAD) {
-        const bool wl = *p.write_logits != 0;
-        unsigned long long best0 = 0ull, best1 = 0ull;
-        uint32_t rng[4] = {p.rng[0], p.rng[1], p.rng[2], p.rng[3]};
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int tok = tok0 + c;
-          if (tok < p.T) {
-            const float it = p.inv_temp[tok];
-            unsigned long long bb = 0ull;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int v = row0 + 8 * h;
-              const float z = acc[nt][2 * h + c];
-              if (wl) p.logits[(size_t)tok * p.N + v] = z;
-              const float key = sample_key(z, it, rng, (uint32_t)tok, (uint32_t)v);
-              if (key != key) {
-                set_status(p.status, ST_NAN);
-              } else {
-                const unsigned long long pk = pack_key_index(key, (uint32_t)v);
-                bb = pk > bb ? pk : bb;
-              }
-            }
-            if (c == 0) best0 = bb; else best1 = bb;
-          }
-        }
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          const unsigned long long x0 = __shfl_xor_sync(0xffffffffu, best0, o);
-          const unsigned long long x1 = __shfl_xor_sync(0xffffffffu, best1, o);
-          best0 = x0 > best0 ? x0 : best0;
-          best1 = x1 > best1 ? x1 : best1;
-        }
-        if (g == 0) {
-          if (tok0 < p.T && best0) atomicMax(p.best + tok0, best0);
-          if (tok0 + 1 < p.T && best1) atomicMax(p.best + tok0 + 1, best1);
-        }
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
+        best = x > best ? x : best;
       }
+      if (lane == 0 && best) atomicMax(p.best + tkn, best);
     }
-  }
-
-  if (EPI == EPI_LMHEAD) {
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -253,27 +436,35 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
       if (threadIdx.x == 0) *p.done_counter = 0;
     }
   }
+  if (S > 1) cluster.sync();  // keep this CTA's tile alive until every CTA of the cluster has read it
 }
 
 // ------------------------------------------------------------------ host side
 
-void gemm_plan(int N, int K, int* RG, int* S, int* kt_per_split) {
+static constexpr int kMaxCluster = 8;
+
+void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split) {
   const int tiles = N / 16, KT = K / 32;
   const int target = 2 * 152;
-  int s = 1, rg = 1;
-  if (tiles >= target) {
+  int rg = 1;
+  if (rg_fixed > 0) {
+    rg = rg_fixed;
+  } else if (tiles >= target) {
     for (int c = 8; c >= 1; c >>= 1)
       if (tiles % c == 0 && tiles / c >= target) {
         rg = c;
         break;
       }
-  } else {
-    const int want = (target + tiles - 1) / tiles;
-    s = KT;
-    for (int c = want; c <= KT; ++c)
+  }
+  const int groups = tiles / rg;
+  int s = 1;
+  if (groups < target) {
+    // the smallest divisor of KT that gives ~2 CTAs per SM, at most the cluster limit
+    const int want = (target + groups - 1) / groups;
+    for (int c = 1; c <= kMaxCluster && c <= KT; ++c)
       if (KT % c == 0) {
         s = c;
-        break;
+        if (c >= want) break;
       }
   }
   *RG = rg;
@@ -281,64 +472,59 @@ void gemm_plan(int N, int K, int* RG, int* S, int* kt_per_split) {
   *kt_per_split = KT / s;
 }
 
-static int chunks_of(int T) { return (T + 63) / 64; }
-
-size_t gemm_ws_floats(int N, int K, int T) {
-  int rg, s, ktn;
-  gemm_plan(N, K, &rg, &s, &ktn);
-  if (s == 1) return 0;
-  return (size_t)chunks_of(T) * (N / 16) * s * 8 * 128;  // NT <= 8 n-tiles of 128 floats per 16-row tile
-}
-
-int gemm_tickets(int N, int K, int T) {
-  int rg, s, ktn;
-  gemm_plan(N, K, &rg, &s, &ktn);
-  return chunks_of(T) * (N / 16 / rg);
-}
-
-template <int NT, int EPI>
+template <int NT, int EPI, bool NORM_IN>
 static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, dim3 grid) {
-  const int pn = p.kt_per_split < kPieceTiles ? p.kt_per_split : kPieceTiles;
-  const size_t xs = (size_t)NT * 8 * (pn * 32 + 8) * 2;
-  const size_t red = (size_t)8 * NT * 32 * 16;
-  const size_t smem = xs > red ? xs : red;
+  const GemmSmem sm = gemm_smem(NT, p.RG, p.kt_per_split);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(k_gemm<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    cudaFuncSetAttribute(k_gemm<NT, EPI, NORM_IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = sm.total;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = o.pdl ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = p.S;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemm<NT, EPI>, p);
+  cfg.numAttrs = p.S > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k_gemm<NT, EPI, NORM_IN>, p);
 }
 
-template <int EPI>
+static int chunks_of(int T) { return (T + 63) / 64; }
+
+template <int EPI, bool NORM_IN>
 static cudaError_t launch_epi(const GemmParams& p, const LaunchOpts& o, cudaStream_t s) {
   const int nRG = p.N / 16 / p.RG;
-  const int chunks = chunks_of(p.T);
-  const dim3 grid(nRG, p.S, chunks);
+  const dim3 grid(nRG, p.S, chunks_of(p.T));
   const int ntiles = p.T >= 64 ? 8 : (p.T + 7) / 8;
-  if (ntiles <= 1) return launch_nt<1, EPI>(p, o, s, grid);
-  if (ntiles <= 2) return launch_nt<2, EPI>(p, o, s, grid);
-  if (ntiles <= 4) return launch_nt<4, EPI>(p, o, s, grid);
-  return launch_nt<8, EPI>(p, o, s, grid);
+  if (ntiles <= 1) return launch_nt<1, EPI, NORM_IN>(p, o, s, grid);
+  if (ntiles <= 2) return launch_nt<2, EPI, NORM_IN>(p, o, s, grid);
+  if (ntiles <= 4) return launch_nt<4, EPI, NORM_IN>(p, o, s, grid);
+  return launch_nt<8, EPI, NORM_IN>(p, o, s, grid);
 }
 
-cudaError_t launch_gemm(const GemmParams& p, int epi, const LaunchOpts& o, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const LaunchOpts& o, cudaStream_t s) {
   if (p.T <= 0) return cudaSuccess;
-  switch (epi) {
-    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(p, o, s);
-    case EPI_RESID: return launch_epi<EPI_RESID>(p, o, s);
-    case EPI_SILU: return launch_epi<EPI_SILU>(p, o, s);
-    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(p, o, s);
+  if (p.S < 1 || p.S > kMaxCluster) return cudaErrorInvalidValue;
+  if (norm_in) {
+    switch (epi) {
+      case EPI_QKV_ROPE: return launch_epi<EPI_QKV_ROPE, true>(p, o, s);
+      case EPI_SILU: return launch_epi<EPI_SILU, true>(p, o, s);
+      case EPI_LMHEAD: return launch_epi<EPI_LMHEAD, true>(p, o, s);
+      case EPI_STORE_F32: return launch_epi<EPI_STORE_F32, true>(p, o, s);
+    }
+  } else {
+    switch (epi) {
+      case EPI_RESID: return launch_epi<EPI_RESID, false>(p, o, s);
+      case EPI_STORE_F32: return launch_epi<EPI_STORE_F32, false>(p, o, s);
+    }
   }
   return cudaErrorInvalidValue;
 }

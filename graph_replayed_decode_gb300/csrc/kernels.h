@@ -23,40 +23,59 @@ struct LaunchOpts {
 cudaError_t launch_pack(const bf16* src, bf16* dst, int N, int K, int interleave_half, cudaStream_t s);
 cudaError_t launch_bf16_to_f32(const bf16* src, float* dst, int64_t n, cudaStream_t s);
 
-// ------------------------------------------------------------------ norms (norm.cu)
-struct NormParams {
-  const float* h_in;     // residual rows [*, H] (ignored in embed mode)
-  float* h_out;          // embed mode: residual rows written here
-  const bf16* embed;     // embed mode: packed embedding [V][H]
-  const int* ids;        // embed mode: token ids [rows]
-  const int* row_index;  // optional gather: row i reads residual row row_index[i]
-  const float* w;        // norm weight [H]
-  bf16* y;               // output [rows][H]
+// ------------------------------------------------------------------ embedding gather (norm.cu)
+struct EmbedParams {
+  const bf16* embed;     // packed embedding [V][H]
+  const int* ids;        // token ids [rows]
+  float* h_out;          // residual rows [rows][H]
+  float* sq_out;         // sum of squares of each row -> sq_out[row * sq_stride]
+  int sq_stride;
   int rows, H, V;
-  float eps;
   int* status;
 };
-cudaError_t launch_rmsnorm(const NormParams& p, bool embed, const LaunchOpts& o, cudaStream_t s);
+cudaError_t launch_embed(const EmbedParams& p, const LaunchOpts& o, cudaStream_t s);
 
 // ------------------------------------------------------------------ skinny GEMM (gemm.cu)
-enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID = 1, EPI_SILU = 2, EPI_LMHEAD = 3 };
+enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID = 1, EPI_SILU = 2, EPI_LMHEAD = 3, EPI_QKV_ROPE = 4 };
 
 struct GemmParams {
   const bf16* W;   // packed [N][K]
-  const bf16* X;   // activations row-major [>= T][ldx] bf16
+  const bf16* X;   // activations row-major [>= T][ldx] bf16 (plain prologue)
   int ldx;
   int T, N, K;
   int RG;           // 16-row tiles per CTA (1, 2, 4, 8)
   int S;            // k splits
-  int kt_per_split; // 32-column k tiles per split
-  float* ws;        // split-K partials
-  int* tickets;     // one per (row group, token chunk), zero between launches
+  int kt_per_split; // 32-column k tiles per split (the S split CTAs of a row group form a cluster)
+  // norm prologue: X = RMSNorm(h_in[x_rows[t] or t]) * norm_w, from sq_parts partial sums of squares
+  const float* h_in;
+  const float* norm_w;
+  const float* sq_in;
+  int sq_parts;
+  int sq_stride;
+  const int* x_rows;
+  float eps;
   // epilogues
   float* out_f32;   // EPI_STORE_F32: out[t][n] (+ bias[n]), row stride ldo
   int ldo;
   const float* bias;
-  float* resid;     // EPI_RESID: resid[t][n] += v, row stride N
+  float* resid;     // EPI_RESID: resid[t][n] += v (row stride N); sq_out[t * sq_stride + row group] = sum h^2
+  float* sq_out;
   bf16* out_bf16;   // EPI_SILU: out[t][j] = silu(gate_j) * up_j, row stride N / 2
+  // EPI_QKV_ROPE: CTA rows are whole heads of the fused [q | k | v] projection
+  const int* positions;
+  const int* tok2req;
+  const int* seq_lens;
+  const int* bt;
+  int mbs;
+  const float* q_norm;
+  const float* k_norm;
+  const float* cos_sin;   // [max_pos][d/2][2]
+  int max_pos;
+  bf16* q_out;            // [T][Hq][d]
+  bf16* k_pool;           // this layer's K plane [NB+1][Hkv][16][d]
+  bf16* v_pool;
+  int* slots;             // [T]
+  int Hq, Hkv, d, NB;
   // EPI_LMHEAD: logits and sampling
   float* logits;                // [T][N] when *write_logits != 0
   const int* write_logits;      // device flag
@@ -68,33 +87,9 @@ struct GemmParams {
   int* status;
 };
 // Picks RG / S / kt_per_split for an [N][K] weight (independent of T, so every token count computes
-// each output with the same summation order).
-void gemm_plan(int N, int K, int* RG, int* S, int* kt_per_split);
-size_t gemm_ws_floats(int N, int K, int T);
-int gemm_tickets(int N, int K, int T);
-cudaError_t launch_gemm(const GemmParams& p, int epi, const LaunchOpts& o, cudaStream_t s);
-
-// ------------------------------------------------------------------ QK-norm + RoPE + KV write (rope_kv.cu)
-struct RopeKvParams {
-  const float* qkv;       // [T][(Hq + 2 Hkv) d] projections (bias applied)
-  const int* positions;   // [T]
-  const int* tok2req;     // [T]
-  const int* seq_lens;    // [R]
-  const int* bt;          // [R][mbs]
-  int mbs;
-  const float* q_norm;    // [d] or null
-  const float* k_norm;    // [d] or null
-  const float* cos_sin;   // [max_pos][d/2][2] (cos, sin)
-  int max_pos;
-  bf16* q_out;            // [T][Hq][d]
-  bf16* k_pool;           // this layer's K plane [NB+1][Hkv][16][d]
-  bf16* v_pool;           // this layer's V plane
-  int* slots;             // [T] slot of each token, -1 for padding rows
-  int T, Hq, Hkv, d, NB;
-  float eps;
-  int* status;
-};
-cudaError_t launch_rope_kv(const RopeKvParams& p, const LaunchOpts& o, cudaStream_t s);
+// each output with the same summation order).  rg_fixed > 0 forces the rows per CTA (whole heads).
+void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split);
+cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const LaunchOpts& o, cudaStream_t s);
 
 // ------------------------------------------------------------------ attention (attn_decode.cu, attn_prefill.cu)
 struct AttnDecodeParams {
