@@ -1146,4 +1146,40 @@ int eng_sample(const float* logits_dev, int32_t rows, int32_t vocab, const float
   return rc;
 }
 
+int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature,
+                       uint64_t seed, uint64_t offset, int32_t* out_ids_dev, void* stream) {
+  if (rows < 0 || vocab < 1 || (rows > 0 && (!logits_dev || !temperature || !out_ids_dev)))
+    return fail(nullptr, ENG_EINVAL, "bad eng_sample_noalloc arguments");
+  const int max_rows = noalloc_max_rows();
+  if (rows > max_rows)
+    return fail(nullptr, ENG_EINVAL, "eng_sample_noalloc takes at most " + std::to_string(max_rows) +
+                                         " rows per call (got " + std::to_string(rows) + ")");
+  if (rows == 0) return ENG_OK;
+  uint32_t* scratch = nullptr;
+  const cudaError_t se = noalloc_scratch(&scratch);
+  if (se != cudaSuccess)
+    return fail(nullptr, ENG_ECUDA, std::string("cudaGetSymbolAddress of the sampler scratch failed: ") +
+                                        cudaGetErrorString(se));
+  // [inverse temperatures][seed_lo, seed_hi, offset_lo, offset_hi]: every word is rewritten by each call
+  uint32_t words[4096 + 4];
+  for (int r = 0; r < rows; ++r) {
+    if (!(temperature[r] >= 0.f) || !std::isfinite(temperature[r]))
+      return fail(nullptr, ENG_EINVAL, "temperature must be finite and >= 0");
+    const float it = inv_temperature(temperature[r]);
+    memcpy(&words[r], &it, 4);
+  }
+  words[rows + 0] = (uint32_t)seed;
+  words[rows + 1] = (uint32_t)(seed >> 32);
+  words[rows + 2] = (uint32_t)offset;
+  words[rows + 3] = (uint32_t)(offset >> 32);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // pageable source: the call returns once the words are staged, so the stack buffer may go away
+  cudaError_t r = cudaMemcpyAsync(scratch, words, (size_t)(rows + 4) * 4, cudaMemcpyHostToDevice, st);
+  if (r == cudaSuccess)
+    r = launch_sample(logits_dev, rows, vocab, reinterpret_cast<const float*>(scratch), scratch + rows, nullptr,
+                      out_ids_dev, nullptr, st);
+  if (r != cudaSuccess) return fail(nullptr, ENG_ECUDA, std::string("eng_sample_noalloc: ") + cudaGetErrorString(r));
+  return ENG_OK;
+}
+
 }  // extern "C"

@@ -149,5 +149,8 @@ cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int
 cudaError_t launch_gumbel(const float* u, float* g, int64_t n, cudaStream_t s);
 cudaError_t launch_sample(const float* logits, int rows, int vocab, const float* inv_temp, const uint32_t* rng,
                           unsigned long long* best, int* out_ids, int* status, cudaStream_t s);
+// Fixed device array for eng_sample_noalloc: [inverse temperatures of up to noalloc_max_rows() rows][4 words].
+int noalloc_max_rows();
+cudaError_t noalloc_scratch(uint32_t** out);
 
 }  // namespace grd

@@ -2,6 +2,8 @@
 // Gumbel transform and the greedy / Gumbel-max argmax over caller-provided logits.  The fused LM-head
 // epilogue (gemm.cu) uses the same device functions, so these launches let tests compare the GPU's
 // noise and log bit for bit with a CPU restatement.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "sampling.cuh"
@@ -77,6 +79,43 @@ cudaError_t launch_sample(const float* logits, int rows, int vocab, const float*
   if (rows <= 0) return cudaSuccess;
   k_sample<<<rows, 256, 0, s>>>(logits, vocab, inv_temp, rng, out_ids, status);
   return cudaGetLastError();
+}
+
+}  // namespace grd
+
+// ------------------------------------------------------------------ sampler without any allocation
+//
+// eng_sample copies each call's inverse temperatures and Philox words into a small device block it
+// allocates.  The variant below keeps that block in a fixed array linked into this library instead, for
+// callers that are not allowed to allocate device memory.  Every GPU that loads the library holds the
+// array (kNoAllocMaxRows + 4 words) until the process exits, and every call on that GPU shares it.
+
+namespace grd {
+
+static constexpr int kNoAllocMaxRows = 4096;
+static constexpr int kMaxDevices = 64;
+static __device__ __align__(256) uint32_t g_sample_scratch[kNoAllocMaxRows + 4];
+
+int noalloc_max_rows() { return kNoAllocMaxRows; }
+
+// Device address of g_sample_scratch for the current device, looked up once per device.  In host code the
+// array's name is only a host-side handle, so the address must come from cudaGetSymbolAddress.
+cudaError_t noalloc_scratch(uint32_t** out) {
+  static std::mutex mu;
+  static uint32_t* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t r = cudaGetDevice(&dev);
+  if (r != cudaSuccess) return r;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    r = cudaGetSymbolAddress(&p, g_sample_scratch);
+    if (r != cudaSuccess) return r;
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace grd

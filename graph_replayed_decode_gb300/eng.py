@@ -99,6 +99,8 @@ SIGNATURES = [
     ("eng_gumbel", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     ("eng_sample", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, _F32P, ctypes.c_uint64,
                                   ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]),
+    ("eng_sample_noalloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, _F32P, ctypes.c_uint64,
+                                          ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]),
 ]
 
 
@@ -296,3 +298,11 @@ def eng_sample(logits_dev: int, rows: int, vocab: int, temperature, seed: int, o
     t = np.ascontiguousarray(temperature, dtype=np.float32)
     _check(None, lib().eng_sample(logits_dev, rows, vocab, t.ctypes.data_as(_F32P), seed, offset, out_ids_dev,
                                   stream))
+
+
+def eng_sample_noalloc(logits_dev: int, rows: int, vocab: int, temperature, seed: int, offset: int,
+                       out_ids_dev: int, stream: int | None = None):
+    """eng_sample with its per-call scratch in a fixed array of the library (no device allocation)."""
+    t = np.ascontiguousarray(temperature, dtype=np.float32)
+    _check(None, lib().eng_sample_noalloc(logits_dev, rows, vocab, t.ctypes.data_as(_F32P), seed, offset,
+                                          out_ids_dev, stream))

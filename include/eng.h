@@ -288,6 +288,24 @@ int eng_gumbel(const float* u_dev, float* g_dev, int64_t n, void* stream);
 int eng_sample(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature, uint64_t seed,
                uint64_t offset, int32_t* out_ids_dev, void* stream);
 
+/*
+ * eng_sample_noalloc -- eng_sample without any device allocation.  The pages have no counterpart: this
+ * entry point exists for callers that may not allocate device memory during a call -- for example a
+ * serving runtime that has handed all free device memory to its own pool or caching allocator, or a
+ * latency-critical loop that cannot take an allocation's implicit synchronisation.
+ * Arguments, results and errors are those of eng_sample, with rows <= 4096 (ENG_EINVAL beyond that,
+ * with a message).  The per-call scratch (the rows' inverse temperatures and the four Philox words) lives
+ * in one fixed 16 KiB array inside this library; every GPU that loads the library holds it until the
+ * process exits.  The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.  All calls on a device share
+ * the array, and each call rewrites every word it reads, so nothing carries over between calls -- but
+ * calls whose work overlaps on the GPU (for example on two unordered streams) race on it.  The call copies
+ * from pageable memory, so it returns after the copy into the array has been staged; synchronise the
+ * stream before reading out_ids_dev.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature,
+                       uint64_t seed, uint64_t offset, int32_t* out_ids_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
