@@ -5,19 +5,35 @@
 // the page's A10), and section "Bottleneck": kernels that split the key/value length across the GPU are
 // the standard fix for this shape of work.  "33. Removing overhead", section "CUDA graphs for a changing
 // batch": a row with length 0 (padding) must produce zeros, never NaN, and a graphed kernel must not
-// take its grid from host-side batch values -- here the grid is (rows, kv_heads, max_splits) with
-// max_splits fixed by the block-table width, and CTAs past a row's real length exit at once.
+// take its grid from host-side batch values -- here the grid is (rows, kv_heads, splits) with the split
+// count fixed by the block-table width, and CTAs past a row's real length do no work.
 //
 // Work of one CTA: request row, KV head, and a range of `split_blocks` 16-key blocks.  The G = Hq / Hkv
 // query heads of the KV head share every K/V load: they are the rows of a 16-row MMA tile.  Each of the
-// 4 warps takes every 4th block of the range (cp.async double buffering into an XOR-swizzled tile),
-// computes S = Q K^T and O += P V with bf16 m16n8k16 MMAs and an online softmax in base 2.  Warps merge
-// through shared memory; splits merge in the last-arriving CTA (atomic ticket, no waiting), always in
-// split order, so the result does not depend on arrival order.
+// 4 warps takes every 4th block of the range (cp.async double buffering into an XOR-swizzled tile; blocks
+// already in the pool are fetched before the kernel waits for the preceding kernel, only the block that
+// holds this step's new token after), computes S = Q K^T and O += P V with bf16 m16n8k16 MMAs and an
+// online softmax in base 2.  Warps merge through shared memory.  The splits of one (row, KV head) form a
+// thread-block cluster: split 0 merges them through distributed shared memory in split order, so the
+// result does not depend on timing and needs no global workspace.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
+namespace cg = cooperative_groups;
+
 namespace grd {
+
+static constexpr int kStages = 2;    // K/V blocks in flight per warp
+static constexpr int kMaxSplits = 8;  // splits of one (row, KV head): one thread-block cluster
+
+// Per-warp K/V stages, reused for the warp merge afterwards ([4][16] M, [4][16] L, [4][16][D] O, [G][D+2]).
+__host__ __device__ constexpr size_t attn_stage_bytes(int D) {
+  return (size_t)4 * kStages * 2 * 16 * D * 2 > (size_t)(128 + 4 * 16 * D + 16 * (D + 2)) * 4
+             ? (size_t)4 * kStages * 2 * 16 * D * 2
+             : (size_t)(128 + 4 * 16 * D + 16 * (D + 2)) * 4;
+}
 
 template <int D>
 __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
@@ -29,7 +45,10 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   const int g = lane >> 2, t = lane & 3;
   const int G = p.Hq / p.Hkv;
   const int h0 = kvh * G;
+  cg::cluster_group cluster = cg::this_cluster();
 
+  if (threadIdx.x == 0 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
+  // lengths and block tables are step inputs, final before the step's first kernel
   const int r = p.r0 + row;
   const int sl = p.seq_lens[r];
   const int tok = p.cu[r];
@@ -40,18 +59,13 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
     nblk = p.mbs;
   }
   const int nsplit = min((nblk + p.split_blocks - 1) / p.split_blocks, p.max_splits);
-  if (sl <= 0) {  // padding row: zeros
-    pdl_wait();
-    if (split == 0)
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
-    return;
-  }
-  if (split >= nsplit) return;
+  const bool active = sl > 0 && split < nsplit;
   const int b_begin = split * p.split_blocks;
   const int b_end = min(nblk, b_begin + p.split_blocks);
 
   extern __shared__ __align__(16) uint8_t smem[];
-  bf16* wbuf = reinterpret_cast<bf16*>(smem) + warp * (4 * TILE);  // 2 stages x (K, V)
+  bf16* wbuf = reinterpret_cast<bf16*>(smem) + warp * (kStages * 2 * TILE);  // kStages x (K, V) per warp
+  float* recv = reinterpret_cast<float*>(smem + attn_stage_bytes(D));        // split 0: [splits][G][D + 2]
 
   float o[D / 8][4];
 #pragma unroll
@@ -66,7 +80,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
     }
     const bf16* ks_ = p.k_pool + ((size_t)blk * p.Hkv + kvh) * TILE;
     const bf16* vs_ = p.v_pool + ((size_t)blk * p.Hkv + kvh) * TILE;
-    bf16* kd = wbuf + stage * 2 * TILE;
+    bf16* kd = wbuf + (stage % kStages) * 2 * TILE;
     bf16* vd = kd + TILE;
 #pragma unroll
     for (int i = lane; i < 16 * NCH; i += 32) {
@@ -78,32 +92,44 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
     cp_async_commit();
   };
 
-  int b = b_begin + warp;
-  int stage = 0;
-  // context blocks already in the pool can be fetched before the preceding kernel finishes; the block that
-  // holds this step's new token (the last one) is written by that kernel
-  const bool early = b < b_end && b != nblk - 1;
-  if (early) issue(b, 0);
+  // this warp's blocks: b_begin + warp + 4 j, j < nb; up to kStages of them in flight.  Blocks already in
+  // the pool are fetched before the kernel waits for the preceding kernel; the block that holds this
+  // step's new token (the sequence's last block) only after.
+  const int nb = active && b_begin + warp < b_end ? (b_end - b_begin - warp + 3) / 4 : 0;
+  const int ahead = min(nb, kStages);
+  int issued = 0;
+  for (; issued < ahead; ++issued) {
+    const int bb = b_begin + warp + 4 * issued;
+    if (bb == nblk - 1) break;
+    issue(bb, issued);
+  }
+  if (p.max_splits > 1) cluster.sync();  // every split has started before any pushes into split 0's memory
+  pdl_trigger();
   pdl_wait();
-  if (b < b_end && !early) issue(b, 0);
-  // Q fragments: rows = the G query heads (rows >= G are zero), k = head dimension
+  for (; issued < ahead; ++issued) issue(b_begin + warp + 4 * issued, issued);
+
   uint32_t qa[KS][4];
-  const bf16* qb = p.q + (size_t)tok * p.Hq * D + (size_t)h0 * D;
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    const int d0 = ks * 16 + 2 * t;
-    qa[ks][0] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0) : 0u;
-    qa[ks][1] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0) : 0u;
-    qa[ks][2] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0 + 8) : 0u;
-    qa[ks][3] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0 + 8) : 0u;
+  for (int ks = 0; ks < KS; ++ks) qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
+  if (active) {  // Q fragments: rows = the G query heads (rows >= G are zero), k = head dimension
+    const bf16* qb = p.q + (size_t)tok * p.Hq * D + (size_t)h0 * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int d0 = ks * 16 + 2 * t;
+      qa[ks][0] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0) : 0u;
+      qa[ks][1] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0) : 0u;
+      qa[ks][2] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0 + 8) : 0u;
+      qa[ks][3] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0 + 8) : 0u;
+    }
   }
 
-  for (; b < b_end; b += 4) {
-    if (b + 4 < b_end) {
-      issue(b + 4, stage ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  for (int j = 0; j < nb; ++j) {
+    const int b = b_begin + warp + 4 * j;
+    const int stage = j % kStages;
+    switch (issued - j - 1) {  // block j has landed once at most this many later groups are pending
+      case 0: cp_async_wait<0>(); break;
+      case 1: cp_async_wait<1>(); break;
+      default: cp_async_wait<2>(); break;
     }
     __syncwarp();
     const bf16* kt = wbuf + stage * 2 * TILE;
@@ -190,14 +216,18 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
       mma_bf16(o[c + 1], pa0, pa1, pa2, pa3, bb[2], bb[3]);
     }
     __syncwarp();
-    stage ^= 1;
+    if (issued < nb) {  // refill the stage just consumed
+      issue(b_begin + warp + 4 * issued, issued % kStages);
+      ++issued;
+    }
   }
 
-  // ---- merge the 4 warps (fixed order)
+  // ---- merge the 4 warps (fixed order) into this CTA's partial [G][D + 2] = (O, M, L)
   __syncthreads();
   float* ms = reinterpret_cast<float*>(smem);  // [4][16]
   float* ls = ms + 64;                          // [4][16]
   float* os = ls + 64;                          // [4][16][D]
+  float* part = os + 4 * 16 * D;                // [G][D + 2]
   if (t == 0) {
     ms[warp * 16 + g] = m0;
     ms[warp * 16 + g + 8] = m1;
@@ -214,100 +244,86 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
     r8[1] = o[c][3];
   }
   __syncthreads();
-
-  const bool single = nsplit == 1;
-  float* part = p.ws + (((size_t)row * p.Hkv + kvh) * p.max_splits + split) * (size_t)G * (D + 2);
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int hr = i / D, dd = i - hr * D;
-    float M = -INFINITY;
+  if (active) {
+    float* dst = nsplit > 1 ? cluster.map_shared_rank(recv, 0) + (size_t)split * G * (D + 2) : nullptr;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+      const int hr = i / D, dd = i - hr * D;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, ms[w * 16 + hr]);
-    float L = 0.f, O = 0.f;
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, ms[w * 16 + hr]);
+      float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float sc_ = exp2f(ms[w * 16 + hr] - M);
-      L += ls[w * 16 + hr] * sc_;
-      O += os[(w * 16 + hr) * D + dd] * sc_;
+      for (int w = 0; w < 4; ++w) {
+        const float sc_ = exp2f(ms[w * 16 + hr] - M);
+        L += ls[w * 16 + hr] * sc_;
+        O += os[(w * 16 + hr) * D + dd] * sc_;
+      }
+      if (nsplit == 1) {
+        out[hr * D + dd] = __float2bfloat16_rn(O / L);
+      } else {  // push this split's (O, M, L) into split 0's receive buffer
+        dst[hr * (D + 2) + dd] = O;
+        if (dd == 0) {
+          dst[hr * (D + 2) + D] = M;
+          dst[hr * (D + 2) + D + 1] = L;
+        }
+      }
     }
-    if (single) {
-      out[hr * D + dd] = __float2bfloat16_rn(O / L);
-    } else {
-      __stcg(part + hr * (D + 2) + dd, O);
-      if (dd == 0) {
-        __stcg(part + hr * (D + 2) + D, M);
-        __stcg(part + hr * (D + 2) + D + 1, L);
+  } else if (sl <= 0 && split == 0) {  // padding row: zeros
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
+  }
+
+  // ---- split 0 merges the pushed partials, in split order, from its own shared memory
+  if (p.max_splits > 1) {
+    cluster.sync();
+    if (split == 0 && sl > 0 && nsplit > 1) {
+      float* wts = ms;           // [nsplit][G] weights (nsplit * G <= 128)
+      float* inv = ms + 8 * 16;  // [G] 1 / L
+      if (threadIdx.x < G) {
+        const int hr = threadIdx.x;
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, recv[((size_t)sp * G + hr) * (D + 2) + D]);
+        float L = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float w = exp2f(recv[((size_t)sp * G + hr) * (D + 2) + D] - M);
+          wts[sp * G + hr] = w;
+          L += recv[((size_t)sp * G + hr) * (D + 2) + D + 1] * w;
+        }
+        inv[hr] = 1.f / L;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+        const int hr = i / D, dd = i - hr * D;
+        float O = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp) O += recv[((size_t)sp * G + hr) * (D + 2) + dd] * wts[sp * G + hr];
+        out[hr * D + dd] = __float2bfloat16_rn(O * inv[hr]);
       }
     }
   }
-  if (single) return;
-
-  // ---- split merge by the last CTA of (row, kv head), in split order
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int* tk = p.tickets + (size_t)row * p.Hkv + kvh;
-    const int old = atomicAdd(tk, 1);
-    s_last = (old == nsplit - 1);
-    if (s_last) *tk = 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const float* base = p.ws + ((size_t)row * p.Hkv + kvh) * p.max_splits * (size_t)G * (D + 2);
-  // split weights exp2(M_s - M) and the total L per head row, all loads in flight at once
-  float* sw = reinterpret_cast<float*>(smem);   // [nsplit][G] weights
-  float* sm = sw + p.max_splits * G;            // [G] merged max, then [G] 1 / L
-  for (int i = threadIdx.x; i < nsplit * G; i += blockDim.x) {
-    const int sp = i / G, hr = i - sp * G;
-    sw[i] = __ldcg(base + ((size_t)sp * G + hr) * (D + 2) + D);
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    const int hr = threadIdx.x;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, sw[sp * G + hr]);
-    float L = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float w = exp2f(sw[sp * G + hr] - M);
-      sw[sp * G + hr] = w;
-      L += __ldcg(base + ((size_t)sp * G + hr) * (D + 2) + D + 1) * w;
-    }
-    sm[hr] = 1.f / L;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int hr = i / D, dd = i - hr * D;
-    float O = 0.f;
-#pragma unroll 8
-    for (int sp = 0; sp < nsplit; ++sp) O += __ldcg(base + ((size_t)sp * G + hr) * (D + 2) + dd) * sw[sp * G + hr];
-    out[hr * D + dd] = __float2bfloat16_rn(O * sm[hr]);
-  }
 }
 
-size_t attn_decode_ws_floats(int rows, int Hq, int Hkv, int d, int max_splits) {
-  const int G = Hq / Hkv;
-  return (size_t)rows * Hkv * max_splits * G * (d + 2);
-}
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, cudaStream_t s) {
   if (p.rows <= 0) return cudaSuccess;
+  if (p.max_splits < 1 || p.max_splits > kMaxSplits) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.rows, p.Hkv, p.max_splits);
   cfg.blockDim = dim3(128);
-  const size_t tiles = (size_t)4 * 4 * 16 * p.d * 2;                  // 4 warps x 2 stages x (K, V)
-  const size_t merge = (size_t)(128 + 4 * 16 * p.d) * 4;
-  cfg.dynamicSmemBytes = tiles > merge ? tiles : merge;
+  const int G = p.Hq / p.Hkv;
+  cfg.dynamicSmemBytes = attn_stage_bytes(p.d) + (size_t)kMaxSplits * G * (p.d + 2) * 4;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = o.pdl ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = p.max_splits;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.max_splits > 1 ? 2 : 1;
   if (p.d == 128) {
     static bool set = false;
     if (!set) {
-      cudaFuncSetAttribute(k_attn_decode<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+      cudaFuncSetAttribute(k_attn_decode<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
       set = true;
     }
     return cudaLaunchKernelEx(&cfg, k_attn_decode<128>, p);
@@ -315,7 +331,7 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, c
   if (p.d == 64) {
     static bool set = false;
     if (!set) {
-      cudaFuncSetAttribute(k_attn_decode<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+      cudaFuncSetAttribute(k_attn_decode<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
       set = true;
     }
     return cudaLaunchKernelEx(&cfg, k_attn_decode<64>, p);

@@ -67,6 +67,61 @@ ENG_DEVICE void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N));
 }
 
+// ------------------------------------------------------------------ L2 prefetch
+ENG_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// This CTA's share of an L2 prefetch of `bytes` (a multiple of 16) at p, split evenly over the grid.
+ENG_DEVICE void prefetch_share(const void* p, unsigned long long bytes) {
+  const unsigned long long ctas = (unsigned long long)gridDim.x * gridDim.y * gridDim.z;
+  const unsigned long long id = blockIdx.x + (unsigned long long)gridDim.x * (blockIdx.y + (unsigned long long)gridDim.y * blockIdx.z);
+  const unsigned long long share = ((bytes + ctas - 1) / ctas + 15) & ~15ull;
+  unsigned long long lo = id * share, hi = lo + share;
+  if (hi > bytes) hi = bytes;
+  for (unsigned long long o = lo; o < hi; o += 65536) {
+    const unsigned long long n = hi - o < 65536 ? hi - o : 65536;
+    prefetch_l2(static_cast<const char*>(p) + o, (uint32_t)n);
+  }
+}
+
+// ------------------------------------------------------------------ TMA bulk copies and mbarriers
+// One mbarrier tracks the bytes of the bulk copies issued against it; waits are bounded.
+ENG_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+ENG_DEVICE void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global to this CTA's shared
+// memory, completing on `bar`.
+ENG_DEVICE void tma_load_1d(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Waits for phase `parity` of the barrier to complete; gives up after `limit` polls and returns false.
+ENG_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // ------------------------------------------------------------------ warp MMA (m16n8k16, bf16 in, f32 accumulate)
 // A: 16x16 row-major fragment (4 regs), B: 16x8 column fragment (2 regs), C/D: 16x8 f32 (4 regs).
 ENG_DEVICE void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,

@@ -102,8 +102,6 @@ struct eng {
   float* logits = nullptr; // [Rm][V]
   int* ids = nullptr;      // [Rm]
   int* slots = nullptr;    // [Tm]
-  float* attn_ws = nullptr;
-  int* attn_tickets = nullptr;
   unsigned long long* best = nullptr;
   int* done_counter = nullptr;
   int* status = nullptr;
@@ -131,6 +129,7 @@ struct eng {
   std::map<int, int> graph_launches;
   bool eager_only = false;
   bool pdl = false;
+  bool l2_prefetch = true;
   int launches = 0;
   eng_step_info_t last{};
 };
@@ -414,12 +413,11 @@ static int setup_buffers(eng_t* e) {
   e->sq_stride = std::max(e->g_o.groups(), e->g_down.groups());
   TRY(dev_alloc(e, &e->sq, (size_t)Tm * e->sq_stride));
 
-  // decode attention splits: 16-key blocks per split chosen from the block-table width so that a row
-  // never needs more than 32 splits; fixed per engine, so eager and replayed steps agree bit for bit
-  e->split_blocks = std::max(4, (c.max_blocks_per_seq + 31) / 32);
+  // decode attention splits: 16-key blocks per split chosen from the block-table width so that a row has
+  // at most 8 splits (one thread-block cluster); fixed per engine, so eager and replayed steps agree bit
+  // for bit
+  e->split_blocks = (c.max_blocks_per_seq + 7) / 8;
   e->max_splits = (c.max_blocks_per_seq + e->split_blocks - 1) / e->split_blocks;
-  TRY(dev_alloc(e, &e->attn_ws, attn_decode_ws_floats(Rm, c.q_heads, c.kv_heads, d, e->max_splits)));
-  TRY(dev_alloc(e, &e->attn_tickets, (size_t)Rm * c.kv_heads));
 
   e->used.assign(c.num_blocks, 0);
   e->free_list.clear();
@@ -451,6 +449,19 @@ static int64_t gemm_bytes(const GemmSite& s, int T, int epi, bool norm_in) {
   if (epi == EPI_SILU) b += (int64_t)T * (s.N / 2) * 2;
   if (epi == EPI_LMHEAD) b += (int64_t)T * 4;
   return b;
+}
+
+// Weights of the GEMM two launches ahead, prefetched into L2 by the current kernel when they take a small
+// share of L2 (large models stream their weights straight from HBM).
+static void set_prefetch(eng_t* e, const void*& ptr, unsigned long long& bytes, const bf16* w, const GemmSite& s) {
+  const unsigned long long b = (unsigned long long)s.N * s.K * 2;
+  if (e->l2_prefetch && b <= 24ull << 20) {
+    ptr = w;
+    bytes = b;
+  } else {
+    ptr = nullptr;
+    bytes = 0;
+  }
 }
 
 // Parameters shared by every GEMM launch of the engine.
@@ -553,6 +564,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     q.Hkv = Hkv;
     q.d = d;
     q.NB = c.num_blocks;
+    set_prefetch(e, q.pf_ptr, q.pf_bytes, L.o, e->g_o);
     if ((r = gemm_launch(e, q, e->g_qkv, EPI_QKV_ROPE, true, ENG_K_GEMM_QKV, st)) != cudaSuccess) return r;
 
     // ---- attention, split by kind inside the step
@@ -592,8 +604,6 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       dp.r0 = P;
       dp.rows = R - P;
       dp.out = e->attn;
-      dp.ws = e->attn_ws;
-      dp.tickets = e->attn_tickets;
       dp.Hq = Hq;
       dp.Hkv = Hkv;
       dp.d = d;
@@ -602,6 +612,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       dp.max_splits = splits;
       dp.scale_log2 = scale_log2;
       dp.status = e->status;
+      set_prefetch(e, dp.pf_ptr, dp.pf_bytes, L.gu, e->g_gu);
       e->launches++;
       prof_begin(e, st, ENG_K_ATTN_DECODE, kv_read + (int64_t)(R - P) * Hq * d * 4);
       r = launch_attn_decode(dp, o, st);
@@ -614,6 +625,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     po.X = e->attn;
     po.resid = e->h;
     po.sq_out = e->sq;
+    set_prefetch(e, po.pf_ptr, po.pf_bytes, L.down, e->g_down);
     if ((r = gemm_launch(e, po, e->g_o, EPI_RESID, false, ENG_K_GEMM_O, st)) != cudaSuccess) return r;
     sq_parts = e->g_o.groups();
 
@@ -624,6 +636,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     pg.sq_in = e->sq;
     pg.sq_parts = sq_parts;
     pg.out_bf16 = e->act;
+    if (l + 1 < c.layers) set_prefetch(e, pg.pf_ptr, pg.pf_bytes, e->layers[l + 1].qkv, e->g_qkv);
     if ((r = gemm_launch(e, pg, e->g_gu, EPI_SILU, true, ENG_K_GEMM_GATE_UP, st)) != cudaSuccess) return r;
 
     // ---- down projection + residual
@@ -721,6 +734,9 @@ int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_w
     // programmatic dependent launch between the step's kernels (ENG_PDL=0 turns it off for comparison)
     const char* v = getenv("ENG_PDL");
     e->pdl = !(v && v[0] == '0');
+    // L2 prefetch of the next GEMM's weights (ENG_L2_PREFETCH=0 turns it off for comparison)
+    const char* w = getenv("ENG_L2_PREFETCH");
+    e->l2_prefetch = !(w && w[0] == '0');
   }
   cudaGetDevice(&e->device);
   int rc = ENG_OK;

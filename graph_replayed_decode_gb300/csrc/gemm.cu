@@ -38,33 +38,52 @@ namespace cg = cooperative_groups;
 namespace grd {
 
 static constexpr int kPieceTiles = 16;          // k-tiles (x32 columns) per X piece when X does not fit whole
-static constexpr int kPre = 4;                  // k-tiles per warp loaded into registers before waiting
+static constexpr int kPreMax = 8;               // k-tiles per warp loaded into registers before waiting
 static constexpr size_t kWholeXBytes = 64 * 1024;
 static constexpr int kMaxClusterDev = 8;        // largest split-K cluster
 static constexpr int kCsTokens = 8;             // tokens whose RoPE row is staged before the wait
+static constexpr size_t kWholeRowsBytes = 32 * 1024;  // residual rows a norm-prologue CTA loads whole
 
-ENG_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// Shared-memory plan of one launch (host and device agree on it).
+// Shared-memory plan of one launch (host and device agree on it).  When the CTA's weight slice is at most
+// kTmaMaxBytes it is bulk-copied (TMA) into shared memory before the kernel waits for its inputs; the X
+// staging area and the reduction tiles follow it.
 struct GemmSmem {
   int piece;       // k-tiles of X staged per piece
+  bool tma;        // weights staged in shared memory
+  size_t w_bytes;  // weight slice (0 unless tma)
   size_t x_bytes;  // X staging
   size_t red_bytes;
   size_t ts_bytes;
+  size_t recv_bytes;
+  size_t nw_bytes;
   size_t total;
 };
 
-__host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn) {
+static constexpr size_t kTmaMaxBytes = 128 * 1024;
+static constexpr size_t kSmemBudget = 200 * 1024;  // dynamic shared memory a GEMM CTA may use
+
+__host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn, int S) {
   GemmSmem m;
   const size_t whole = (size_t)NT * 8 * (ktn * 32 + 8) * 2;
   m.piece = whole <= kWholeXBytes ? ktn : (ktn < kPieceTiles ? ktn : kPieceTiles);
+  const size_t w = (size_t)RG * ktn * 1024;
+  m.tma = w <= kTmaMaxBytes;
+  m.w_bytes = m.tma ? w : 0;
   m.x_bytes = (size_t)NT * 8 * (m.piece * 32 + 8) * 2;
   m.red_bytes = (size_t)8 * NT * 32 * 16;
   m.ts_bytes = (size_t)16 * RG * (NT * 8 + 1) * 4;
-  const size_t tail = m.red_bytes + m.ts_bytes;
-  m.total = m.x_bytes > tail ? m.x_bytes : tail;
+  // split-K: every CTA pushes its tile's columns for the tokens another CTA finishes into that CTA's
+  // receive buffer [S][16 RG rows][tokens per CTA]
+  m.recv_bytes = S > 1 ? (size_t)S * 16 * RG * ((NT * 8 + S - 1) / S) * 4 : 0;
+  m.nw_bytes = (size_t)ktn * 32 * 4;  // the norm weight slice of this CTA's K-range
+  const size_t tail = m.red_bytes + m.ts_bytes + m.recv_bytes;
+  const size_t stage = m.x_bytes + (NT <= 2 ? kWholeRowsBytes : 0);  // + whole residual rows (norm prologue)
+  m.total = m.w_bytes + m.nw_bytes + (stage > tail ? stage : tail);
+  if (m.tma && m.total > kSmemBudget) {  // too big with the weights staged: stream them through registers
+    m.tma = false;
+    m.total -= m.w_bytes;
+    m.w_bytes = 0;
+  }
   return m;
 }
 
@@ -82,13 +101,16 @@ ENG_DEVICE void mma_tile(float (&acc)[NT][4], const uint4& a0, const uint4& a1, 
 }
 
 template <int NT, int EPI, bool NORM_IN>
-__global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
+__global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
+  constexpr int kPre = NT <= 2 ? kPreMax : kPreMax / 2;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float s_rstd[64];
   __shared__ int s_flag;
   __shared__ int s_slot[64];           // EPI_QKV_ROPE: KV slot of each finished token (-1 padding, -2 bad)
   __shared__ int s_pos[64];            //               and its position
   __shared__ float s_cs[kCsTokens][128];  //          and its RoPE row (cos, sin pairs) for the first tokens
+  __shared__ float s_qn[128], s_kn[128];   //          the QK-norm weights
+  __shared__ float s_bias[128];            //          and this CTA's bias rows
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rgi = blockIdx.x, split = blockIdx.y, chunk = blockIdx.z;
   const int S = p.S;
@@ -100,24 +122,41 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
   const int rt = warp % RG, kg = warp / RG;
   const int row_tile = rgi * RG + rt;
   const int ntok = min(NT * 8, p.T - n0);  // valid tokens of this chunk
-  const GemmSmem sm = gemm_smem(NT, RG, ktn);
+  const GemmSmem sm = gemm_smem(NT, RG, ktn, S);
 
   // ---- before waiting: weights do not depend on the preceding kernel
+  __shared__ __align__(8) uint64_t s_wbar;
+  float* nw_s = reinterpret_cast<float*>(smem + sm.w_bytes);  // norm weight slice (NORM_IN)
+  uint8_t* area = smem + sm.w_bytes + sm.nw_bytes;            // X staging, then the reduction tiles
+  cg::cluster_group cluster = cg::this_cluster();
   const uint4* wp = reinterpret_cast<const uint4*>(p.W) + ((size_t)row_tile * KT + kt0) * 64 + lane;
   const int pn0 = min(sm.piece, ktn);
   uint4 pre[kPre][2];
-#pragma unroll
-  for (int u = 0; u < kPre; ++u) {
-    const int kt = kg + u * KG;
-    if (kt < pn0) {
-      pre[u][0] = ld_stream16(wp + (size_t)kt * 64);
-      pre[u][1] = ld_stream16(wp + (size_t)kt * 64 + 32);
-    } else {
-      pre[u][0] = pre[u][1] = make_uint4(0u, 0u, 0u, 0u);
+  if (sm.tma) {
+    // the CTA's whole slice (RG row tiles x ktn k-tiles, contiguous per row tile) into shared memory
+    if (threadIdx.x == 0) {
+      mbar_init(&s_wbar, 1);
+      mbar_expect_tx(&s_wbar, (uint32_t)sm.w_bytes);
+      for (int r = 0; r < RG; ++r)
+        tma_load_1d(smem + (size_t)r * ktn * 1024, p.W + ((size_t)(rgi * RG + r) * KT + kt0) * 512,
+                    (uint32_t)ktn * 1024u, &s_wbar);
     }
+    __syncthreads();  // the barrier is initialised before any thread waits on it
+  } else {
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int kt = kg + u * KG;
+      if (kt < pn0) {
+        pre[u][0] = ld_stream16(wp + (size_t)kt * 64);
+        pre[u][1] = ld_stream16(wp + (size_t)kt * 64 + 32);
+      } else {
+        pre[u][0] = pre[u][1] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (threadIdx.x < RG && ktn > kPre * KG)
+      prefetch_l2(p.W + ((size_t)(rgi * RG + threadIdx.x) * KT + kt0) * 512, (uint32_t)ktn * 1024u);
   }
-  if (threadIdx.x < RG && ktn > kPre * KG)
-    prefetch_l2(p.W + ((size_t)(rgi * RG + threadIdx.x) * KT + kt0) * 512, (uint32_t)ktn * 1024u);
+  if (threadIdx.x == 32 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
 
   // tokens this CTA finishes: split, split + S, ... (all of them when S == 1)
   const int tok_first = S > 1 ? split : 0;
@@ -147,6 +186,11 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
       const int k = i / p.d, j = i - k * p.d;
       s_cs[k][j] = p.cos_sin[(size_t)s_pos[k] * p.d + j];
     }
+    if (threadIdx.x < p.d) {
+      s_qn[threadIdx.x] = p.q_norm ? p.q_norm[threadIdx.x] : 1.f;
+      s_kn[threadIdx.x] = p.k_norm ? p.k_norm[threadIdx.x] : 1.f;
+    }
+    if (threadIdx.x < 16 * RG) s_bias[threadIdx.x] = p.bias ? p.bias[rgi * 16 * RG + threadIdx.x] : 0.f;
   }
   float4 wn_pre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
   const int cpr0 = pn0 * 4;
@@ -156,10 +200,51 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
     wn_pre[0] = wn[0];
     wn_pre[1] = wn[1];
   }
+  if (NORM_IN)
+    for (int i = threadIdx.x; i < ktn * 8; i += 256)
+      reinterpret_cast<float4*>(nw_s)[i] = reinterpret_cast<const float4*>(p.norm_w + kt0 * 32)[i];
+  if (S > 1) cluster.sync();  // every CTA of the cluster has started before any pushes into its memory
   pdl_trigger();
   pdl_wait();
+  // EPI_RESID: the residual values this thread updates in the epilogue (warps over its first two owned
+  // tokens, lanes over up to four rows each), fetched now so the epilogue needs no further round trip
+  float h_old[2][4];
+  if (EPI == EPI_RESID) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      const int k = warp + 8 * a;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int r = lane + 32 * b;
+        h_old[a][b] = (k < nown && r < 16 * RG)
+                          ? p.resid[(size_t)(n0 + tok_first + k * tok_step) * p.N + rgi * 16 * RG + r]
+                          : 0.f;
+      }
+    }
+  }
+  // small token counts: every CTA loads its tokens' whole residual rows once and computes their norms
+  // itself, so the norm costs no round trip beyond the load of X
+  const bool whole_rows = NORM_IN && NT <= 2 && (size_t)ntok * p.K * 4 <= kWholeRowsBytes;
+  float* hrow_s = reinterpret_cast<float*>(area + sm.x_bytes);  // [ntok][K] fp32 when whole_rows
+  if (whole_rows) {
+    for (int i = threadIdx.x; i < ntok * (p.K / 4); i += 256) {
+      const int r = i / (p.K / 4), c4 = i - r * (p.K / 4);
+      const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
+      reinterpret_cast<float4*>(hrow_s)[i] = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K)[c4];
+    }
+    __syncthreads();
+    for (int r = warp; r < NT * 8; r += 8) {
+      float ss = 0.f;
+      if (r < ntok) {
+        for (int c = lane; c < p.K; c += 32) ss += hrow_s[(size_t)r * p.K + c] * hrow_s[(size_t)r * p.K + c];
+        ss = warp_sum(ss);
+      }
+      if (lane == 0) s_rstd[r] = r < ntok ? rsqrtf(ss / (float)p.K + p.eps) : 0.f;
+    }
+    __syncthreads();
+  }
   float4 h_pre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-  if (reg_stage && threadIdx.x < ntok * cpr0) {  // in flight together with the partial sums below
+  if (!whole_rows && reg_stage && threadIdx.x < ntok * cpr0) {  // in flight together with the partial sums below
     const int r = threadIdx.x / cpr0;
     const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
     const float4* hp = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K + kt0 * 32 + (threadIdx.x % cpr0) * 8);
@@ -167,7 +252,7 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
     h_pre[1] = hp[1];
   }
 
-  if (NORM_IN) {  // 1 / rms of each staged token, from its producer's partial sums of squares
+  if (NORM_IN && !whole_rows) {  // 1 / rms of each staged token, from its producer's partial sums of squares
     for (int r = warp; r < NT * 8; r += 8) {
       float ss = 0.f;
       if (r < ntok) {
@@ -185,7 +270,12 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
-  bf16* xs = reinterpret_cast<bf16*>(smem);
+  bf16* xs = reinterpret_cast<bf16*>(area);
+  const uint4* ws = reinterpret_cast<const uint4*>(smem) + (size_t)rt * ktn * 64 + lane;  // tma: this warp's row tile
+  if (sm.tma && !mbar_wait(&s_wbar, 0, 1u << 26)) {
+    set_status(p.status, ST_TIMEOUT);
+    mbar_wait(&s_wbar, 0, 1u << 26);  // never leave while the copy may still write shared memory
+  }
   for (int pc = 0; pc < ktn; pc += sm.piece) {
     const int pn = min(sm.piece, ktn - pc);
     const int xstride = pn * 32 + 8;
@@ -194,7 +284,19 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
     for (int i = threadIdx.x; i < NT * 8 * cpr; i += 256) {
       const int r = i / cpr, c = i - r * cpr;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (reg_stage && pc == 0) {
+      if (whole_rows) {
+        if (r < ntok) {
+          const int col = (kt0 + pc) * 32 + c * 8;
+          const float4* hp = reinterpret_cast<const float4*>(hrow_s + (size_t)r * p.K + col);
+          const float4* wn = reinterpret_cast<const float4*>(nw_s + (pc + c / 4) * 32 + (c & 3) * 8);
+          const float4 a = hp[0], b = hp[1], wa = wn[0], wb = wn[1];
+          const float rs = s_rstd[r];
+          v.x = pack_bf16x2(a.x * rs * wa.x, a.y * rs * wa.y);
+          v.y = pack_bf16x2(a.z * rs * wa.z, a.w * rs * wa.w);
+          v.z = pack_bf16x2(b.x * rs * wb.x, b.y * rs * wb.y);
+          v.w = pack_bf16x2(b.z * rs * wb.z, b.w * rs * wb.w);
+        }
+      } else if (reg_stage && pc == 0) {
         if (r < ntok) {
           const float rs = s_rstd[r];
           const float4 a = h_pre[0], b = h_pre[1], wa = wn_pre[0], wb = wn_pre[1];
@@ -208,7 +310,7 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
         if (NORM_IN) {
           const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
           const float4* hp = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K + col);
-          const float4* wn = reinterpret_cast<const float4*>(p.norm_w + col);
+          const float4* wn = reinterpret_cast<const float4*>(nw_s + (pc + c / 4) * 32 + (c & 3) * 8);
           const float4 a = hp[0], b = hp[1], wa = wn[0], wb = wn[1];
           const float rs = s_rstd[r];
           v.x = pack_bf16x2(a.x * rs * wa.x, a.y * rs * wa.y);
@@ -223,6 +325,26 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
     }
     __syncthreads();
 
+    if (sm.tma) {
+      constexpr int UT = 4;
+      for (int base = kg; base < pn; base += KG * UT) {
+        uint4 a[UT][2];
+#pragma unroll
+        for (int u = 0; u < UT; ++u) {
+          const int kt = base + u * KG;
+          if (kt < pn) {
+            a[u][0] = ws[(size_t)(pc + kt) * 64];
+            a[u][1] = ws[(size_t)(pc + kt) * 64 + 32];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < UT; ++u) {
+          const int kt = base + u * KG;
+          if (kt < pn) mma_tile<NT>(acc, a[u][0], a[u][1], xs, xstride, kt, lane);
+        }
+      }
+      continue;
+    }
     int first = kg;
     if (pc == 0) {  // the fragments loaded before waiting
 #pragma unroll
@@ -255,8 +377,8 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
 
   // ---- this CTA's tile: sum the KG warps of each row tile in warp order
   __syncthreads();
-  float4* red = reinterpret_cast<float4*>(smem);
-  float* ts = reinterpret_cast<float*>(smem + sm.red_bytes);
+  float4* red = reinterpret_cast<float4*>(area);
+  float* ts = reinterpret_cast<float*>(area + sm.red_bytes);
   constexpr int TS = NT * 8 + 1;  // token stride (padded)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -283,27 +405,27 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
   const int row0 = rgi * rows;
 
   // ---- split-K across the cluster: CTA `split` finishes tokens split, split + S, ... (sum in split order)
-  cg::cluster_group cluster = cg::this_cluster();
   if (S > 1) {
-    const float* peer[kMaxClusterDev];
-#pragma unroll
-    for (int sp = 0; sp < kMaxClusterDev; ++sp) peer[sp] = cluster.map_shared_rank(ts, sp < S ? sp : 0);
+    // push this CTA's columns of the tokens CTA q finishes into q's receive buffer, then every CTA adds
+    // its received columns in split order (its own columns at its own position)
+    const int kmax = (NT * 8 + S - 1) / S;
+    float* recv = ts + rows * TS;  // [S][rows][kmax]
+    for (int i = threadIdx.x; i < rows * ntok; i += 256) {
+      const int tok = i / rows, r = i - tok * rows;
+      const int q = tok % S;
+      if (q == split) continue;
+      cluster.map_shared_rank(recv, q)[((size_t)split * rows + r) * kmax + tok / S] = ts[r * TS + tok];
+    }
     cluster.sync();
     for (int i = threadIdx.x; i < rows * nown; i += 256) {
       const int k = i / rows, r = i - k * rows;
-      const int idx = r * TS + tok_first + k * tok_step;
-      float v[kMaxClusterDev];
-#pragma unroll
-      for (int sp = 0; sp < kMaxClusterDev; ++sp) v[sp] = sp < S ? peer[sp][idx] : 0.f;
-      float sum = v[0];
-#pragma unroll
-      for (int sp = 1; sp < kMaxClusterDev; ++sp)
-        if (sp < S) sum += v[sp];
-      ts[idx] = sum;
+      const int tok = tok_first + k * tok_step;
+      float v = 0.f;
+      for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kmax + k];
+      ts[r * TS + tok] = v;
     }
     __syncthreads();
   }
-
   if (EPI == EPI_STORE_F32) {
     for (int i = threadIdx.x; i < rows * nown; i += 256) {
       const int k = i / rows, r = i - k * rows;
@@ -317,7 +439,9 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
       float* hrow = p.resid + (size_t)(n0 + tok) * p.N + row0;
       float ss = 0.f;
       for (int r = lane; r < rows; r += 32) {
-        const float v = hrow[r] + ts[r * TS + tok];
+        const int a = k >> 3, b = r >> 5;
+        const float old = (a < 2 && b < 4) ? h_old[a & 1][b & 3] : hrow[r];
+        const float v = old + ts[r * TS + tok];
         hrow[r] = v;
         ss += v * v;
       }
@@ -357,13 +481,13 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
       float x[4];
       for (int e = 0; e < E; ++e) {
         const int r = rbase + lane * E + e;
-        x[e] = ts[r * TS + tok] + (p.bias ? p.bias[row0 + r] : 0.f);
+        x[e] = ts[r * TS + tok] + s_bias[r];
       }
       const bool is_q = head < p.Hq;
       const bool is_k = !is_q && head < p.Hq + p.Hkv;
       if (is_q || is_k) {
-        const float* nw = is_q ? p.q_norm : p.k_norm;
-        if (nw) {
+        const float* nw = is_q ? s_qn : s_kn;
+        if (is_q ? p.q_norm != nullptr : p.k_norm != nullptr) {
           float ss = 0.f;
           for (int e = 0; e < E; ++e) ss += x[e] * x[e];
           ss = warp_sum(ss);
@@ -436,7 +560,6 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
       if (threadIdx.x == 0) *p.done_counter = 0;
     }
   }
-  if (S > 1) cluster.sync();  // keep this CTA's tile alive until every CTA of the cluster has read it
 }
 
 // ------------------------------------------------------------------ host side
@@ -444,40 +567,58 @@ __global__ void __launch_bounds__(256) k_gemm(GemmParams p) {
 static constexpr int kMaxCluster = 8;
 
 void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split) {
+  // Every round trip after the kernel's wait costs about a microsecond, and so does a cluster reduction,
+  // so the plan first looks for the fewest K splits whose per-CTA weight slice still fits the shared-memory
+  // budget of the bulk copy (the slice is then fetched before the wait), with at most one wave of CTAs at
+  // one CTA per SM (the other half of the SM stays free for the next kernel's early CTAs); among those it
+  // takes the most CTAs.  When no slice fits, it takes the most CTAs in one wave (ties: fewer splits).
   const int tiles = N / 16, KT = K / 32;
-  const int target = 2 * 152;
-  int rg = 1;
-  if (rg_fixed > 0) {
-    rg = rg_fixed;
-  } else if (tiles >= target) {
-    for (int c = 8; c >= 1; c >>= 1)
-      if (tiles % c == 0 && tiles / c >= target) {
-        rg = c;
-        break;
+  const int wave = 152;
+  int best_rg = 0, best_s = 0, best_ctas = 0;
+  for (int sp = 1; sp <= kMaxCluster && sp <= KT && best_ctas == 0; ++sp) {
+    if (KT % sp) continue;
+    for (int rg = 1; rg <= 8; rg <<= 1) {
+      if ((rg_fixed > 0 && rg != rg_fixed) || tiles % rg) continue;
+      const int ctas = tiles / rg * sp;
+      if (ctas > wave || (size_t)rg * (KT / sp) * 1024 > kTmaMaxBytes) continue;
+      if (ctas > best_ctas) {
+        best_ctas = ctas;
+        best_rg = rg;
+        best_s = sp;
       }
+    }
   }
-  const int groups = tiles / rg;
-  int s = 1;
-  if (groups < target) {
-    // the smallest divisor of KT that gives ~2 CTAs per SM, at most the cluster limit
-    const int want = (target + groups - 1) / groups;
-    for (int c = 1; c <= kMaxCluster && c <= KT; ++c)
-      if (KT % c == 0) {
-        s = c;
-        if (c >= want) break;
+  if (best_ctas == 0) {
+    for (int rg = 1; rg <= 8; rg <<= 1) {
+      if ((rg_fixed > 0 && rg != rg_fixed) || tiles % rg) continue;
+      for (int sp = 1; sp <= kMaxCluster && sp <= KT; ++sp) {
+        if (KT % sp) continue;
+        const int ctas = tiles / rg * sp;
+        if (ctas > wave) continue;
+        if (ctas > best_ctas || (ctas == best_ctas && sp < best_s)) {
+          best_ctas = ctas;
+          best_rg = rg;
+          best_s = sp;
+        }
       }
+    }
   }
-  *RG = rg;
-  *S = s;
-  *kt_per_split = KT / s;
+  if (best_ctas == 0) {  // more row tiles than one wave holds: the largest tiles, no split
+    best_rg = rg_fixed > 0 ? rg_fixed : 8;
+    while (best_rg > 1 && tiles % best_rg) best_rg >>= 1;
+    best_s = 1;
+  }
+  *RG = best_rg;
+  *S = best_s;
+  *kt_per_split = KT / best_s;
 }
 
 template <int NT, int EPI, bool NORM_IN>
 static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, dim3 grid) {
-  const GemmSmem sm = gemm_smem(NT, p.RG, p.kt_per_split);
+  const GemmSmem sm = gemm_smem(NT, p.RG, p.kt_per_split, p.S);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(k_gemm<NT, EPI, NORM_IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+    cudaFuncSetAttribute(k_gemm<NT, EPI, NORM_IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};

@@ -46,6 +46,8 @@ struct GemmParams {
   int RG;           // 16-row tiles per CTA (1, 2, 4, 8)
   int S;            // k splits
   int kt_per_split; // 32-column k tiles per split (the S split CTAs of a row group form a cluster)
+  const void* pf_ptr;           // weights of a later kernel to prefetch into L2 (pf_bytes, multiple of 16)
+  unsigned long long pf_bytes;
   // norm prologue: X = RMSNorm(h_in[x_rows[t] or t]) * norm_w, from sq_parts partial sums of squares
   const float* h_in;
   const float* norm_w;
@@ -103,15 +105,14 @@ struct AttnDecodeParams {
   int r0;                 // first request handled (grid.x = rows)
   int rows;
   bf16* out;              // [T][Hq * d]
-  float* ws;              // split partials
-  int* tickets;           // [rows_max][Hkv]
   int Hq, Hkv, d, NB;
   int split_blocks;       // KV blocks per split
-  int max_splits;         // grid.z
+  int max_splits;         // grid.z = cluster size (<= 8): the splits of a (row, KV head) merge on chip
   float scale_log2;       // log2(e) / sqrt(d)
+  const void* pf_ptr;     // weights of a later kernel to prefetch into L2
+  unsigned long long pf_bytes;
   int* status;
 };
-size_t attn_decode_ws_floats(int rows, int Hq, int Hkv, int d, int max_splits);
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, cudaStream_t s);
 
 struct AttnPrefillParams {
