@@ -9,7 +9,9 @@
 // count fixed by the block-table width, and CTAs past a row's real length do no work.
 //
 // Work of one CTA: request row, KV head, and a range of `split_blocks` 16-key blocks.  The G = Hq / Hkv
-// query heads of the KV head share every K/V load: they are the rows of a 16-row MMA tile.  Each of the
+// (<= 8) query heads of the KV head share every K/V load: head g is row g of a 16-row MMA tile and row
+// g + 8 carries the low half of its operand (q as bf16 hi/lo pairs in S = Q K^T, the probabilities as
+// hi/lo pairs in O += P V, common.cuh), so both products keep fp32 operands at no extra MMA.  Each of the
 // 4 warps takes every 4th block of the range (cp.async double buffering into an XOR-swizzled tile; blocks
 // already in the pool are fetched before the kernel waits for the preceding kernel, only the block that
 // holds this step's new token after), computes S = Q K^T and O += P V with bf16 m16n8k16 MMAs and an
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   const int r = p.r0 + row;
   const int sl = p.seq_lens[r];
   const int tok = p.cu[r];
-  bf16* out = p.out + (size_t)tok * p.Hq * D + (size_t)h0 * D;
+  float* out = p.out + (size_t)tok * p.Hq * D + (size_t)h0 * D;
   int nblk = (sl + 15) >> 4;
   if (nblk > p.mbs) {  // never read past a block-table row
     if (split == 0 && threadIdx.x == 0) set_status(p.status, ST_BAD_POSITION);
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   float o[D / 8][4];
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float m0 = -INFINITY, l0 = 0.f;  // running max / sum of head g (rows g and g + 8 are its two halves)
 
   auto issue = [&](int b, int stage) {
     int blk = p.bt[(size_t)r * p.mbs + b];
@@ -111,15 +113,15 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   uint32_t qa[KS][4];
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
-  if (active) {  // Q fragments: rows = the G query heads (rows >= G are zero), k = head dimension
-    const bf16* qb = p.q + (size_t)tok * p.Hq * D + (size_t)h0 * D;
+  if (active && g < G) {  // Q fragments: row g = hi of head g, row g + 8 = its lo (rows of heads >= G: zero)
+    const float* qb = p.q + (size_t)tok * p.Hq * D + (size_t)(h0 + g) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const int d0 = ks * 16 + 2 * t;
-      qa[ks][0] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0) : 0u;
-      qa[ks][1] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0) : 0u;
-      qa[ks][2] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + d0 + 8) : 0u;
-      qa[ks][3] = (g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + d0 + 8) : 0u;
+      const float2 x0 = *reinterpret_cast<const float2*>(qb + d0);
+      const float2 x1 = *reinterpret_cast<const float2*>(qb + d0 + 8);
+      split_bf16x2(x0.x, x0.y, qa[ks][0], qa[ks][1]);
+      split_bf16x2(x1.x, x1.y, qa[ks][2], qa[ks][3]);
     }
   }
 
@@ -161,50 +163,42 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
         mma_bf16(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], bb[2], bb[3]);
       }
     }
+    // head g's score of key nt * 8 + 2 t + j: its hi row (j) plus its lo row (j + 2)
+    float sv[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int key = b * 16 + nt * 8 + 2 * t + (j & 1);
-        sc[nt][j] = (key < sl) ? sc[nt][j] * p.scale_log2 : -INFINITY;
+      for (int j = 0; j < 2; ++j) {
+        const int key = b * 16 + nt * 8 + 2 * t + j;
+        sv[nt][j] = (key < sl) ? (sc[nt][j] + sc[nt][j + 2]) * p.scale_log2 : -INFINITY;
       }
-    float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-    float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
-    float pr[2][4];
+    float mx = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m0, mx);  // finite: the block holds at least one key < sl
+    const float a0 = exp2f(m0 - mn);
+    float pr[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      pr[nt][0] = exp2f(sc[nt][0] - mn0);
-      pr[nt][1] = exp2f(sc[nt][1] - mn0);
-      pr[nt][2] = exp2f(sc[nt][2] - mn1);
-      pr[nt][3] = exp2f(sc[nt][3] - mn1);
+      pr[nt][0] = exp2f(sv[nt][0] - mn);
+      pr[nt][1] = exp2f(sv[nt][1] - mn);
     }
     float s0 = pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
-    float s1 = pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
     s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
     s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
     l0 = l0 * a0 + s0;
-    l1 = l1 * a1 + s1;
-    m0 = mn0;
-    m1 = mn1;
+    m0 = mn;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       o[c][0] *= a0;
       o[c][1] *= a0;
-      o[c][2] *= a1;
-      o[c][3] *= a1;
+      o[c][2] *= a0;
+      o[c][3] *= a0;
     }
-    const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
-    const uint32_t pa1 = pack_bf16x2(pr[0][2], pr[0][3]);
-    const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
-    const uint32_t pa3 = pack_bf16x2(pr[1][2], pr[1][3]);
+    // P fragments: row g = hi of the probabilities, row g + 8 = lo
+    uint32_t pa0, pa1, pa2, pa3;
+    split_bf16x2(pr[0][0], pr[0][1], pa0, pa1);
+    split_bf16x2(pr[1][0], pr[1][1], pa2, pa3);
 #pragma unroll
     for (int c = 0; c < D / 8; c += 2) {
       const int m = lane >> 3;
@@ -230,18 +224,13 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   float* part = os + 4 * 16 * D;                // [G][D + 2]
   if (t == 0) {
     ms[warp * 16 + g] = m0;
-    ms[warp * 16 + g + 8] = m1;
     ls[warp * 16 + g] = l0;
-    ls[warp * 16 + g + 8] = l1;
   }
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c) {
+  for (int c = 0; c < D / 8; ++c) {  // head g's output: hi row + lo row
     float* r0 = os + (warp * 16 + g) * D + c * 8 + 2 * t;
-    float* r8 = os + (warp * 16 + g + 8) * D + c * 8 + 2 * t;
-    r0[0] = o[c][0];
-    r0[1] = o[c][1];
-    r8[0] = o[c][2];
-    r8[1] = o[c][3];
+    r0[0] = o[c][0] + o[c][2];
+    r0[1] = o[c][1] + o[c][3];
   }
   __syncthreads();
   if (active) {
@@ -259,7 +248,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
         O += os[(w * 16 + hr) * D + dd] * sc_;
       }
       if (nsplit == 1) {
-        out[hr * D + dd] = __float2bfloat16_rn(O / L);
+        out[hr * D + dd] = O / L;
       } else {  // push this split's (O, M, L) into split 0's receive buffer
         dst[hr * (D + 2) + dd] = O;
         if (dd == 0) {
@@ -269,7 +258,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
       }
     }
   } else if (sl <= 0 && split == 0) {  // padding row: zeros
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = 0.f;
   }
 
   // ---- split 0 merges the pushed partials, in split order, from its own shared memory
@@ -295,7 +284,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
         const int hr = i / D, dd = i - hr * D;
         float O = 0.f;
         for (int sp = 0; sp < nsplit; ++sp) O += recv[((size_t)sp * G + hr) * (D + 2) + dd] * wts[sp * G + hr];
-        out[hr * D + dd] = __float2bfloat16_rn(O * inv[hr]);
+        out[hr * D + dd] = O * inv[hr];
       }
     }
   }

@@ -8,7 +8,8 @@
 // One CTA per (work item, query head): a work item is up to 64 consecutive query tokens of one request;
 // its 4 warps own 16 query rows each.  Keys stream through shared memory 64 at a time (4 paged blocks,
 // cp.async double buffering, XOR-swizzled 16-byte chunks); S = Q K^T and O += P V use bf16 m16n8k16 MMAs
-// with an online softmax in base 2.  Key rows past the chunk's last position are zero-filled so that
+// with an online softmax in base 2.  Q and P enter the products as bf16 hi/lo pairs (common.cuh): one MMA
+// per half, so both keep fp32 operands.  Key rows past the chunk's last position are zero-filled so that
 // masked (zero) probabilities never meet stale NaN values.
 #include "common.cuh"
 #include "kernels.h"
@@ -39,16 +40,21 @@ __global__ void __launch_bounds__(128) k_attn_prefill(AttnPrefillParams p) {
   const int qp8 = v8 ? p.positions[first + rb + g + 8] : maxpos;
   const int warp_max = (rb < count) ? p.positions[first + min(count - 1, rb + 15)] : -1;
 
-  uint32_t qa[KS][4];
-  const bf16* q0 = p.q + ((size_t)(first + rb + g) * p.Hq + h) * D;
-  const bf16* q8 = p.q + ((size_t)(first + rb + g + 8) * p.Hq + h) * D;
+  uint32_t qa[KS][4], ql[KS][4];  // hi and lo fragments of the warp's 16 query rows
+  const float* q0 = p.q + ((size_t)(first + rb + g) * p.Hq + h) * D;
+  const float* q8 = p.q + ((size_t)(first + rb + g + 8) * p.Hq + h) * D;
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
     const int d0 = ks * 16 + 2 * t;
-    qa[ks][0] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + d0) : 0u;
-    qa[ks][1] = v8 ? *reinterpret_cast<const uint32_t*>(q8 + d0) : 0u;
-    qa[ks][2] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + d0 + 8) : 0u;
-    qa[ks][3] = v8 ? *reinterpret_cast<const uint32_t*>(q8 + d0 + 8) : 0u;
+    const float2 z = make_float2(0.f, 0.f);
+    const float2 a0 = v0 ? *reinterpret_cast<const float2*>(q0 + d0) : z;
+    const float2 a8 = v8 ? *reinterpret_cast<const float2*>(q8 + d0) : z;
+    const float2 b0 = v0 ? *reinterpret_cast<const float2*>(q0 + d0 + 8) : z;
+    const float2 b8 = v8 ? *reinterpret_cast<const float2*>(q8 + d0 + 8) : z;
+    split_bf16x2(a0.x, a0.y, qa[ks][0], ql[ks][0]);
+    split_bf16x2(a8.x, a8.y, qa[ks][1], ql[ks][1]);
+    split_bf16x2(b0.x, b0.y, qa[ks][2], ql[ks][2]);
+    split_bf16x2(b8.x, b8.y, qa[ks][3], ql[ks][3]);
   }
 
   extern __shared__ __align__(16) uint8_t smem[];
@@ -96,10 +102,11 @@ __global__ void __launch_bounds__(128) k_attn_prefill(AttnPrefillParams p) {
     const bf16* kt = buf + stage * 2 * TILE;
     const bf16* vt = kt + TILE;
     if (tile * KT <= warp_max) {
-      float sc[8][4];
+      float sc[8][4], sl[8][4];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ks += 2) {
           const int m = lane >> 3;
@@ -108,9 +115,15 @@ __global__ void __launch_bounds__(128) k_attn_prefill(AttnPrefillParams p) {
           uint32_t bb[4];
           ldmatrix_x4(bb, kt + kr * D + ((ch ^ (kr & 7)) * 8));
           mma_bf16(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], bb[0], bb[1]);
+          mma_bf16(sl[nt], ql[ks][0], ql[ks][1], ql[ks][2], ql[ks][3], bb[0], bb[1]);
           mma_bf16(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], bb[2], bb[3]);
+          mma_bf16(sl[nt], ql[ks + 1][0], ql[ks + 1][1], ql[ks + 1][2], ql[ks + 1][3], bb[2], bb[3]);
         }
       }
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[nt][j] += sl[nt][j];
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
@@ -157,10 +170,11 @@ __global__ void __launch_bounds__(128) k_attn_prefill(AttnPrefillParams p) {
       }
 #pragma unroll
       for (int kk = 0; kk < KT / 16; ++kk) {
-        const uint32_t pa0 = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
-        const uint32_t pa1 = pack_bf16x2(sc[2 * kk][2], sc[2 * kk][3]);
-        const uint32_t pa2 = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-        const uint32_t pa3 = pack_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+        uint32_t pa0, pa1, pa2, pa3, pl0, pl1, pl2, pl3;
+        split_bf16x2(sc[2 * kk][0], sc[2 * kk][1], pa0, pl0);
+        split_bf16x2(sc[2 * kk][2], sc[2 * kk][3], pa1, pl1);
+        split_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], pa2, pl2);
+        split_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], pa3, pl3);
 #pragma unroll
         for (int c = 0; c < D / 8; c += 2) {
           const int m = lane >> 3;
@@ -169,7 +183,9 @@ __global__ void __launch_bounds__(128) k_attn_prefill(AttnPrefillParams p) {
           uint32_t bb[4];
           ldmatrix_x4_trans(bb, vt + vr * D + ((ch ^ (vr & 7)) * 8));
           mma_bf16(o[c], pa0, pa1, pa2, pa3, bb[0], bb[1]);
+          mma_bf16(o[c], pl0, pl1, pl2, pl3, bb[0], bb[1]);
           mma_bf16(o[c + 1], pa0, pa1, pa2, pa3, bb[2], bb[3]);
+          mma_bf16(o[c + 1], pl0, pl1, pl2, pl3, bb[2], bb[3]);
         }
       }
     }
@@ -179,13 +195,13 @@ __global__ void __launch_bounds__(128) k_attn_prefill(AttnPrefillParams p) {
   // rows: g (o[c][0..1]) and g + 8 (o[c][2..3]); l is already summed over the 4 lanes of a row
   const float i0 = (l0 > 0.f) ? 1.f / l0 : 0.f;
   const float i8 = (l1 > 0.f) ? 1.f / l1 : 0.f;
-  bf16* out0 = p.out + ((size_t)(first + rb + g) * p.Hq + h) * D;
-  bf16* out8 = p.out + ((size_t)(first + rb + g + 8) * p.Hq + h) * D;
+  float* out0 = p.out + ((size_t)(first + rb + g) * p.Hq + h) * D;
+  float* out8 = p.out + ((size_t)(first + rb + g + 8) * p.Hq + h) * D;
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
     const int d = c * 8 + 2 * t;
-    if (v0) *reinterpret_cast<uint32_t*>(out0 + d) = pack_bf16x2(o[c][0] * i0, o[c][1] * i0);
-    if (v8) *reinterpret_cast<uint32_t*>(out8 + d) = pack_bf16x2(o[c][2] * i8, o[c][3] * i8);
+    if (v0) *reinterpret_cast<float2*>(out0 + d) = make_float2(o[c][0] * i0, o[c][1] * i0);
+    if (v8) *reinterpret_cast<float2*>(out8 + d) = make_float2(o[c][2] * i8, o[c][3] * i8);
   }
 }
 

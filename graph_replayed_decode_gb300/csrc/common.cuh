@@ -33,6 +33,18 @@ ENG_DEVICE float2 unpack_bf16x2(uint32_t u) {
 
 ENG_DEVICE float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
+// Activation operands of the tensor-core products are carried as bf16 pairs: hi = bf16(v) and
+// lo = bf16(v - hi) (the difference is exact in fp32), so hi + lo keeps about 16 significant bits and a
+// product over the pair (W.hi + W.lo, accumulated in fp32) loses almost nothing to operand rounding.
+// Single-bf16 activations would put every projection's input through a 2^-9 rounding, and over a few
+// dozen layers that alone moves the logits by several hundredths.
+ENG_DEVICE void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = pack_bf16x2(a - hf.x, b - hf.y);
+}
+
 // ------------------------------------------------------------------ reductions (fixed xor trees)
 ENG_DEVICE float warp_sum(float v) {
 #pragma unroll

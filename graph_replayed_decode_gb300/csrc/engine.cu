@@ -92,13 +92,12 @@ struct eng {
 
   // activations and outputs
   float* h = nullptr;      // [Tm][H]
-  bf16* y = nullptr;       // [Tm][H]
   float* sq = nullptr;     // [Tm][sq_stride] per-token partial sums of squares of the residual
   int sq_stride = 1;
-  bf16* q = nullptr;       // [Tm][Hq][d]
-  bf16* attn = nullptr;    // [Tm][Hq d]
-  bf16* act = nullptr;     // [Tm][I]
-  bf16* ylast = nullptr;   // [Rm][H]
+  // activations between kernels stay fp32; the projections read them as bf16 hi/lo pairs
+  float* q = nullptr;      // [Tm][Hq][d]
+  float* attn = nullptr;   // [Tm][Hq d]
+  float* act = nullptr;    // [Tm][I]
   float* logits = nullptr; // [Rm][V]
   int* ids = nullptr;      // [Rm]
   int* slots = nullptr;    // [Tm]
@@ -177,7 +176,7 @@ static std::string check_config(const eng_config_t& c) {
     return "non-positive model dimension";
   if (c.head_dim != 64 && c.head_dim != 128) return "head_dim must be 64 or 128";
   if (c.q_heads % c.kv_heads != 0) return "q_heads must be a multiple of kv_heads";
-  if (c.q_heads / c.kv_heads > 16) return "at most 16 query heads per KV head";
+  if (c.q_heads / c.kv_heads > 8) return "at most 8 query heads per KV head";
   if (c.hidden % 32 || c.intermediate % 32 || (c.q_heads * c.head_dim) % 32) return "reduction widths must be multiples of 32";
   if (c.vocab % 16) return "vocab must be a multiple of 16";
   if (c.dtype != ENG_DTYPE_BF16) return "only ENG_DTYPE_BF16 weights are supported";
@@ -385,11 +384,9 @@ static int setup_buffers(eng_t* e) {
   }
 
   TRY(dev_alloc(e, &e->h, (size_t)Tm * H));
-  TRY(dev_alloc(e, &e->y, (size_t)Tm * H));
   TRY(dev_alloc(e, &e->q, (size_t)Tm * c.q_heads * d));
   TRY(dev_alloc(e, &e->attn, (size_t)Tm * c.q_heads * d));
   TRY(dev_alloc(e, &e->act, (size_t)Tm * c.intermediate));
-  TRY(dev_alloc(e, &e->ylast, (size_t)Rm * H));
   TRY(dev_alloc(e, &e->logits, (size_t)Rm * c.vocab));
   TRY(dev_alloc(e, &e->ids, Rm));
   TRY(dev_alloc(e, &e->slots, Tm));
@@ -635,7 +632,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     pg.norm_w = L.post_norm;
     pg.sq_in = e->sq;
     pg.sq_parts = sq_parts;
-    pg.out_bf16 = e->act;
+    pg.out_act = e->act;
     if (l + 1 < c.layers) set_prefetch(e, pg.pf_ptr, pg.pf_bytes, e->layers[l + 1].qkv, e->g_qkv);
     if ((r = gemm_launch(e, pg, e->g_gu, EPI_SILU, true, ENG_K_GEMM_GATE_UP, st)) != cudaSuccess) return r;
 

@@ -12,9 +12,11 @@
 //   * W is pre-packed in m16n8k16 fragment order (common.cuh).  Before waiting for its inputs
 //     (griddepcontrol.wait) every warp loads its first k-tiles' A fragments into registers and the CTA
 //     asks L2 to prefetch the rest of its slice, so weight streaming overlaps the preceding kernel;
-//   * X is staged through shared memory (in one piece when it fits) and read with ldmatrix.  With a norm
-//     prologue X = RMSNorm(h) * w is computed from the fp32 residual h and the per-token partial sums of
-//     squares its producer wrote (EPI_RESID), a warp per token, so no norm kernel runs;
+//   * X is staged through shared memory (in one piece when it fits) and read with ldmatrix, as two bf16
+//     planes hi = bf16(x) and lo = bf16(x - hi) (common.cuh): every weight fragment meets both, into two
+//     fp32 accumulators added at the end, so the product keeps fp32 activations to about 2^-16.  With a
+//     norm prologue X = RMSNorm(h) * w is computed from the fp32 residual h and the per-token partial sums
+//     of squares its producer wrote (EPI_RESID), a warp per token, so no norm kernel runs;
 //   * a CTA owns RG 16-row tiles and one of S K-ranges; its 8 warps split the K-range and sum in a fixed
 //     order; the S CTAs of a row group form a thread-block cluster and add their tiles through distributed
 //     shared memory, always in split order (each CTA finishing every S-th token) -- deterministic and
@@ -39,7 +41,7 @@ namespace grd {
 
 static constexpr int kPieceTiles = 16;          // k-tiles (x32 columns) per X piece when X does not fit whole
 static constexpr int kPreMax = 8;               // k-tiles per warp loaded into registers before waiting
-static constexpr size_t kWholeXBytes = 64 * 1024;
+static constexpr size_t kWholeXBytes = 128 * 1024;  // both planes
 static constexpr int kMaxClusterDev = 8;        // largest split-K cluster
 static constexpr int kCsTokens = 8;             // tokens whose RoPE row is staged before the wait
 static constexpr size_t kWholeRowsBytes = 32 * 1024;  // residual rows a norm-prologue CTA loads whole
@@ -51,10 +53,11 @@ struct GemmSmem {
   int piece;       // k-tiles of X staged per piece
   bool tma;        // weights staged in shared memory
   size_t w_bytes;  // weight slice (0 unless tma)
-  size_t x_bytes;  // X staging
+  size_t x_bytes;  // X staging: hi plane, then lo plane
   size_t red_bytes;
   size_t ts_bytes;
   size_t recv_bytes;
+  size_t recv_off;  // offset of the receive buffer inside the staging area
   size_t nw_bytes;
   size_t total;
 };
@@ -64,21 +67,24 @@ static constexpr size_t kSmemBudget = 200 * 1024;  // dynamic shared memory a GE
 
 __host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn, int S) {
   GemmSmem m;
-  const size_t whole = (size_t)NT * 8 * (ktn * 32 + 8) * 2;
+  const size_t whole = (size_t)2 * NT * 8 * (ktn * 32 + 8) * 2;
   m.piece = whole <= kWholeXBytes ? ktn : (ktn < kPieceTiles ? ktn : kPieceTiles);
   const size_t w = (size_t)RG * ktn * 1024;
   m.tma = w <= kTmaMaxBytes;
   m.w_bytes = m.tma ? w : 0;
-  m.x_bytes = (size_t)NT * 8 * (m.piece * 32 + 8) * 2;
+  m.x_bytes = (size_t)2 * NT * 8 * (m.piece * 32 + 8) * 2;
   m.red_bytes = (size_t)8 * NT * 32 * 16;
   m.ts_bytes = (size_t)16 * RG * (NT * 8 + 1) * 4;
   // split-K: every CTA pushes its tile's columns for the tokens another CTA finishes into that CTA's
   // receive buffer [S][16 RG rows][tokens per CTA]
   m.recv_bytes = S > 1 ? (size_t)S * 16 * RG * ((NT * 8 + S - 1) / S) * 4 : 0;
   m.nw_bytes = (size_t)ktn * 32 * 4;  // the norm weight slice of this CTA's K-range
-  const size_t tail = m.red_bytes + m.ts_bytes + m.recv_bytes;
+  const size_t tail = m.red_bytes + m.ts_bytes;
   const size_t stage = m.x_bytes + (NT <= 2 ? kWholeRowsBytes : 0);  // + whole residual rows (norm prologue)
-  m.total = m.w_bytes + m.nw_bytes + (stage > tail ? stage : tail);
+  // the receive buffer gets its own space: peers push into it while this CTA may still be staging X or
+  // reducing its own tile
+  m.recv_off = stage > tail ? stage : tail;
+  m.total = m.w_bytes + m.nw_bytes + m.recv_off + m.recv_bytes;
   if (m.tma && m.total > kSmemBudget) {  // too big with the weights staged: stream them through registers
     m.tma = false;
     m.total -= m.w_bytes;
@@ -87,22 +93,43 @@ __host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn, int S) {
   return m;
 }
 
+// One 16x32 weight tile against NT 8-token column tiles of X: the hi plane into acc, the lo plane into accl.
 template <int NT>
-ENG_DEVICE void mma_tile(float (&acc)[NT][4], const uint4& a0, const uint4& a1, const bf16* xs, int xstride, int kt,
-                         int lane) {
+ENG_DEVICE void mma_tile(float (&acc)[NT][4], float (&accl)[NT][4], const uint4& a0, const uint4& a1, const bf16* xs,
+                         const bf16* xl, int xstride, int kt, int lane) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    uint32_t b[4];
+    uint32_t b[4], bl[4];
     const int m = lane >> 3;
-    ldmatrix_x4(b, xs + (nt * 8 + (lane & 7)) * xstride + kt * 32 + (m >> 1) * 16 + (m & 1) * 8);
+    const int off = (nt * 8 + (lane & 7)) * xstride + kt * 32 + (m >> 1) * 16 + (m & 1) * 8;
+    ldmatrix_x4(b, xs + off);
+    ldmatrix_x4(bl, xl + off);
     mma_bf16(acc[nt], a0.x, a0.y, a0.z, a0.w, b[0], b[1]);
+    mma_bf16(accl[nt], a0.x, a0.y, a0.z, a0.w, bl[0], bl[1]);
     mma_bf16(acc[nt], a1.x, a1.y, a1.z, a1.w, b[2], b[3]);
+    mma_bf16(accl[nt], a1.x, a1.y, a1.z, a1.w, bl[2], bl[3]);
   }
+}
+
+ENG_DEVICE float4 scale4(const float4 a, float rs, const float4 w) {
+  return make_float4(a.x * rs * w.x, a.y * rs * w.y, a.z * rs * w.z, a.w * rs * w.w);
+}
+
+// Eight consecutive fp32 activations -> the hi and lo planes at element index idx.
+ENG_DEVICE void stage8(bf16* xs, bf16* xl, int idx, const float4 a, const float4 b) {
+  uint4 h, l;
+  split_bf16x2(a.x, a.y, h.x, l.x);
+  split_bf16x2(a.z, a.w, h.y, l.y);
+  split_bf16x2(b.x, b.y, h.z, l.z);
+  split_bf16x2(b.z, b.w, h.w, l.w);
+  *reinterpret_cast<uint4*>(xs + idx) = h;
+  *reinterpret_cast<uint4*>(xl + idx) = l;
 }
 
 template <int NT, int EPI, bool NORM_IN>
 __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
-  constexpr int kPre = NT <= 2 ? kPreMax : kPreMax / 2;
+  constexpr int kPre = NT <= 2 ? kPreMax : (NT == 4 ? kPreMax / 2 : kPreMax / 4);
+  constexpr int kUnroll = NT >= 8 ? 2 : 4;  // weight k-tiles loaded per group (register budget)
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float s_rstd[64];
   __shared__ int s_flag;
@@ -266,11 +293,15 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
     __syncthreads();
   }
 
-  float acc[NT][4];
+  float acc[NT][4], accl[NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  for (int nt = 0; nt < NT; ++nt) {
+    acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    accl[nt][0] = accl[nt][1] = accl[nt][2] = accl[nt][3] = 0.f;
+  }
 
   bf16* xs = reinterpret_cast<bf16*>(area);
+  bf16* xl = xs + (size_t)NT * 8 * (sm.piece * 32 + 8);  // lo plane
   const uint4* ws = reinterpret_cast<const uint4*>(smem) + (size_t)rt * ktn * 64 + lane;  // tma: this warp's row tile
   if (sm.tma && !mbar_wait(&s_wbar, 0, 1u << 26)) {
     set_status(p.status, ST_TIMEOUT);
@@ -283,27 +314,19 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
     if (pc > 0) __syncthreads();
     for (int i = threadIdx.x; i < NT * 8 * cpr; i += 256) {
       const int r = i / cpr, c = i - r * cpr;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
       if (whole_rows) {
         if (r < ntok) {
           const int col = (kt0 + pc) * 32 + c * 8;
           const float4* hp = reinterpret_cast<const float4*>(hrow_s + (size_t)r * p.K + col);
           const float4* wn = reinterpret_cast<const float4*>(nw_s + (pc + c / 4) * 32 + (c & 3) * 8);
-          const float4 a = hp[0], b = hp[1], wa = wn[0], wb = wn[1];
-          const float rs = s_rstd[r];
-          v.x = pack_bf16x2(a.x * rs * wa.x, a.y * rs * wa.y);
-          v.y = pack_bf16x2(a.z * rs * wa.z, a.w * rs * wa.w);
-          v.z = pack_bf16x2(b.x * rs * wb.x, b.y * rs * wb.y);
-          v.w = pack_bf16x2(b.z * rs * wb.z, b.w * rs * wb.w);
+          a = scale4(hp[0], s_rstd[r], wn[0]);
+          b = scale4(hp[1], s_rstd[r], wn[1]);
         }
       } else if (reg_stage && pc == 0) {
         if (r < ntok) {
-          const float rs = s_rstd[r];
-          const float4 a = h_pre[0], b = h_pre[1], wa = wn_pre[0], wb = wn_pre[1];
-          v.x = pack_bf16x2(a.x * rs * wa.x, a.y * rs * wa.y);
-          v.y = pack_bf16x2(a.z * rs * wa.z, a.w * rs * wa.w);
-          v.z = pack_bf16x2(b.x * rs * wb.x, b.y * rs * wb.y);
-          v.w = pack_bf16x2(b.z * rs * wb.z, b.w * rs * wb.w);
+          a = scale4(h_pre[0], s_rstd[r], wn_pre[0]);
+          b = scale4(h_pre[1], s_rstd[r], wn_pre[1]);
         }
       } else if (r < ntok) {
         const int col = (kt0 + pc) * 32 + c * 8;
@@ -311,22 +334,20 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
           const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
           const float4* hp = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K + col);
           const float4* wn = reinterpret_cast<const float4*>(nw_s + (pc + c / 4) * 32 + (c & 3) * 8);
-          const float4 a = hp[0], b = hp[1], wa = wn[0], wb = wn[1];
-          const float rs = s_rstd[r];
-          v.x = pack_bf16x2(a.x * rs * wa.x, a.y * rs * wa.y);
-          v.y = pack_bf16x2(a.z * rs * wa.z, a.w * rs * wa.w);
-          v.z = pack_bf16x2(b.x * rs * wb.x, b.y * rs * wb.y);
-          v.w = pack_bf16x2(b.z * rs * wb.z, b.w * rs * wb.w);
+          a = scale4(hp[0], s_rstd[r], wn[0]);
+          b = scale4(hp[1], s_rstd[r], wn[1]);
         } else {
-          v = *reinterpret_cast<const uint4*>(p.X + (size_t)(n0 + r) * p.ldx + col);
+          const float4* xp = reinterpret_cast<const float4*>(p.X + (size_t)(n0 + r) * p.ldx + col);
+          a = xp[0];
+          b = xp[1];
         }
       }
-      *reinterpret_cast<uint4*>(xs + r * xstride + c * 8) = v;
+      stage8(xs, xl, r * xstride + c * 8, a, b);
     }
     __syncthreads();
 
     if (sm.tma) {
-      constexpr int UT = 4;
+      constexpr int UT = kUnroll;
       for (int base = kg; base < pn; base += KG * UT) {
         uint4 a[UT][2];
 #pragma unroll
@@ -340,7 +361,7 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
 #pragma unroll
         for (int u = 0; u < UT; ++u) {
           const int kt = base + u * KG;
-          if (kt < pn) mma_tile<NT>(acc, a[u][0], a[u][1], xs, xstride, kt, lane);
+          if (kt < pn) mma_tile<NT>(acc, accl, a[u][0], a[u][1], xs, xl, xstride, kt, lane);
         }
       }
       continue;
@@ -350,11 +371,11 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
 #pragma unroll
       for (int u = 0; u < kPre; ++u) {
         const int kt = kg + u * KG;
-        if (kt < pn) mma_tile<NT>(acc, pre[u][0], pre[u][1], xs, xstride, kt, lane);
+        if (kt < pn) mma_tile<NT>(acc, accl, pre[u][0], pre[u][1], xs, xl, xstride, kt, lane);
       }
       first = kg + kPre * KG;
     }
-    constexpr int U = 4;
+    constexpr int U = kUnroll;
     for (int base = first; base < pn; base += KG * U) {
       uint4 a[U][2];
 #pragma unroll
@@ -370,10 +391,14 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int kt = base + u * KG;
-        if (kt < pn) mma_tile<NT>(acc, a[u][0], a[u][1], xs, xstride, kt, lane);
+        if (kt < pn) mma_tile<NT>(acc, accl, a[u][0], a[u][1], xs, xl, xstride, kt, lane);
       }
     }
   }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[nt][j] += accl[nt][j];
 
   // ---- this CTA's tile: sum the KG warps of each row tile in warp order
   __syncthreads();
@@ -409,7 +434,7 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
     // push this CTA's columns of the tokens CTA q finishes into q's receive buffer, then every CTA adds
     // its received columns in split order (its own columns at its own position)
     const int kmax = (NT * 8 + S - 1) / S;
-    float* recv = ts + rows * TS;  // [S][rows][kmax]
+    float* recv = reinterpret_cast<float*>(area + sm.recv_off);  // [S][rows][kmax]
     for (int i = threadIdx.x; i < rows * ntok; i += 256) {
       const int tok = i / rows, r = i - tok * rows;
       const int q = tok % S;
@@ -456,7 +481,7 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       const int tok = tok_first + k * tok_step;
       const int r = (jj >> 3) * 16 + (jj & 7);
       const float ga = ts[r * TS + tok], up = ts[(r + 8) * TS + tok];
-      p.out_bf16[(size_t)(n0 + tok) * I + (row0 >> 1) + jj] = __float2bfloat16_rn(ga / (1.f + expf(-ga)) * up);
+      p.out_act[(size_t)(n0 + tok) * I + (row0 >> 1) + jj] = ga / (1.f + expf(-ga)) * up;
     }
   } else if (EPI == EPI_QKV_ROPE) {
     const int D = p.d;
@@ -505,16 +530,16 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
         }
         for (int e = 0; e < E; ++e) x[e] = y[e];
       }
-      bf16* dst;
-      if (is_q) {
-        dst = p.q_out + ((size_t)tkn * p.Hq + head) * D;
-      } else {
+      if (is_q) {  // q stays fp32: the attention splits it into hi/lo operands
+        float* dq = p.q_out + ((size_t)tkn * p.Hq + head) * D + lane * E;
+        for (int e = 0; e < E; ++e) dq[e] = x[e];
+      } else {     // the cache holds bf16
         const int kvh = is_k ? head - p.Hq : head - p.Hq - p.Hkv;
         bf16* plane = is_k ? p.k_pool : p.v_pool;
-        dst = plane + (((size_t)blk * p.Hkv + kvh) * 16 + off) * D;
+        bf16* dst = plane + (((size_t)blk * p.Hkv + kvh) * 16 + off) * D;
+        for (int e = 0; e < E; e += 2)
+          *reinterpret_cast<uint32_t*>(dst + lane * E + e) = pack_bf16x2(x[e], x[e + 1]);
       }
-      for (int e = 0; e < E; e += 2)
-        *reinterpret_cast<uint32_t*>(dst + lane * E + e) = pack_bf16x2(x[e], x[e + 1]);
     }
   } else if (EPI == EPI_LMHEAD) {
     const bool wl = *p.write_logits != 0;

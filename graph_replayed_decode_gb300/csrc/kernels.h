@@ -40,7 +40,7 @@ enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID = 1, EPI_SILU = 2, EPI_LMHEAD = 3, E
 
 struct GemmParams {
   const bf16* W;   // packed [N][K]
-  const bf16* X;   // activations row-major [>= T][ldx] bf16 (plain prologue)
+  const float* X;  // activations row-major [>= T][ldx] fp32 (plain prologue), staged as bf16 hi/lo pairs
   int ldx;
   int T, N, K;
   int RG;           // 16-row tiles per CTA (1, 2, 4, 8)
@@ -62,7 +62,7 @@ struct GemmParams {
   const float* bias;
   float* resid;     // EPI_RESID: resid[t][n] += v (row stride N); sq_out[t * sq_stride + row group] = sum h^2
   float* sq_out;
-  bf16* out_bf16;   // EPI_SILU: out[t][j] = silu(gate_j) * up_j, row stride N / 2
+  float* out_act;   // EPI_SILU: out[t][j] = silu(gate_j) * up_j, row stride N / 2
   // EPI_QKV_ROPE: CTA rows are whole heads of the fused [q | k | v] projection
   const int* positions;
   const int* tok2req;
@@ -73,7 +73,7 @@ struct GemmParams {
   const float* k_norm;
   const float* cos_sin;   // [max_pos][d/2][2]
   int max_pos;
-  bf16* q_out;            // [T][Hq][d]
+  float* q_out;           // [T][Hq][d]
   bf16* k_pool;           // this layer's K plane [NB+1][Hkv][16][d]
   bf16* v_pool;
   int* slots;             // [T]
@@ -95,7 +95,7 @@ cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const Launch
 
 // ------------------------------------------------------------------ attention (attn_decode.cu, attn_prefill.cu)
 struct AttnDecodeParams {
-  const bf16* q;          // [T][Hq][d]
+  const float* q;         // [T][Hq][d]
   const bf16* k_pool;     // layer K plane
   const bf16* v_pool;     // layer V plane
   const int* bt;          // [R][mbs]
@@ -104,7 +104,7 @@ struct AttnDecodeParams {
   const int* cu;          // [R+1]: request r's query token is cu[r]
   int r0;                 // first request handled (grid.x = rows)
   int rows;
-  bf16* out;              // [T][Hq * d]
+  float* out;             // [T][Hq * d]
   int Hq, Hkv, d, NB;
   int split_blocks;       // KV blocks per split
   int max_splits;         // grid.z = cluster size (<= 8): the splits of a (row, KV head) merge on chip
@@ -116,7 +116,7 @@ struct AttnDecodeParams {
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, cudaStream_t s);
 
 struct AttnPrefillParams {
-  const bf16* q;          // [T][Hq][d]
+  const float* q;         // [T][Hq][d]
   const bf16* k_pool;
   const bf16* v_pool;
   const int* bt;
@@ -124,7 +124,7 @@ struct AttnPrefillParams {
   const int* positions;   // [T]
   const int4* items;      // work items: (request, first token, token count <= 64, unused)
   int n_items;
-  bf16* out;              // [T][Hq * d]
+  float* out;             // [T][Hq * d]
   int Hq, Hkv, d, NB;
   float scale_log2;
   int* status;

@@ -60,8 +60,9 @@ typedef struct eng eng_t;
  * Model and engine shape.  Projection widths must be multiples of 16 (rows)
  * and reduction widths multiples of 32: hidden, q_heads*head_dim and
  * intermediate are multiples of 32, vocab a multiple of 16.  head_dim is 64 or
- * 128; q_heads is a multiple of kv_heads with at most 16 query heads per KV
- * head; block_size must be 16.  max_reqs bounds the requests of one step and
+ * 128; q_heads is a multiple of kv_heads with at most 8 query heads per KV
+ * head (a KV head's query heads and the low halves of their operands share one
+ * 16-row tensor-core tile in decode attention); block_size must be 16.  max_reqs bounds the requests of one step and
  * the capture sizes; max_tokens bounds the packed tokens of one step;
  * max_blocks_per_seq bounds a block-table row (positions < max_blocks_per_seq * 16).
  */

@@ -24,6 +24,7 @@ from .model import (
     ContiguousCache,
     PagedCache,
     widen_bf16,
+    round_bf16,
     rms_norm,
     silu,
     rope_inv_freq,
@@ -46,7 +47,7 @@ from .sampler import (
 from .pool import BlockPool, PoolExhausted, blocks_needed
 
 __all__ = [
-    "OracleModel", "ContiguousCache", "PagedCache", "widen_bf16", "rms_norm", "silu", "rope_inv_freq",
+    "OracleModel", "ContiguousCache", "PagedCache", "widen_bf16", "round_bf16", "rms_norm", "silu", "rope_inv_freq",
     "apply_rope", "attend_one", "attend_rows", "attend_packed", "forward_step", "fused_qkv",
     "fused_gate_up", "philox4x32_10", "uniforms", "ln_f32", "gumbel_f32", "sample", "sample_row",
     "BlockPool", "PoolExhausted", "blocks_needed",

@@ -76,6 +76,11 @@ def test_config_validation_rejects_bad_shapes_before_touching_a_device():
             eng.eng_create(cfg, eng.TensorList([]), None)
         assert ei.value.code == eng.ENG_EINVAL
     cfg = eng.make_config(s, 16, 4, 64, 4)
+    cfg.q_heads, cfg.kv_heads = 16, 1        # 16 query heads per KV head: beyond one MMA tile's hi/lo rows
+    with pytest.raises(eng.EngError) as ei:
+        eng.eng_create(cfg, eng.TensorList([]), None)
+    assert ei.value.code == eng.ENG_EINVAL and "8 query heads" in str(ei.value)
+    cfg = eng.make_config(s, 16, 4, 64, 4)
     cfg.block_size = 32
     with pytest.raises(eng.EngError) as ei:
         eng.eng_create(cfg, eng.TensorList([]), None)

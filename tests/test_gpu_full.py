@@ -1,0 +1,188 @@
+"""Parity at the full workload sizes, on outputs the CPU oracle can compute one request at a time.
+
+These are the deep models (28 and 36 layers) where the precision of the activations decides the bar: the
+oracle's own bf16-activation mode lands 0.02-0.08 from its float64 forward here, so the engine carries its
+activation operands as bf16 hi/lo pairs and is held to the float64 oracle.
+
+Decode rows are independent (pinned on the oracle by test_step_requests_are_independent), so for batches
+the oracle recomputes a sample of rows from the same synthetic context K/V the GPU pool holds.  Every case
+runs the captured-graph path the benchmark times; the batch-1 case also checks the device-resident loop
+(eng_decode) against host-driven steps.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle.model import widen_bf16
+
+from harness import GpuEngine, block_table, check_logits_and_ids
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+CAPTURE = [1, 2, 4, 8, 16, 32, 64]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _fill_oracle_context(s, cache: "oracle.ContiguousCache", key_of_row, rows, ctxs):
+    for r in rows:
+        for l in range(s.layers):
+            kv = synth.kv_context(s, l, key_of_row(r), ctxs[r])
+            cache.keys[(l, r)][:, :ctxs[r], :] = widen_bf16(kv[0])
+            cache.values[(l, r)][:, :ctxs[r], :] = widen_bf16(kv[1])
+
+
+def _decode_batch_case(shape_name, ctxs, temps, key_of_row, sample_rows, steps=2, seed=0):
+    """Pure-decode batch over synthetic contexts: GPU graph replay vs oracle on sampled rows."""
+    from graph_replayed_decode_gb300.eng import StepArrays
+    s = synth.shape(shape_name)
+    w = synth.make_weights(s, seed=0)
+    B = len(ctxs)
+    need = [oracle.blocks_needed(c + steps + 1) for c in ctxs]
+    mbs = max(need)
+    g = GpuEngine(s, w, num_blocks=sum(need) + 4, max_reqs=64, max_tokens=64, max_blocks_per_seq=mbs)
+    try:
+        pool = oracle.BlockPool(sum(need) + 4)
+        blocks = []
+        for r in range(B):
+            got = g.alloc(need[r])
+            np.testing.assert_array_equal(got, pool.alloc(need[r]))     # block tables bit-exact
+            blocks.append(list(got))
+        for l in range(s.layers):
+            for r in range(B):
+                g.fill_context(l, blocks[r], synth.kv_context(s, l, key_of_row(r), ctxs[r]))
+        g.capture(CAPTURE)
+        bt = block_table(blocks, mbs)
+        model = oracle.OracleModel(s, w, cache_layers=False)
+        cache = oracle.ContiguousCache(s, {r: ctxs[r] + steps + 1 for r in sample_rows})
+        _fill_oracle_context(s, cache, key_of_row, sample_rows, ctxs)
+        ids = synth.decode_ids(B, s.vocab, 1)
+        pos = np.array(ctxs)
+        temps = np.asarray(temps, dtype=np.float32)
+        for k in range(steps):
+            st = StepArrays(ids, pos, np.arange(B + 1), bt, pos + 1, temps, seed=seed, offset=k)
+            gid, glog = g.step(st)
+            assert g.info().replayed == 1
+            rows = list(sample_rows)
+            olog = oracle.forward_step(model, cache, ids[rows], pos[rows], np.arange(len(rows) + 1), request_keys=rows)
+            check_logits_and_ids(glog, gid, olog, temps, seed, k, rows=rows)
+            ids, pos = gid.copy(), pos + 1
+        assert g.status() == 0
+    finally:
+        g.close()
+
+
+def test_qwen3_0p6b_batch1_prefill_then_graph_decode():
+    """Qwen3-0.6B shape, batch 1: a 512-token prompt prefilled eagerly, then graph-replayed decode,
+    greedy and Gumbel-max (T = 0.8); the device-resident loop reproduces the host-driven ids."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    from graph_replayed_decode_gb300.eng import StepArrays
+    s = synth.shape("qwen3_0p6b")
+    w = synth.make_weights(s, seed=0)
+    steps, P = 4, 512
+    nb = oracle.blocks_needed(P + 2 * steps + 2)
+    g = GpuEngine(s, w, num_blocks=nb + 2, max_reqs=64, max_tokens=512, max_blocks_per_seq=nb)
+    try:
+        blocks = list(g.alloc(nb))
+        bt = block_table([blocks], nb)
+        g.capture(CAPTURE)
+        model = oracle.OracleModel(s, w)
+        for temp in [0.0, 0.8]:
+            cache = oracle.PagedCache(s, nb + 2)
+            cache.set_block_table(0, blocks)
+            prompt = synth.prompt_ids(P, s.vocab, 0)
+            temps = np.array([temp], dtype=np.float32)
+            gid, glog = g.step(StepArrays(prompt, np.arange(P), [0, P], bt, [P], temps, seed=3, offset=0))
+            assert g.info().replayed == 0                                   # prefill runs eagerly
+            olog = oracle.forward_step(model, cache, prompt, np.arange(P), [0, P])
+            check_logits_and_ids(glog, gid, olog, temps, 3, 0)
+            ids, pos, host = gid.copy(), P, [gid[0]]
+            for k in range(1, steps):
+                gid, glog = g.step(StepArrays(ids, [pos], [0, 1], bt, [pos + 1], temps, seed=3, offset=k))
+                assert g.info().replayed == 1
+                olog = oracle.forward_step(model, cache, ids, [pos], [0, 1])
+                check_logits_and_ids(glog, gid, olog, temps, 3, k)
+                ids, pos = gid.copy(), pos + 1
+                host.append(gid[0])
+            # the benchmark's launch configuration: replay + in-place advance, ids fed back on the device.
+            # Decode step k reads host[k-1] at position P + k - 1 and samples host[k]; redo step 2 through
+            # eng_step, then step 3 through eng_decode.
+            again, _ = g.step(StepArrays([host[1]], [P + 1], [0, 1], bt, [P + 2], temps, seed=3, offset=2),
+                              want_logits=False)
+            assert again[0] == host[2]
+            ring = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+            eng.eng_decode(g.h, 1, ring.data_ptr())
+            torch.cuda.synchronize()
+            assert int(ring[0, 0]) == host[3]
+        assert g.status() == 0
+    finally:
+        g.close()
+
+
+def test_qwen3_0p6b_batch32_mixed_contexts():
+    """Qwen3-0.6B shape, batch 32, contexts drawn from {16, 64, 256, 1024, 4096}, T = 1.0, bucket 32."""
+    ctxs = [int(c) for c in synth.context_lengths(32, (16, 64, 256, 1024, 4096), key=0, seed=0)]
+    longest = int(np.argmax(ctxs))
+    _decode_batch_case("qwen3_0p6b", ctxs, [1.0] * 32, lambda r: r, sorted({0, 13, 31, longest}))
+
+
+def test_dense_8b_batch64_context2048():
+    """8B shape, batch 64 at context 2048, T = 0.7, bucket 64 (eight distinct synthetic contexts)."""
+    _decode_batch_case("dense_8b", [2048] * 64, [0.7] * 64, lambda r: r % 8, [0, 45], steps=1)
+
+
+def test_qwen2p5_1p5b_mixed_prefill_chunk_and_decode_rows():
+    """Qwen2.5-1.5B shape: a 512-position chunk of fresh prompts (the last one cut) followed by 32 decode
+    rows at contexts from {64, 256, 1024, 4096}, greedy, in one packed step."""
+    from graph_replayed_decode_gb300.eng import StepArrays
+    s = synth.shape("qwen2p5_1p5b")
+    w = synth.make_weights(s, seed=0)
+    chunk = synth.mixed_chunk_prompts(512, key=0, seed=0)
+    P = len(chunk)
+    dctx = [int(c) for c in synth.context_lengths(32, (64, 256, 1024, 4096), key=1, seed=0)]
+    need = [oracle.blocks_needed(plen + 1) for plen, _ in chunk] + [oracle.blocks_needed(c + 1) for c in dctx]
+    mbs = max(need)
+    g = GpuEngine(s, w, num_blocks=sum(need) + 4, max_reqs=64, max_tokens=600, max_blocks_per_seq=mbs)
+    try:
+        blocks = [list(g.alloc(n)) for n in need]
+        for j, c in enumerate(dctx):
+            for l in range(s.layers):
+                g.fill_context(l, blocks[P + j], synth.kv_context(s, l, 100 + j, c))
+        bt = block_table(blocks, mbs)
+        prompts = [synth.prompt_ids(take, s.vocab, 50 + i) for i, (plen, take) in enumerate(chunk)]
+        dec_ids = synth.decode_ids(32, s.vocab, 2)
+        ids = np.concatenate(prompts + [dec_ids])
+        pos = np.concatenate([np.arange(take) for _, take in chunk] + [np.array(dctx)])
+        cu = np.concatenate([[0], np.cumsum([take for _, take in chunk] + [1] * 32)])
+        seq = np.array([take for _, take in chunk] + [c + 1 for c in dctx])
+        temps = np.zeros(P + 32, dtype=np.float32)
+        gid, glog = g.step(StepArrays(ids, pos, cu, bt, seq, temps))
+        assert g.info().num_prefill == P and g.info().replayed == 0
+        model = oracle.OracleModel(s, w, cache_layers=False)
+        # the prompt chunks (fresh prompts: all their keys are in this step)
+        pc = oracle.PagedCache(s, sum(need) + 4)
+        for r in range(P):
+            pc.set_block_table(r, blocks[r])
+        t_pre = int(cu[P])
+        olog = oracle.forward_step(model, pc, ids[:t_pre], pos[:t_pre], cu[:P + 1])
+        check_logits_and_ids(glog, gid, olog, temps, 0, 0, rows=list(range(P)))
+        # sampled decode rows from the same synthetic contexts
+        rows = [P, P + int(np.argmax(dctx)), P + 31]
+        cc = oracle.ContiguousCache(s, {r: dctx[r - P] + 1 for r in rows})
+        for r in rows:
+            for l in range(s.layers):
+                kv = synth.kv_context(s, l, 100 + (r - P), dctx[r - P])
+                cc.keys[(l, r)][:, :dctx[r - P], :] = widen_bf16(kv[0])
+                cc.values[(l, r)][:, :dctx[r - P], :] = widen_bf16(kv[1])
+        dlog = oracle.forward_step(model, cc, ids[t_pre + np.array(rows) - P], pos[t_pre + np.array(rows) - P],
+                                   np.arange(len(rows) + 1), request_keys=rows)
+        check_logits_and_ids(glog, gid, dlog, temps, 0, 0, rows=rows)
+        assert g.status() == 0
+    finally:
+        g.close()

@@ -269,3 +269,48 @@ def test_planted_mistake_is_caught(monkeypatch):
 
     bad = wrong_rows(s, cache, 0, q, [0] * n, np.arange(n))
     assert not np.allclose(good, bad)
+
+
+# ----------------------------------------------------------------------------- bf16 activations
+
+
+def test_round_bf16_matches_torch_on_float32_values():
+    """Every float32 value has one nearest bf16 value: torch's conversion is the library pin, with
+    exact ties (low 16 bits 0x8000) of both significand parities included."""
+    x32 = (RNG.standard_normal(200000) * np.exp2(RNG.integers(-30, 30, 200000))).astype(np.float32)
+    bits = RNG.integers(0x00800000, 0x7F000000, 4000, dtype=np.uint32)
+    ties = ((bits & np.uint32(0xFFFF0000)) | np.uint32(0x8000)).view(np.float32)
+    x32 = np.concatenate([x32, ties, -ties])
+    want = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(om.round_bf16(x32.astype(np.float64)), want)
+
+
+def test_round_bf16_is_nearest_with_ties_to_even_brute_force():
+    """Float64 inputs (no float32 step in between): the nearest of all bf16 values in [1/4, 4] by
+    exhaustive search, an exact midpoint going to the even bit pattern."""
+    grid_bits = np.arange(0x3E80, 0x4081, dtype=np.uint16)
+    grid = om.widen_bf16(grid_bits)
+    mids = (grid[:-1] + grid[1:]) / 2
+    x = np.concatenate([RNG.uniform(0.2501, 3.999, 3000), mids[::5], grid[::11]])
+    got = om.round_bf16(x)
+    for xi, gi in zip(x, got):
+        d = np.abs(grid - xi)
+        near = np.flatnonzero(d == d.min())
+        pick = near[0] if len(near) == 1 else next(i for i in near if grid_bits[i] % 2 == 0)
+        assert gi == grid[pick], (xi, gi, grid[pick])
+    np.testing.assert_array_equal(om.round_bf16(-x), -got)
+
+
+def test_bf16_activation_step_caches_bf16_values_and_stays_near_f64():
+    s, m = _tiny_model()
+    ids = synth.prompt_ids(21, s.vocab, 3)
+    c64, c16 = oracle.ContiguousCache(s, {0: 40}), oracle.ContiguousCache(s, {0: 40})
+    a = oracle.forward_step(m, c64, ids, np.arange(21), [0, 21])
+    b = oracle.forward_step(m, c16, ids, np.arange(21), [0, 21], activations="bf16")
+    assert 0 < np.abs(a - b).max() < 0.05
+    for l in range(s.layers):
+        for kv in (c16.keys[(l, 0)][:, :21], c16.values[(l, 0)][:, :21]):
+            np.testing.assert_array_equal(om.round_bf16(kv), kv)                # the cache holds bf16 values
+        assert not np.array_equal(om.round_bf16(c64.keys[(l, 0)][:, :21]), c64.keys[(l, 0)][:, :21])
+    with pytest.raises(ValueError):
+        oracle.forward_step(m, c16, ids[:1], [21], [0, 1], activations="fp16")
