@@ -47,6 +47,10 @@ WORKLOADS = {
     "dense_8b_b64": dict(shape="dense_8b", batch=64, contexts=[2048] * 64, temperature=0.7, prefill=False,
                          text="8B-shaped dense decoder, batch 64 pure decode at context 2048 (synthetic KV), "
                               "Gumbel-max T=0.7, bucket 64"),
+    # profiling case: the batch-32 kernels on a 2.5 GB device footprint (small enough for ncu captures)
+    "qwen3_0p6b_b32_ctx256": dict(shape="qwen3_0p6b", batch=32, contexts=[256] * 32, temperature=1.0, prefill=False,
+                                  text="Qwen3-0.6B-shaped decoder, batch 32 pure decode at context 256 "
+                                       "(synthetic KV), Gumbel-max T=1.0, bucket 32"),
 }
 
 

@@ -55,3 +55,24 @@ cudaError_t launch_advance(const AdvanceParams& p, const LaunchOpts& o, cudaStre
 }
 
 }  // namespace grd
+
+namespace grd {
+
+// Holds the stream for `ns` nanoseconds of device time (bounded by the global timer): put in front of an
+// eagerly enqueued step that is timed launch by launch, it lets the host enqueue every launch before the
+// first one runs, so that each event pair brackets device work only, not host launch latency.
+__global__ void k_hold(unsigned long long ns) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  do {
+    __nanosleep(1000);
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  } while (t - t0 < ns);
+}
+
+cudaError_t launch_hold(unsigned long long ns, cudaStream_t s) {
+  k_hold<<<1, 1, 0, s>>>(ns);
+  return cudaGetLastError();
+}
+
+}  // namespace grd

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   const int r = p.r0 + row;
   const int sl = p.seq_lens[r];
   const int tok = p.cu[r];
-  float* out = p.out + (size_t)tok * p.Hq * D + (size_t)h0 * D;
+  const size_t obase = (size_t)tok * p.Hq * D + (size_t)h0 * D;  // this KV head's outputs (operand planes)
   int nblk = (sl + 15) >> 4;
   if (nblk > p.mbs) {  // never read past a block-table row
     if (split == 0 && threadIdx.x == 0) set_status(p.status, ST_BAD_POSITION);
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
         O += os[(w * 16 + hr) * D + dd] * sc_;
       }
       if (nsplit == 1) {
-        out[hr * D + dd] = O / L;
+        put_split(p.out_h, p.out_l, obase + hr * D + dd, O / L);
       } else {  // push this split's (O, M, L) into split 0's receive buffer
         dst[hr * (D + 2) + dd] = O;
         if (dd == 0) {
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
       }
     }
   } else if (sl <= 0 && split == 0) {  // padding row: zeros
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = 0.f;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) put_split(p.out_h, p.out_l, obase + i, 0.f);
   }
 
   // ---- split 0 merges the pushed partials, in split order, from its own shared memory
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
         const int hr = i / D, dd = i - hr * D;
         float O = 0.f;
         for (int sp = 0; sp < nsplit; ++sp) O += recv[((size_t)sp * G + hr) * (D + 2) + dd] * wts[sp * G + hr];
-        out[hr * D + dd] = O * inv[hr];
+        put_split(p.out_h, p.out_l, obase + hr * D + dd, O * inv[hr]);
       }
     }
   }

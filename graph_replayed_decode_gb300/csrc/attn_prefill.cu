@@ -195,13 +195,13 @@ __global__ void __launch_bounds__(128) k_attn_prefill(AttnPrefillParams p) {
   // rows: g (o[c][0..1]) and g + 8 (o[c][2..3]); l is already summed over the 4 lanes of a row
   const float i0 = (l0 > 0.f) ? 1.f / l0 : 0.f;
   const float i8 = (l1 > 0.f) ? 1.f / l1 : 0.f;
-  float* out0 = p.out + ((size_t)(first + rb + g) * p.Hq + h) * D;
-  float* out8 = p.out + ((size_t)(first + rb + g + 8) * p.Hq + h) * D;
+  const size_t out0 = ((size_t)(first + rb + g) * p.Hq + h) * D;  // rows g and g + 8 in the operand planes
+  const size_t out8 = ((size_t)(first + rb + g + 8) * p.Hq + h) * D;
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
     const int d = c * 8 + 2 * t;
-    if (v0) *reinterpret_cast<float2*>(out0 + d) = make_float2(o[c][0] * i0, o[c][1] * i0);
-    if (v8) *reinterpret_cast<float2*>(out8 + d) = make_float2(o[c][2] * i8, o[c][3] * i8);
+    if (v0) put_split2(p.out_h, p.out_l, out0 + d, o[c][0] * i0, o[c][1] * i0);
+    if (v8) put_split2(p.out_h, p.out_l, out8 + d, o[c][2] * i8, o[c][3] * i8);
   }
 }
 

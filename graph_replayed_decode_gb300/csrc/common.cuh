@@ -45,6 +45,21 @@ ENG_DEVICE void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
   lo = pack_bf16x2(a - hf.x, b - hf.y);
 }
 
+// One value into the operand planes at element index i.
+ENG_DEVICE void put_split(bf16* xh, bf16* xl, size_t i, float v) {
+  const bf16 h = __float2bfloat16_rn(v);
+  xh[i] = h;
+  xl[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+// Two adjacent values (i even) into the operand planes.
+ENG_DEVICE void put_split2(bf16* xh, bf16* xl, size_t i, float a, float b) {
+  uint32_t h, l;
+  split_bf16x2(a, b, h, l);
+  *reinterpret_cast<uint32_t*>(xh + i) = h;
+  *reinterpret_cast<uint32_t*>(xl + i) = l;
+}
+
 // ------------------------------------------------------------------ reductions (fixed xor trees)
 ENG_DEVICE float warp_sum(float v) {
 #pragma unroll

@@ -94,10 +94,15 @@ struct eng {
   float* h = nullptr;      // [Tm][H]
   float* sq = nullptr;     // [Tm][sq_stride] per-token partial sums of squares of the residual
   int sq_stride = 1;
-  // activations between kernels stay fp32; the projections read them as bf16 hi/lo pairs
+  // activations: q stays fp32 (the attention splits it); every projection input is written by its
+  // producer as two bf16 planes hi = bf16(x), lo = bf16(x - hi)
   float* q = nullptr;      // [Tm][Hq][d]
-  float* attn = nullptr;   // [Tm][Hq d]
-  float* act = nullptr;    // [Tm][I]
+  bf16* xn_h = nullptr;    // [Tm][H]     h * (next norm weight): QKV, gate|up and LM-head input
+  bf16* xn_l = nullptr;
+  bf16* attn_h = nullptr;  // [Tm][Hq d]  attention output: o_proj input
+  bf16* attn_l = nullptr;
+  bf16* act_h = nullptr;   // [Tm][I]     silu(gate) * up: down-projection input
+  bf16* act_l = nullptr;
   float* logits = nullptr; // [Rm][V]
   int* ids = nullptr;      // [Rm]
   int* slots = nullptr;    // [Tm]
@@ -385,8 +390,12 @@ static int setup_buffers(eng_t* e) {
 
   TRY(dev_alloc(e, &e->h, (size_t)Tm * H));
   TRY(dev_alloc(e, &e->q, (size_t)Tm * c.q_heads * d));
-  TRY(dev_alloc(e, &e->attn, (size_t)Tm * c.q_heads * d));
-  TRY(dev_alloc(e, &e->act, (size_t)Tm * c.intermediate));
+  TRY(dev_alloc(e, &e->xn_h, (size_t)Tm * H));
+  TRY(dev_alloc(e, &e->xn_l, (size_t)Tm * H));
+  TRY(dev_alloc(e, &e->attn_h, (size_t)Tm * c.q_heads * d));
+  TRY(dev_alloc(e, &e->attn_l, (size_t)Tm * c.q_heads * d));
+  TRY(dev_alloc(e, &e->act_h, (size_t)Tm * c.intermediate));
+  TRY(dev_alloc(e, &e->act_l, (size_t)Tm * c.intermediate));
   TRY(dev_alloc(e, &e->logits, (size_t)Rm * c.vocab));
   TRY(dev_alloc(e, &e->ids, Rm));
   TRY(dev_alloc(e, &e->slots, Tm));
@@ -439,11 +448,12 @@ static void prof_end(eng_t* e, cudaStream_t st) {
 }
 
 static int64_t gemm_bytes(const GemmSite& s, int T, int epi, bool norm_in) {
+  (void)norm_in;
   int64_t b = (int64_t)s.N * s.K * 2;                          // weights once
-  b += norm_in ? (int64_t)T * s.K * 4 : (int64_t)T * s.K * 2;   // activations in (fp32 residual or bf16)
+  b += (int64_t)T * s.K * 4;                                    // activation planes in
   if (epi == EPI_STORE_F32) b += (int64_t)T * s.N * 4;
-  if (epi == EPI_RESID) b += (int64_t)T * s.N * 8;              // residual read + write
-  if (epi == EPI_SILU) b += (int64_t)T * (s.N / 2) * 2;
+  if (epi == EPI_RESID) b += (int64_t)T * s.N * 12;             // residual read + write, planes out
+  if (epi == EPI_SILU) b += (int64_t)T * (s.N / 2) * 4;
   if (epi == EPI_LMHEAD) b += (int64_t)T * 4;
   return b;
 }
@@ -521,12 +531,15 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
   ep.h_out = e->h;
   ep.sq_out = e->sq;
   ep.sq_stride = e->sq_stride;
+  ep.norm_w = e->layers[0].in_norm;
+  ep.xh_out = e->xn_h;
+  ep.xl_out = e->xn_l;
   ep.rows = T;
   ep.H = H;
   ep.V = c.vocab;
   ep.status = e->status;
   e->launches++;
-  prof_begin(e, st, ENG_K_EMBED_NORM, (int64_t)T * H * (2 + 4));
+  prof_begin(e, st, ENG_K_EMBED_NORM, (int64_t)T * H * (2 + 4 + 4));
   r = launch_embed(ep, o, st);
   prof_end(e, st);
   if (r != cudaSuccess) return r;
@@ -539,8 +552,8 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
 
     // ---- input RMSNorm + fused QKV projection + QK-norm + RoPE + paged KV write
     GemmParams q = gemm_params(e, e->g_qkv, L.qkv, T);
-    q.h_in = e->h;
-    q.norm_w = L.in_norm;
+    q.Xh = e->xn_h;
+    q.Xl = e->xn_l;
     q.sq_in = e->sq;
     q.sq_parts = sq_parts;
     q.bias = L.qkv_bias;
@@ -576,7 +589,8 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       ap.positions = in + e->in.pos;
       ap.items = reinterpret_cast<const int4*>(in + e->in.items);
       ap.n_items = n_items;
-      ap.out = e->attn;
+      ap.out_h = e->attn_h;
+      ap.out_l = e->attn_l;
       ap.Hq = Hq;
       ap.Hkv = Hkv;
       ap.d = d;
@@ -600,7 +614,8 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       dp.cu = in + e->in.cu;
       dp.r0 = P;
       dp.rows = R - P;
-      dp.out = e->attn;
+      dp.out_h = e->attn_h;
+      dp.out_l = e->attn_l;
       dp.Hq = Hq;
       dp.Hkv = Hkv;
       dp.d = d;
@@ -611,7 +626,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       dp.status = e->status;
       set_prefetch(e, dp.pf_ptr, dp.pf_bytes, L.gu, e->g_gu);
       e->launches++;
-      prof_begin(e, st, ENG_K_ATTN_DECODE, kv_read + (int64_t)(R - P) * Hq * d * 4);
+      prof_begin(e, st, ENG_K_ATTN_DECODE, kv_read + (int64_t)(R - P) * Hq * d * 8);
       r = launch_attn_decode(dp, o, st);
       prof_end(e, st);
       if (r != cudaSuccess) return r;
@@ -619,36 +634,45 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
 
     // ---- output projection + residual (+ sums of squares for the next norm)
     GemmParams po = gemm_params(e, e->g_o, L.o, T);
-    po.X = e->attn;
+    po.Xh = e->attn_h;
+    po.Xl = e->attn_l;
     po.resid = e->h;
     po.sq_out = e->sq;
+    po.next_norm_w = L.post_norm;
+    po.xh_out = e->xn_h;
+    po.xl_out = e->xn_l;
     set_prefetch(e, po.pf_ptr, po.pf_bytes, L.down, e->g_down);
     if ((r = gemm_launch(e, po, e->g_o, EPI_RESID, false, ENG_K_GEMM_O, st)) != cudaSuccess) return r;
     sq_parts = e->g_o.groups();
 
     // ---- post-attention RMSNorm + fused gate|up projection + SiLU * up
     GemmParams pg = gemm_params(e, e->g_gu, L.gu, T);
-    pg.h_in = e->h;
-    pg.norm_w = L.post_norm;
+    pg.Xh = e->xn_h;
+    pg.Xl = e->xn_l;
     pg.sq_in = e->sq;
     pg.sq_parts = sq_parts;
-    pg.out_act = e->act;
+    pg.xh_out = e->act_h;
+    pg.xl_out = e->act_l;
     if (l + 1 < c.layers) set_prefetch(e, pg.pf_ptr, pg.pf_bytes, e->layers[l + 1].qkv, e->g_qkv);
     if ((r = gemm_launch(e, pg, e->g_gu, EPI_SILU, true, ENG_K_GEMM_GATE_UP, st)) != cudaSuccess) return r;
 
     // ---- down projection + residual
     GemmParams pd = gemm_params(e, e->g_down, L.down, T);
-    pd.X = e->act;
+    pd.Xh = e->act_h;
+    pd.Xl = e->act_l;
     pd.resid = e->h;
     pd.sq_out = e->sq;
+    pd.next_norm_w = l + 1 < c.layers ? e->layers[l + 1].in_norm : e->final_norm;
+    pd.xh_out = e->xn_h;
+    pd.xl_out = e->xn_l;
     if ((r = gemm_launch(e, pd, e->g_down, EPI_RESID, false, ENG_K_GEMM_DOWN, st)) != cudaSuccess) return r;
     sq_parts = e->g_down.groups();
   }
 
   // ---- final RMSNorm at each request's last token + LM head + sampling
   GemmParams pl = gemm_params(e, e->g_lm, e->lm, R);
-  pl.h_in = e->h;
-  pl.norm_w = e->final_norm;
+  pl.Xh = e->xn_h;
+  pl.Xl = e->xn_l;
   pl.sq_in = e->sq;
   pl.sq_parts = sq_parts;
   pl.x_rows = in + e->in.last;
@@ -1098,6 +1122,8 @@ int eng_profile(eng_t* e, int32_t capacity, int32_t* kinds, float* ms, int64_t* 
   e->prof_bytes.clear();
   e->prof_on = true;
   e->launches = 0;
+  // hold the stream while the host enqueues the step, so each event pair times device work only
+  CUDA_OR_FAIL(e, launch_hold(20ull * 1000 * 1000, e->stream));
   const cudaError_t r = enqueue_forward(e, rows, rows, 0, 0, e->max_splits, true, e->stream);
   e->prof_on = false;
   CUDA_OR_FAIL(e, r);

@@ -12,19 +12,24 @@
 //   * W is pre-packed in m16n8k16 fragment order (common.cuh).  Before waiting for its inputs
 //     (griddepcontrol.wait) every warp loads its first k-tiles' A fragments into registers and the CTA
 //     asks L2 to prefetch the rest of its slice, so weight streaming overlaps the preceding kernel;
-//   * X is staged through shared memory (in one piece when it fits) and read with ldmatrix, as two bf16
-//     planes hi = bf16(x) and lo = bf16(x - hi) (common.cuh): every weight fragment meets both, into two
-//     fp32 accumulators added at the end, so the product keeps fp32 activations to about 2^-16.  With a
-//     norm prologue X = RMSNorm(h) * w is computed from the fp32 residual h and the per-token partial sums
-//     of squares its producer wrote (EPI_RESID), a warp per token, so no norm kernel runs;
+//   * X arrives as two bf16 planes hi = bf16(x) and lo = bf16(x - hi) (common.cuh), written by the
+//     producing kernel; every weight fragment meets both, into two fp32 accumulators added at the end, so
+//     the product keeps fp32 activations to about 2^-16.  After the wait, warp 0 bulk-copies each token's
+//     rows of the CTA's K-range into shared memory (one copy per row and plane, in one piece when it fits)
+//     and the warps read them with ldmatrix;
+//   * a norm before the GEMM costs no pass: the producer of the residual h writes the planes of h * w
+//     (w the norm weight) and per-row-group partial sums of h^2, and since RMSNorm(h) W^T equals
+//     (1 / rms(h)) ((h * w) W^T), the kernel scales each token's outputs by its 1 / rms, computed from the
+//     partial sums while the copies are in flight;
 //   * a CTA owns RG 16-row tiles and one of S K-ranges; its 8 warps split the K-range and sum in a fixed
 //     order; the S CTAs of a row group form a thread-block cluster and add their tiles through distributed
 //     shared memory, always in split order (each CTA finishing every S-th token) -- deterministic and
 //     independent of T, so graph replay and eager execution are bit-identical;
 //   * epilogues run over the finished [16 RG rows x tokens] tile in shared memory:
 //       EPI_STORE_F32  out = Y (+bias)
-//       EPI_RESID      h += Y, plus each token's sum of h^2 over this CTA's rows (for the next norm)
-//       EPI_SILU       out = silu(gate) * up on row-interleaved gate|up tiles
+//       EPI_RESID      h += Y, each token's sum of h^2 over this CTA's rows and the planes of h * w_next
+//                      (for the next norm and GEMM)
+//       EPI_SILU       planes of silu(gate) * up, on row-interleaved gate|up tiles
 //       EPI_QKV_ROPE   the CTA's rows are whole heads: +bias, per-head QK-RMSNorm, rotate-half RoPE, and the
 //                      paged KV write (q heads -> q buffer, k/v heads -> pool slot of the token)
 //       EPI_LMHEAD     logits (optional) and a per-token (key, index) maximum for greedy / Gumbel-max
@@ -44,7 +49,6 @@ static constexpr int kPreMax = 8;               // k-tiles per warp loaded into 
 static constexpr size_t kWholeXBytes = 128 * 1024;  // both planes
 static constexpr int kMaxClusterDev = 8;        // largest split-K cluster
 static constexpr int kCsTokens = 8;             // tokens whose RoPE row is staged before the wait
-static constexpr size_t kWholeRowsBytes = 32 * 1024;  // residual rows a norm-prologue CTA loads whole
 
 // Shared-memory plan of one launch (host and device agree on it).  When the CTA's weight slice is at most
 // kTmaMaxBytes it is bulk-copied (TMA) into shared memory before the kernel waits for its inputs; the X
@@ -53,12 +57,11 @@ struct GemmSmem {
   int piece;       // k-tiles of X staged per piece
   bool tma;        // weights staged in shared memory
   size_t w_bytes;  // weight slice (0 unless tma)
-  size_t x_bytes;  // X staging: hi plane, then lo plane
+  size_t x_bytes;  // X staging: hi plane, then lo plane, [NT * 8 rows][piece * 32 + 8] each
   size_t red_bytes;
   size_t ts_bytes;
   size_t recv_bytes;
   size_t recv_off;  // offset of the receive buffer inside the staging area
-  size_t nw_bytes;
   size_t total;
 };
 
@@ -78,13 +81,12 @@ __host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn, int S) {
   // split-K: every CTA pushes its tile's columns for the tokens another CTA finishes into that CTA's
   // receive buffer [S][16 RG rows][tokens per CTA]
   m.recv_bytes = S > 1 ? (size_t)S * 16 * RG * ((NT * 8 + S - 1) / S) * 4 : 0;
-  m.nw_bytes = (size_t)ktn * 32 * 4;  // the norm weight slice of this CTA's K-range
   const size_t tail = m.red_bytes + m.ts_bytes;
-  const size_t stage = m.x_bytes + (NT <= 2 ? kWholeRowsBytes : 0);  // + whole residual rows (norm prologue)
   // the receive buffer gets its own space: peers push into it while this CTA may still be staging X or
   // reducing its own tile
-  m.recv_off = stage > tail ? stage : tail;
-  m.total = m.w_bytes + m.nw_bytes + m.recv_off + m.recv_bytes;
+  m.recv_off = m.x_bytes > tail ? m.x_bytes : tail;
+  m.recv_off = (m.recv_off + 15) & ~(size_t)15;
+  m.total = m.w_bytes + m.recv_off + m.recv_bytes;
   if (m.tma && m.total > kSmemBudget) {  // too big with the weights staged: stream them through registers
     m.tma = false;
     m.total -= m.w_bytes;
@@ -93,7 +95,6 @@ __host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn, int S) {
   return m;
 }
 
-// One 16x32 weight tile against NT 8-token column tiles of X: the hi plane into acc, the lo plane into accl.
 template <int NT>
 ENG_DEVICE void mma_tile(float (&acc)[NT][4], float (&accl)[NT][4], const uint4& a0, const uint4& a1, const bf16* xs,
                          const bf16* xl, int xstride, int kt, int lane) {
@@ -128,7 +129,7 @@ ENG_DEVICE void stage8(bf16* xs, bf16* xl, int idx, const float4 a, const float4
 
 template <int NT, int EPI, bool NORM_IN>
 __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
-  constexpr int kPre = NT <= 2 ? kPreMax : (NT == 4 ? kPreMax / 2 : kPreMax / 4);
+  constexpr int kPre = NT <= 2 ? kPreMax / 2 : (NT == 4 ? kPreMax / 4 : kPreMax / 8);
   constexpr int kUnroll = NT >= 8 ? 2 : 4;  // weight k-tiles loaded per group (register budget)
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float s_rstd[64];
@@ -137,7 +138,8 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
   __shared__ int s_pos[64];            //               and its position
   __shared__ float s_cs[kCsTokens][128];  //          and its RoPE row (cos, sin pairs) for the first tokens
   __shared__ float s_qn[128], s_kn[128];   //          the QK-norm weights
-  __shared__ float s_bias[128];            //          and this CTA's bias rows
+  __shared__ float s_row[128];  // per output row of this CTA: bias (QKV, STORE) or next norm weight (RESID)
+  __shared__ __align__(8) uint64_t s_wbar, s_xbar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rgi = blockIdx.x, split = blockIdx.y, chunk = blockIdx.z;
   const int S = p.S;
@@ -150,26 +152,29 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
   const int row_tile = rgi * RG + rt;
   const int ntok = min(NT * 8, p.T - n0);  // valid tokens of this chunk
   const GemmSmem sm = gemm_smem(NT, RG, ktn, S);
+  const int rows = 16 * RG;
+  const int row0 = rgi * rows;
 
-  // ---- before waiting: weights do not depend on the preceding kernel
-  __shared__ __align__(8) uint64_t s_wbar;
-  float* nw_s = reinterpret_cast<float*>(smem + sm.w_bytes);  // norm weight slice (NORM_IN)
-  uint8_t* area = smem + sm.w_bytes + sm.nw_bytes;            // X staging, then the reduction tiles
+  // ---- before waiting: weights and step inputs do not depend on the preceding kernel
+  uint8_t* area = smem + sm.w_bytes;  // X staging, then the reduction tiles
+  bf16* xs = reinterpret_cast<bf16*>(area);
+  const int xstride = sm.piece * 32 + 8;           // padded row stride of a plane (16-byte multiple)
+  bf16* xl = xs + (size_t)NT * 8 * xstride;        // lo plane
   cg::cluster_group cluster = cg::this_cluster();
   const uint4* wp = reinterpret_cast<const uint4*>(p.W) + ((size_t)row_tile * KT + kt0) * 64 + lane;
   const int pn0 = min(sm.piece, ktn);
   uint4 pre[kPre][2];
-  if (sm.tma) {
-    // the CTA's whole slice (RG row tiles x ktn k-tiles, contiguous per row tile) into shared memory
-    if (threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
+    mbar_init(&s_xbar, 1);
+    if (sm.tma) {  // the CTA's whole slice (RG row tiles x ktn k-tiles, contiguous per row tile)
       mbar_init(&s_wbar, 1);
       mbar_expect_tx(&s_wbar, (uint32_t)sm.w_bytes);
       for (int r = 0; r < RG; ++r)
         tma_load_1d(smem + (size_t)r * ktn * 1024, p.W + ((size_t)(rgi * RG + r) * KT + kt0) * 512,
                     (uint32_t)ktn * 1024u, &s_wbar);
     }
-    __syncthreads();  // the barrier is initialised before any thread waits on it
-  } else {
+  }
+  if (!sm.tma) {
 #pragma unroll
     for (int u = 0; u < kPre; ++u) {
       const int kt = kg + u * KG;
@@ -184,6 +189,13 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       prefetch_l2(p.W + ((size_t)(rgi * RG + threadIdx.x) * KT + kt0) * 512, (uint32_t)ktn * 1024u);
   }
   if (threadIdx.x == 32 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
+  // padding token rows of both planes are zero (the copies below fill rows < ntok only)
+  {
+    const int pad = (NT * 8 - ntok) * xstride / 8;  // 16-byte chunks per plane
+    uint4* zh = reinterpret_cast<uint4*>(xs + (size_t)ntok * xstride);
+    uint4* zl = reinterpret_cast<uint4*>(xl + (size_t)ntok * xstride);
+    for (int i = threadIdx.x; i < pad; i += 256) zh[i] = zl[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
 
   // tokens this CTA finishes: split, split + S, ... (all of them when S == 1)
   const int tok_first = S > 1 ? split : 0;
@@ -217,22 +229,31 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       s_qn[threadIdx.x] = p.q_norm ? p.q_norm[threadIdx.x] : 1.f;
       s_kn[threadIdx.x] = p.k_norm ? p.k_norm[threadIdx.x] : 1.f;
     }
-    if (threadIdx.x < 16 * RG) s_bias[threadIdx.x] = p.bias ? p.bias[rgi * 16 * RG + threadIdx.x] : 0.f;
   }
-  float4 wn_pre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-  const int cpr0 = pn0 * 4;
-  const bool reg_stage = NORM_IN && ntok * cpr0 <= 256;  // one 8-column chunk of X per thread
-  if (reg_stage && threadIdx.x < ntok * cpr0) {
-    const float4* wn = reinterpret_cast<const float4*>(p.norm_w + kt0 * 32 + (threadIdx.x % cpr0) * 8);
-    wn_pre[0] = wn[0];
-    wn_pre[1] = wn[1];
+  if (threadIdx.x < rows) {
+    const float* rv = EPI == EPI_RESID ? p.next_norm_w : p.bias;
+    s_row[threadIdx.x] = rv ? rv[row0 + threadIdx.x] : (EPI == EPI_RESID ? 1.f : 0.f);
   }
-  if (NORM_IN)
-    for (int i = threadIdx.x; i < ktn * 8; i += 256)
-      reinterpret_cast<float4*>(nw_s)[i] = reinterpret_cast<const float4*>(p.norm_w + kt0 * 32)[i];
+  __syncthreads();        // barriers initialised, padding rows zeroed
   if (S > 1) cluster.sync();  // every CTA of the cluster has started before any pushes into its memory
   pdl_trigger();
   pdl_wait();
+
+  // X piece [pc, pc + pn) k-tiles: one bulk copy per token row and plane, issued by warp 0
+  auto issue_x = [&](int pc, int pn) {
+    if (warp == 0) {
+      if (lane == 0) mbar_expect_tx(&s_xbar, (uint32_t)(ntok * pn * 64 * 2));
+      __syncwarp();
+      for (int r = lane; r < ntok; r += 32) {
+        const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
+        const size_t off = (size_t)src * p.ldx + (size_t)(kt0 + pc) * 32;
+        tma_load_1d(xs + (size_t)r * xstride, p.Xh + off, (uint32_t)pn * 64u, &s_xbar);
+        tma_load_1d(xl + (size_t)r * xstride, p.Xl + off, (uint32_t)pn * 64u, &s_xbar);
+      }
+    }
+  };
+  issue_x(0, pn0);
+
   // EPI_RESID: the residual values this thread updates in the epilogue (warps over its first two owned
   // tokens, lanes over up to four rows each), fetched now so the epilogue needs no further round trip
   float h_old[2][4];
@@ -243,54 +264,19 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int r = lane + 32 * b;
-        h_old[a][b] = (k < nown && r < 16 * RG)
-                          ? p.resid[(size_t)(n0 + tok_first + k * tok_step) * p.N + rgi * 16 * RG + r]
-                          : 0.f;
+        h_old[a][b] = (k < nown && r < rows) ? p.resid[(size_t)(n0 + tok_first + k * tok_step) * p.N + row0 + r] : 0.f;
       }
     }
   }
-  // small token counts: every CTA loads its tokens' whole residual rows once and computes their norms
-  // itself, so the norm costs no round trip beyond the load of X
-  const bool whole_rows = NORM_IN && NT <= 2 && (size_t)ntok * p.K * 4 <= kWholeRowsBytes;
-  float* hrow_s = reinterpret_cast<float*>(area + sm.x_bytes);  // [ntok][K] fp32 when whole_rows
-  if (whole_rows) {
-    for (int i = threadIdx.x; i < ntok * (p.K / 4); i += 256) {
-      const int r = i / (p.K / 4), c4 = i - r * (p.K / 4);
+  if (NORM_IN) {  // 1 / rms of each staged token, from its producer's partial sums of squares
+    for (int r = warp; r < ntok; r += 8) {
       const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
-      reinterpret_cast<float4*>(hrow_s)[i] = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K)[c4];
-    }
-    __syncthreads();
-    for (int r = warp; r < NT * 8; r += 8) {
+      const float* part = p.sq_in + (size_t)src * p.sq_stride;
       float ss = 0.f;
-      if (r < ntok) {
-        for (int c = lane; c < p.K; c += 32) ss += hrow_s[(size_t)r * p.K + c] * hrow_s[(size_t)r * p.K + c];
-        ss = warp_sum(ss);
-      }
-      if (lane == 0) s_rstd[r] = r < ntok ? rsqrtf(ss / (float)p.K + p.eps) : 0.f;
+      for (int j = lane; j < p.sq_parts; j += 32) ss += part[j];
+      ss = warp_sum(ss);
+      if (lane == 0) s_rstd[r] = rsqrtf(ss / (float)p.K + p.eps);
     }
-    __syncthreads();
-  }
-  float4 h_pre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-  if (!whole_rows && reg_stage && threadIdx.x < ntok * cpr0) {  // in flight together with the partial sums below
-    const int r = threadIdx.x / cpr0;
-    const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
-    const float4* hp = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K + kt0 * 32 + (threadIdx.x % cpr0) * 8);
-    h_pre[0] = hp[0];
-    h_pre[1] = hp[1];
-  }
-
-  if (NORM_IN && !whole_rows) {  // 1 / rms of each staged token, from its producer's partial sums of squares
-    for (int r = warp; r < NT * 8; r += 8) {
-      float ss = 0.f;
-      if (r < ntok) {
-        const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
-        const float* part = p.sq_in + (size_t)src * p.sq_stride;
-        for (int j = lane; j < p.sq_parts; j += 32) ss += part[j];
-        ss = warp_sum(ss);
-      }
-      if (lane == 0) s_rstd[r] = r < ntok ? rsqrtf(ss / (float)p.K + p.eps) : 0.f;
-    }
-    __syncthreads();
   }
 
   float acc[NT][4], accl[NT][4];
@@ -300,51 +286,23 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
     accl[nt][0] = accl[nt][1] = accl[nt][2] = accl[nt][3] = 0.f;
   }
 
-  bf16* xs = reinterpret_cast<bf16*>(area);
-  bf16* xl = xs + (size_t)NT * 8 * (sm.piece * 32 + 8);  // lo plane
   const uint4* ws = reinterpret_cast<const uint4*>(smem) + (size_t)rt * ktn * 64 + lane;  // tma: this warp's row tile
   if (sm.tma && !mbar_wait(&s_wbar, 0, 1u << 26)) {
     set_status(p.status, ST_TIMEOUT);
     mbar_wait(&s_wbar, 0, 1u << 26);  // never leave while the copy may still write shared memory
   }
-  for (int pc = 0; pc < ktn; pc += sm.piece) {
+  int piece_no = 0;
+  for (int pc = 0; pc < ktn; pc += sm.piece, ++piece_no) {
     const int pn = min(sm.piece, ktn - pc);
-    const int xstride = pn * 32 + 8;
-    const int cpr = pn * 4;  // 16-byte chunks per staged row
-    if (pc > 0) __syncthreads();
-    for (int i = threadIdx.x; i < NT * 8 * cpr; i += 256) {
-      const int r = i / cpr, c = i - r * cpr;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-      if (whole_rows) {
-        if (r < ntok) {
-          const int col = (kt0 + pc) * 32 + c * 8;
-          const float4* hp = reinterpret_cast<const float4*>(hrow_s + (size_t)r * p.K + col);
-          const float4* wn = reinterpret_cast<const float4*>(nw_s + (pc + c / 4) * 32 + (c & 3) * 8);
-          a = scale4(hp[0], s_rstd[r], wn[0]);
-          b = scale4(hp[1], s_rstd[r], wn[1]);
-        }
-      } else if (reg_stage && pc == 0) {
-        if (r < ntok) {
-          a = scale4(h_pre[0], s_rstd[r], wn_pre[0]);
-          b = scale4(h_pre[1], s_rstd[r], wn_pre[1]);
-        }
-      } else if (r < ntok) {
-        const int col = (kt0 + pc) * 32 + c * 8;
-        if (NORM_IN) {
-          const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
-          const float4* hp = reinterpret_cast<const float4*>(p.h_in + (size_t)src * p.K + col);
-          const float4* wn = reinterpret_cast<const float4*>(nw_s + (pc + c / 4) * 32 + (c & 3) * 8);
-          a = scale4(hp[0], s_rstd[r], wn[0]);
-          b = scale4(hp[1], s_rstd[r], wn[1]);
-        } else {
-          const float4* xp = reinterpret_cast<const float4*>(p.X + (size_t)(n0 + r) * p.ldx + col);
-          a = xp[0];
-          b = xp[1];
-        }
-      }
-      stage8(xs, xl, r * xstride + c * 8, a, b);
+    if (pc > 0) {  // every warp is done with the previous piece before its rows are overwritten
+      __syncthreads();
+      if (warp == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue_x(pc, pn);
     }
-    __syncthreads();
+    if (!mbar_wait(&s_xbar, piece_no & 1, 1u << 26)) {
+      set_status(p.status, ST_TIMEOUT);
+      mbar_wait(&s_xbar, piece_no & 1, 1u << 26);
+    }
 
     if (sm.tma) {
       constexpr int UT = kUnroll;
@@ -426,8 +384,6 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
     ts[(r0 + 8) * TS + c0 + 1] = v.w;
   }
   __syncthreads();
-  const int rows = 16 * RG;
-  const int row0 = rgi * rows;
 
   // ---- split-K across the cluster: CTA `split` finishes tokens split, split + S, ... (sum in split order)
   if (S > 1) {
@@ -451,23 +407,34 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
     }
     __syncthreads();
   }
+  if (NORM_IN) {  // RMSNorm(h) W^T = (1 / rms(h)) ((h * w) W^T)
+    for (int i = threadIdx.x; i < rows * nown; i += 256) {
+      const int k = i / rows, r = i - k * rows;
+      const int tok = tok_first + k * tok_step;
+      ts[r * TS + tok] *= s_rstd[tok];
+    }
+    __syncthreads();
+  }
   if (EPI == EPI_STORE_F32) {
     for (int i = threadIdx.x; i < rows * nown; i += 256) {
       const int k = i / rows, r = i - k * rows;
       const int tok = tok_first + k * tok_step;
-      p.out_f32[(size_t)(n0 + tok) * p.ldo + row0 + r] = ts[r * TS + tok] + (p.bias ? p.bias[row0 + r] : 0.f);
+      p.out_f32[(size_t)(n0 + tok) * p.ldo + row0 + r] = ts[r * TS + tok] + s_row[r];
     }
   } else if (EPI == EPI_RESID) {
-    // h += Y and this CTA's share of each token's sum of squares (lanes over rows, warps over tokens)
+    // h += Y, this CTA's share of each token's sum of squares (lanes over rows, warps over tokens) and
+    // the next GEMM's operand planes of h * next norm weight
     for (int k = warp; k < nown; k += 8) {
       const int tok = tok_first + k * tok_step;
-      float* hrow = p.resid + (size_t)(n0 + tok) * p.N + row0;
+      const size_t base = (size_t)(n0 + tok) * p.N + row0;
+      float* hrow = p.resid + base;
       float ss = 0.f;
       for (int r = lane; r < rows; r += 32) {
         const int a = k >> 3, b = r >> 5;
         const float old = (a < 2 && b < 4) ? h_old[a & 1][b & 3] : hrow[r];
         const float v = old + ts[r * TS + tok];
         hrow[r] = v;
+        put_split(p.xh_out, p.xl_out, base + r, v * s_row[r]);
         ss += v * v;
       }
       ss = warp_sum(ss);
@@ -481,7 +448,7 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       const int tok = tok_first + k * tok_step;
       const int r = (jj >> 3) * 16 + (jj & 7);
       const float ga = ts[r * TS + tok], up = ts[(r + 8) * TS + tok];
-      p.out_act[(size_t)(n0 + tok) * I + (row0 >> 1) + jj] = ga / (1.f + expf(-ga)) * up;
+      put_split(p.xh_out, p.xl_out, (size_t)(n0 + tok) * I + (row0 >> 1) + jj, ga / (1.f + expf(-ga)) * up);
     }
   } else if (EPI == EPI_QKV_ROPE) {
     const int D = p.d;
@@ -506,7 +473,7 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       float x[4];
       for (int e = 0; e < E; ++e) {
         const int r = rbase + lane * E + e;
-        x[e] = ts[r * TS + tok] + s_bias[r];
+        x[e] = ts[r * TS + tok] + s_row[r];
       }
       const bool is_q = head < p.Hq;
       const bool is_k = !is_q && head < p.Hq + p.Hkv;

@@ -30,6 +30,9 @@ struct EmbedParams {
   float* h_out;          // residual rows [rows][H]
   float* sq_out;         // sum of squares of each row -> sq_out[row * sq_stride]
   int sq_stride;
+  const float* norm_w;   // the first layer's input-norm weight [H]
+  bf16* xh_out;          // operand planes of h * norm_w [rows][H] (see GemmParams)
+  bf16* xl_out;
   int rows, H, V;
   int* status;
 };
@@ -40,7 +43,12 @@ enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID = 1, EPI_SILU = 2, EPI_LMHEAD = 3, E
 
 struct GemmParams {
   const bf16* W;   // packed [N][K]
-  const float* X;  // activations row-major [>= T][ldx] fp32 (plain prologue), staged as bf16 hi/lo pairs
+  // Activation operand: two bf16 planes [rows][ldx], hi = bf16(x) and lo = bf16(x - hi), written by the
+  // producing kernel; row x_rows[t] (or t) is token t's.  With a norm (NORM_IN) the planes hold h * norm_w
+  // and the kernel scales token t's outputs by 1 / rms(h_t), from the producer's partial sums of squares.
+  const bf16* Xh;
+  const bf16* Xl;
+  const int* x_rows;
   int ldx;
   int T, N, K;
   int RG;           // 16-row tiles per CTA (1, 2, 4, 8)
@@ -48,13 +56,10 @@ struct GemmParams {
   int kt_per_split; // 32-column k tiles per split (the S split CTAs of a row group form a cluster)
   const void* pf_ptr;           // weights of a later kernel to prefetch into L2 (pf_bytes, multiple of 16)
   unsigned long long pf_bytes;
-  // norm prologue: X = RMSNorm(h_in[x_rows[t] or t]) * norm_w, from sq_parts partial sums of squares
-  const float* h_in;
-  const float* norm_w;
+  // norm: 1 / rms of token t from its sq_parts partial sums of squares sq_in[x_rows[t] * sq_stride + j]
   const float* sq_in;
   int sq_parts;
   int sq_stride;
-  const int* x_rows;
   float eps;
   // epilogues
   float* out_f32;   // EPI_STORE_F32: out[t][n] (+ bias[n]), row stride ldo
@@ -62,7 +67,9 @@ struct GemmParams {
   const float* bias;
   float* resid;     // EPI_RESID: resid[t][n] += v (row stride N); sq_out[t * sq_stride + row group] = sum h^2
   float* sq_out;
-  float* out_act;   // EPI_SILU: out[t][j] = silu(gate_j) * up_j, row stride N / 2
+  const float* next_norm_w;  //         and the next GEMM's operand planes of h * next_norm_w
+  bf16* xh_out;     // EPI_RESID, EPI_SILU: operand planes written for the next GEMM (row stride N, or N / 2)
+  bf16* xl_out;     // EPI_SILU: silu(gate_j) * up_j
   // EPI_QKV_ROPE: CTA rows are whole heads of the fused [q | k | v] projection
   const int* positions;
   const int* tok2req;
@@ -104,7 +111,8 @@ struct AttnDecodeParams {
   const int* cu;          // [R+1]: request r's query token is cu[r]
   int r0;                 // first request handled (grid.x = rows)
   int rows;
-  float* out;             // [T][Hq * d]
+  bf16* out_h;            // operand planes of the output [T][Hq * d] (hi, lo) for the output projection
+  bf16* out_l;
   int Hq, Hkv, d, NB;
   int split_blocks;       // KV blocks per split
   int max_splits;         // grid.z = cluster size (<= 8): the splits of a (row, KV head) merge on chip
@@ -124,7 +132,8 @@ struct AttnPrefillParams {
   const int* positions;   // [T]
   const int4* items;      // work items: (request, first token, token count <= 64, unused)
   int n_items;
-  float* out;             // [T][Hq * d]
+  bf16* out_h;            // operand planes of the output [T][Hq * d]
+  bf16* out_l;
   int Hq, Hkv, d, NB;
   float scale_log2;
   int* status;
@@ -144,6 +153,8 @@ struct AdvanceParams {
   int* status;
 };
 cudaError_t launch_advance(const AdvanceParams& p, const LaunchOpts& o, cudaStream_t s);
+// One thread sleeping on the global timer for `ns` nanoseconds (front of a launch-by-launch timed step).
+cudaError_t launch_hold(unsigned long long ns, cudaStream_t s);
 
 // ------------------------------------------------------------------ sampler pieces (sample.cu)
 cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int vocab, float* out, cudaStream_t s);

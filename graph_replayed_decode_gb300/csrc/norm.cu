@@ -1,9 +1,10 @@
 // norm.cu -- embedding gather of layer 0 into the fp32 residual stream.
 //
-// h[t] = E[id[t]] (the embedding is stored packed; packed_offset finds each element) and the row's sum of
-// squares, which the first QKV GEMM turns into its input RMSNorm ("33. Removing overhead", section
-// "Fewer, larger matmuls": add_norm does a residual update and the next norm in one pass; here every norm
-// is folded into the GEMM that consumes it).  One CTA per token, fixed reduction order.
+// h[t] = E[id[t]] (the embedding is stored packed; packed_offset finds each element), the row's sum of
+// squares, and the first QKV GEMM's operand planes of h * w_in, which that GEMM turns into its input
+// RMSNorm by scaling with 1 / rms(h) ("33. Removing overhead", section "Fewer, larger matmuls": add_norm
+// does a residual update and the next norm in one pass; here every norm is folded into the GEMM that
+// consumes it).  One CTA per token, fixed reduction order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,6 +28,7 @@ __global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
     const float v = __bfloat162float(p.embed[packed_offset(id, c, H)]);
     p.h_out[(size_t)row * H + c] = v;
+    put_split(p.xh_out, p.xl_out, (size_t)row * H + c, v * p.norm_w[c]);
     ss += v * v;
   }
   ss = warp_sum(ss);

@@ -207,8 +207,10 @@ int eng_decode(eng_t* e, int32_t n_steps, int32_t* out_ids_dev);
  * n_steps = 1, launched eagerly on the engine's stream) with a CUDA event pair around each launch, and
  * report per launch its kind (ENG_K_*), duration in milliseconds and algorithmic HBM bytes (weights
  * read once, activations in and out, K/V read over the rows' current lengths and written at the new
- * position).  kinds/ms/bytes: host arrays of `capacity` entries; *count receives the launch count.
- * Synchronises the stream.  Errors: ENG_ESTATE (no decode batch), ENG_EINVAL (capacity too small).
+ * position).  A 20 ms device-side hold runs first so that the whole step is enqueued before its first
+ * kernel starts: the pairs then time device work only (launches run back to back, without the overlap
+ * programmatic dependent launch gives them inside a graph).  kinds/ms/bytes: host arrays of `capacity`
+ * entries; *count receives the launch count.  Synchronises the stream.  Errors: ENG_ESTATE (no decode batch), ENG_EINVAL (capacity too small).
  */
 int eng_profile(eng_t* e, int32_t capacity, int32_t* kinds, float* ms, int64_t* bytes, int32_t* count);
 
