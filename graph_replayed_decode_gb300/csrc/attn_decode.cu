@@ -15,9 +15,11 @@
 // 4 warps takes every 4th block of the range (cp.async double buffering into an XOR-swizzled tile; blocks
 // already in the pool are fetched before the kernel waits for the preceding kernel, only the block that
 // holds this step's new token after), computes S = Q K^T and O += P V with bf16 m16n8k16 MMAs and an
-// online softmax in base 2.  Warps merge through shared memory.  The splits of one (row, KV head) form a
-// thread-block cluster: split 0 merges them through distributed shared memory in split order, so the
-// result does not depend on timing and needs no global workspace.
+// online softmax in base 2.  Warps merge through shared memory.  A split past the row's length (short
+// rows in a batch sized for long ones) exits at once.  With several splits, each writes its unnormalised
+// (O, max, sum) to a global workspace and counts itself in on an atomic counter; the split that finishes
+// last merges all of them in split order and resets the counter, so the result does not depend on which
+// split finishes last, and the next launch (or graph replay) finds the counter at zero.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -28,7 +30,8 @@ namespace cg = cooperative_groups;
 namespace grd {
 
 static constexpr int kStages = 2;    // K/V blocks in flight per warp
-static constexpr int kMaxSplits = 8;  // splits of one (row, KV head): one thread-block cluster
+static constexpr int kMaxSplits = 16;   // splits of one (row, KV head)
+static constexpr int kClusterSplits = 8;  // at most this many merge on chip (one thread-block cluster)
 
 // Per-warp K/V stages, reused for the warp merge afterwards ([4][16] M, [4][16] L, [4][16][D] O, [G][D+2]).
 __host__ __device__ constexpr size_t attn_stage_bytes(int D) {
@@ -37,7 +40,36 @@ __host__ __device__ constexpr size_t attn_stage_bytes(int D) {
              : (size_t)(128 + 4 * 16 * D + 16 * (D + 2)) * 4;
 }
 
-template <int D>
+// Final merge of a row's split partials (O unnormalised, M, L per head), in split order, written as the
+// output projection's operand planes.  get(sp, head, j) reads partial sp's value j (j < D: O, D: M,
+// D + 1: L); the on-chip and the global-memory merges share this code, so they agree bit for bit.
+template <int D, typename Get>
+ENG_DEVICE void merge_splits(const AttnDecodeParams& p, int nsplit, int G, size_t obase, float* s_w, float* s_inv,
+                             Get get) {
+  if (threadIdx.x < G) {
+    const int hr = threadIdx.x;
+    float M = -INFINITY;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, get(sp, hr, D));
+    float L = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float w = exp2f(get(sp, hr, D) - M);
+      s_w[sp * G + hr] = w;
+      L += get(sp, hr, D + 1) * w;
+    }
+    s_inv[hr] = 1.f / L;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int hr = i / D, dd = i - hr * D;
+    float O = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) O += get(sp, hr, dd) * s_w[sp * G + hr];
+    put_split(p.out_h, p.out_l, obase + hr * D + dd, O * s_inv[hr]);
+  }
+}
+
+// CLUSTER: the splits of a (row, KV head) form a thread-block cluster and split 0 merges them from its
+// own shared memory (lowest latency; few rows).  Otherwise the global workspace and the last finisher.
+template <int D, bool CLUSTER>
 __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   constexpr int NCH = D / 8;  // 16-byte chunks per key row
   constexpr int KS = D / 16;  // k-steps of Q K^T
@@ -47,6 +79,8 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   const int g = lane >> 2, t = lane & 3;
   const int G = p.Hq / p.Hkv;
   const int h0 = kvh * G;
+  __shared__ int s_last;
+  __shared__ float s_w[kMaxSplits * 8], s_inv[8];
   cg::cluster_group cluster = cg::this_cluster();
 
   if (threadIdx.x == 0 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
@@ -64,10 +98,17 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   const bool active = sl > 0 && split < nsplit;
   const int b_begin = split * p.split_blocks;
   const int b_end = min(nblk, b_begin + p.split_blocks);
+  if (!CLUSTER && !active) {  // nothing to read: a padding row (zeros from split 0) or a split past its length
+    pdl_trigger();
+    if (sl <= 0 && split == 0) {
+      pdl_wait();
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x) put_split(p.out_h, p.out_l, obase + i, 0.f);
+    }
+    return;
+  }
 
   extern __shared__ __align__(16) uint8_t smem[];
   bf16* wbuf = reinterpret_cast<bf16*>(smem) + warp * (kStages * 2 * TILE);  // kStages x (K, V) per warp
-  float* recv = reinterpret_cast<float*>(smem + attn_stage_bytes(D));        // split 0: [splits][G][D + 2]
 
   float o[D / 8][4];
 #pragma unroll
@@ -105,7 +146,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
     if (bb == nblk - 1) break;
     issue(bb, issued);
   }
-  if (p.max_splits > 1) cluster.sync();  // every split has started before any pushes into split 0's memory
+  if (CLUSTER && p.max_splits > 1) cluster.sync();  // every split has started before pushes into split 0
   pdl_trigger();
   pdl_wait();
   for (; issued < ahead; ++issued) issue(b_begin + warp + 4 * issued, issued);
@@ -221,7 +262,6 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   float* ms = reinterpret_cast<float*>(smem);  // [4][16]
   float* ls = ms + 64;                          // [4][16]
   float* os = ls + 64;                          // [4][16][D]
-  float* part = os + 4 * 16 * D;                // [G][D + 2]
   if (t == 0) {
     ms[warp * 16 + g] = m0;
     ls[warp * 16 + g] = l0;
@@ -233,72 +273,104 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
     r0[1] = o[c][1] + o[c][3];
   }
   __syncthreads();
-  if (active) {
-    float* dst = nsplit > 1 ? cluster.map_shared_rank(recv, 0) + (size_t)split * G * (D + 2) : nullptr;
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-      const int hr = i / D, dd = i - hr * D;
-      float M = -INFINITY;
+  // this CTA's partial (O unnormalised, M, L) of head hr, element dd
+  auto partial = [&](int hr, int dd, float& O, float& M, float& L) {
+    M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) M = fmaxf(M, ms[w * 16 + hr]);
-      float L = 0.f, O = 0.f;
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, ms[w * 16 + hr]);
+    L = 0.f;
+    O = 0.f;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float sc_ = exp2f(ms[w * 16 + hr] - M);
-        L += ls[w * 16 + hr] * sc_;
-        O += os[(w * 16 + hr) * D + dd] * sc_;
-      }
-      if (nsplit == 1) {
-        put_split(p.out_h, p.out_l, obase + hr * D + dd, O / L);
-      } else {  // push this split's (O, M, L) into split 0's receive buffer
-        dst[hr * (D + 2) + dd] = O;
-        if (dd == 0) {
-          dst[hr * (D + 2) + D] = M;
-          dst[hr * (D + 2) + D + 1] = L;
-        }
-      }
+    for (int w = 0; w < 4; ++w) {
+      const float sc_ = exp2f(ms[w * 16 + hr] - M);
+      L += ls[w * 16 + hr] * sc_;
+      O += os[(w * 16 + hr) * D + dd] * sc_;
     }
-  } else if (sl <= 0 && split == 0) {  // padding row: zeros
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) put_split(p.out_h, p.out_l, obase + i, 0.f);
-  }
+  };
 
-  // ---- split 0 merges the pushed partials, in split order, from its own shared memory
-  if (p.max_splits > 1) {
-    cluster.sync();
-    if (split == 0 && sl > 0 && nsplit > 1) {
-      float* wts = ms;           // [nsplit][G] weights (nsplit * G <= 128)
-      float* inv = ms + 8 * 16;  // [G] 1 / L
-      if (threadIdx.x < G) {
-        const int hr = threadIdx.x;
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, recv[((size_t)sp * G + hr) * (D + 2) + D]);
-        float L = 0.f;
-        for (int sp = 0; sp < nsplit; ++sp) {
-          const float w = exp2f(recv[((size_t)sp * G + hr) * (D + 2) + D] - M);
-          wts[sp * G + hr] = w;
-          L += recv[((size_t)sp * G + hr) * (D + 2) + D + 1] * w;
-        }
-        inv[hr] = 1.f / L;
-      }
-      __syncthreads();
+  if (CLUSTER) {
+    float* recv = reinterpret_cast<float*>(smem + attn_stage_bytes(D));  // split 0: [splits][G][D + 2]
+    if (active) {
+      float* dst = nsplit > 1 ? cluster.map_shared_rank(recv, 0) + (size_t)split * G * (D + 2) : nullptr;
       for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
         const int hr = i / D, dd = i - hr * D;
-        float O = 0.f;
-        for (int sp = 0; sp < nsplit; ++sp) O += recv[((size_t)sp * G + hr) * (D + 2) + dd] * wts[sp * G + hr];
-        put_split(p.out_h, p.out_l, obase + hr * D + dd, O * inv[hr]);
+        float O, M, L;
+        partial(hr, dd, O, M, L);
+        if (nsplit == 1) {
+          put_split(p.out_h, p.out_l, obase + hr * D + dd, O / L);
+        } else {  // push this split's partial into split 0's receive buffer
+          dst[hr * (D + 2) + dd] = O;
+          if (dd == 0) {
+            dst[hr * (D + 2) + D] = M;
+            dst[hr * (D + 2) + D + 1] = L;
+          }
+        }
+      }
+    } else if (sl <= 0 && split == 0) {  // padding row: zeros
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x) put_split(p.out_h, p.out_l, obase + i, 0.f);
+    }
+    if (p.max_splits > 1) {
+      cluster.sync();
+      if (split == 0 && sl > 0 && nsplit > 1)
+        merge_splits<D>(p, nsplit, G, obase, s_w, s_inv,
+                        [&](int sp, int hr, int j) { return recv[((size_t)sp * G + hr) * (D + 2) + j]; });
+    }
+    return;
+  }
+
+  float* part = p.ws + (((size_t)row * p.Hkv + kvh) * p.max_splits + split) * G * (D + 2);
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int hr = i / D, dd = i - hr * D;
+    float O, M, L;
+    partial(hr, dd, O, M, L);
+    if (nsplit == 1) {
+      put_split(p.out_h, p.out_l, obase + hr * D + dd, O / L);
+    } else {  // this split's unnormalised partial (O, M, L)
+      part[hr * (D + 2) + dd] = O;
+      if (dd == 0) {
+        part[hr * (D + 2) + D] = M;
+        part[hr * (D + 2) + D + 1] = L;
       }
     }
   }
+  if (nsplit == 1) return;
+
+  // ---- the last split to finish merges the partials in split order
+  __threadfence();
+  __syncthreads();
+  int* counter = p.counters + (size_t)row * p.Hkv + kvh;
+  if (threadIdx.x == 0) s_last = atomicAdd(counter, 1) == nsplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* parts = p.ws + ((size_t)row * p.Hkv + kvh) * p.max_splits * G * (D + 2);
+  merge_splits<D>(p, nsplit, G, obase, s_w, s_inv,
+                  [&](int sp, int hr, int j) { return __ldcg(parts + ((size_t)sp * G + hr) * (D + 2) + j); });
+  if (threadIdx.x == 0) *counter = 0;  // ready for the next launch
 }
 
+template <int D, bool CLUSTER>
+static cudaError_t launch_mode(const AttnDecodeParams& p, cudaLaunchConfig_t cfg) {
+  static bool set = false;
+  if (!set) {
+    cudaFuncSetAttribute(k_attn_decode<D, CLUSTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    set = true;
+  }
+  return cudaLaunchKernelEx(&cfg, k_attn_decode<D, CLUSTER>, p);
+}
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, cudaStream_t s) {
   if (p.rows <= 0) return cudaSuccess;
-  if (p.max_splits < 1 || p.max_splits > kMaxSplits) return cudaErrorInvalidValue;
+  if (p.max_splits < 1 || p.max_splits > kMaxSplits || p.Hq / p.Hkv > 8) return cudaErrorInvalidValue;
+  // a few rows: merge on chip (a cluster per row and KV head); many rows: the global workspace, so that
+  // splits past a short row's length leave their SM at once
+  const bool cluster = p.rows <= 4 && p.max_splits <= kClusterSplits;
+  if (!cluster && p.max_splits > 1 && (!p.ws || !p.counters)) return cudaErrorInvalidValue;
+  const int G = p.Hq / p.Hkv;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.rows, p.Hkv, p.max_splits);
   cfg.blockDim = dim3(128);
-  const int G = p.Hq / p.Hkv;
-  cfg.dynamicSmemBytes = attn_stage_bytes(p.d) + (size_t)kMaxSplits * G * (p.d + 2) * 4;
+  cfg.dynamicSmemBytes = attn_stage_bytes(p.d) + (cluster ? (size_t)kClusterSplits * G * (p.d + 2) * 4 : 0);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -308,23 +380,9 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, c
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = p.max_splits;
   cfg.attrs = attr;
-  cfg.numAttrs = p.max_splits > 1 ? 2 : 1;
-  if (p.d == 128) {
-    static bool set = false;
-    if (!set) {
-      cudaFuncSetAttribute(k_attn_decode<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      set = true;
-    }
-    return cudaLaunchKernelEx(&cfg, k_attn_decode<128>, p);
-  }
-  if (p.d == 64) {
-    static bool set = false;
-    if (!set) {
-      cudaFuncSetAttribute(k_attn_decode<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      set = true;
-    }
-    return cudaLaunchKernelEx(&cfg, k_attn_decode<64>, p);
-  }
+  cfg.numAttrs = cluster && p.max_splits > 1 ? 2 : 1;
+  if (p.d == 128) return cluster ? launch_mode<128, true>(p, cfg) : launch_mode<128, false>(p, cfg);
+  if (p.d == 64) return cluster ? launch_mode<64, true>(p, cfg) : launch_mode<64, false>(p, cfg);
   return cudaErrorInvalidValue;
 }
 

@@ -54,9 +54,18 @@ struct InLayout {
   size_t ids, pos, tok2req, cu, seq, last, invt, rng, wlog, step, items, bt, words;
 };
 
+// One projection of the step with its two launch plans: [0] for steps of at most 8 tokens, [1] for
+// larger ones (the plan only depends on the weight shape and the class, so every token count of a class
+// computes each output with the same summation order).
+struct GemmPlan {
+  int RG = 1, S = 1, ktn = 0;
+};
 struct GemmSite {
-  int N = 0, K = 0, RG = 1, S = 1, ktn = 0, rg_fixed = 0;
-  int groups() const { return N / 16 / RG; }
+  int N = 0, K = 0, rg_fixed = 0;
+  GemmPlan plan[2];
+  const GemmPlan& for_tokens(int T) const { return plan[T >= kLargePlanTokens ? 1 : 0]; }
+  int groups(int T) const { return N / 16 / for_tokens(T).RG; }
+  int max_groups() const { return std::max(N / 16 / plan[0].RG, N / 16 / plan[1].RG); }
 };
 
 }  // namespace
@@ -111,6 +120,8 @@ struct eng {
   int* status = nullptr;
   GemmSite g_qkv, g_o, g_gu, g_down, g_lm;
   int split_blocks = 4, max_splits = 1;
+  float* attn_ws = nullptr;    // decode attention partials of multi-split rows
+  int* attn_counters = nullptr;
   int* ring = nullptr;  // [ring_cap][bucket] ids recorded by the advance kernel
   int ring_cap = 1024;
 
@@ -408,7 +419,8 @@ static int setup_buffers(eng_t* e) {
     s.N = N;
     s.K = K;
     s.rg_fixed = rg_fixed;
-    gemm_plan(N, K, rg_fixed, &s.RG, &s.S, &s.ktn);
+    gemm_plan(N, K, rg_fixed, &s.plan[0].RG, &s.plan[0].S, &s.plan[0].ktn);
+    gemm_plan_large(N, K, rg_fixed, &s.plan[1].RG, &s.plan[1].S, &s.plan[1].ktn);
     return ENG_OK;
   };
   TRY(site(e->g_qkv, QKV, H, d / 16, Tm));  // a CTA owns one whole head (QK-norm and RoPE in the epilogue)
@@ -416,14 +428,15 @@ static int setup_buffers(eng_t* e) {
   TRY(site(e->g_gu, 2 * c.intermediate, H, 0, Tm));
   TRY(site(e->g_down, H, c.intermediate, 0, Tm));
   TRY(site(e->g_lm, c.vocab, H, 0, Rm));
-  e->sq_stride = std::max(e->g_o.groups(), e->g_down.groups());
+  e->sq_stride = std::max(e->g_o.max_groups(), e->g_down.max_groups());
   TRY(dev_alloc(e, &e->sq, (size_t)Tm * e->sq_stride));
 
-  // decode attention splits: 16-key blocks per split chosen from the block-table width so that a row has
-  // at most 8 splits (one thread-block cluster); fixed per engine, so eager and replayed steps agree bit
-  // for bit
-  e->split_blocks = (c.max_blocks_per_seq + 7) / 8;
+  // decode attention splits: up to 8 per row for block tables of at most 128 blocks (a row's splits can
+  // then merge on chip), up to 16 beyond; fixed per engine, so eager and replayed steps agree bit for bit
+  e->split_blocks = c.max_blocks_per_seq <= 128 ? (c.max_blocks_per_seq + 7) / 8 : (c.max_blocks_per_seq + 15) / 16;
   e->max_splits = (c.max_blocks_per_seq + e->split_blocks - 1) / e->split_blocks;
+  TRY(dev_alloc(e, &e->attn_ws, (size_t)Rm * c.kv_heads * e->max_splits * (c.q_heads / c.kv_heads) * (d + 2)));
+  TRY(dev_alloc(e, &e->attn_counters, (size_t)Rm * c.kv_heads));
 
   e->used.assign(c.num_blocks, 0);
   e->free_list.clear();
@@ -479,9 +492,10 @@ static GemmParams gemm_params(eng_t* e, const GemmSite& s, const bf16* W, int T)
   p.T = T;
   p.N = s.N;
   p.K = s.K;
-  p.RG = s.RG;
-  p.S = s.S;
-  p.kt_per_split = s.ktn;
+  const GemmPlan& pl = s.for_tokens(T);
+  p.RG = pl.RG;
+  p.S = pl.S;
+  p.kt_per_split = pl.ktn;
   p.ldo = s.N;
   p.eps = e->c.rms_eps;
   p.sq_stride = e->sq_stride;
@@ -622,6 +636,8 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
       dp.NB = c.num_blocks;
       dp.split_blocks = e->split_blocks;
       dp.max_splits = splits;
+      dp.ws = e->attn_ws;
+      dp.counters = e->attn_counters;
       dp.scale_log2 = scale_log2;
       dp.status = e->status;
       set_prefetch(e, dp.pf_ptr, dp.pf_bytes, L.gu, e->g_gu);
@@ -643,7 +659,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     po.xl_out = e->xn_l;
     set_prefetch(e, po.pf_ptr, po.pf_bytes, L.down, e->g_down);
     if ((r = gemm_launch(e, po, e->g_o, EPI_RESID, false, ENG_K_GEMM_O, st)) != cudaSuccess) return r;
-    sq_parts = e->g_o.groups();
+    sq_parts = e->g_o.groups(T);
 
     // ---- post-attention RMSNorm + fused gate|up projection + SiLU * up
     GemmParams pg = gemm_params(e, e->g_gu, L.gu, T);
@@ -666,7 +682,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     pd.xh_out = e->xn_h;
     pd.xl_out = e->xn_l;
     if ((r = gemm_launch(e, pd, e->g_down, EPI_RESID, false, ENG_K_GEMM_DOWN, st)) != cudaSuccess) return r;
-    sq_parts = e->g_down.groups();
+    sq_parts = e->g_down.groups(T);
   }
 
   // ---- final RMSNorm at each request's last token + LM head + sampling

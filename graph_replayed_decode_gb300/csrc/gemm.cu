@@ -605,6 +605,41 @@ void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split) {
   *kt_per_split = KT / best_s;
 }
 
+void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split) {
+  // Steps of more than 8 tokens: every CTA also reads its K-range of the activation planes for each token
+  // (T x K-range x 4 bytes from L2), which at 32 tokens outweighs a thin weight slice.  The plan minimises
+  // the bytes one SM moves, waves x (2 W + X) with W the CTA's weight slice (from HBM, counted twice) and X
+  // its activation slice for 32 tokens, over row groups of 1..8 tiles and 1..8 K splits in at most two
+  // waves (ties: fewer CTAs, then fewer splits).  Falls back to the small-step plan when nothing fits.
+  const int tiles = N / 16, KT = K / 32;
+  const int wave = 152;
+  double best = 0.0;
+  int best_rg = 0, best_s = 0, best_ctas = 0;
+  for (int rg = 1; rg <= 8; rg <<= 1) {
+    if ((rg_fixed > 0 && rg != rg_fixed) || tiles % rg) continue;
+    for (int sp = 1; sp <= kMaxCluster && sp <= KT; ++sp) {
+      if (KT % sp) continue;
+      const int ctas = tiles / rg * sp;
+      if (ctas > 2 * wave) continue;
+      const double w = (double)rg * 16 * (K / sp) * 2, x = 32.0 * (K / sp) * 4;
+      const double cost = (double)((ctas + wave - 1) / wave) * (2.0 * w + x);
+      if (best_ctas == 0 || cost < best || (cost == best && (ctas < best_ctas || (ctas == best_ctas && sp < best_s)))) {
+        best = cost;
+        best_rg = rg;
+        best_s = sp;
+        best_ctas = ctas;
+      }
+    }
+  }
+  if (best_ctas == 0) {
+    gemm_plan(N, K, rg_fixed, RG, S, kt_per_split);
+    return;
+  }
+  *RG = best_rg;
+  *S = best_s;
+  *kt_per_split = KT / best_s;
+}
+
 template <int NT, int EPI, bool NORM_IN>
 static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, dim3 grid) {
   const GemmSmem sm = gemm_smem(NT, p.RG, p.kt_per_split, p.S);

@@ -98,6 +98,10 @@ struct GemmParams {
 // Picks RG / S / kt_per_split for an [N][K] weight (independent of T, so every token count computes
 // each output with the same summation order).  rg_fixed > 0 forces the rows per CTA (whole heads).
 void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split);
+// The plan for steps of more than 8 tokens (activation bytes per CTA weigh in; see gemm.cu).
+void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split);
+// Token count from which a step uses the large plans.
+static constexpr int kLargePlanTokens = 9;
 cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const LaunchOpts& o, cudaStream_t s);
 
 // ------------------------------------------------------------------ attention (attn_decode.cu, attn_prefill.cu)
@@ -115,7 +119,9 @@ struct AttnDecodeParams {
   bf16* out_l;
   int Hq, Hkv, d, NB;
   int split_blocks;       // KV blocks per split
-  int max_splits;         // grid.z = cluster size (<= 8): the splits of a (row, KV head) merge on chip
+  int max_splits;         // grid.z (<= 16)
+  float* ws;              // [rows][Hkv][max_splits][G][d + 2] partials of multi-split rows
+  int* counters;          // [rows][Hkv] finished splits, zero between launches
   float scale_log2;       // log2(e) / sqrt(d)
   const void* pf_ptr;     // weights of a later kernel to prefetch into L2
   unsigned long long pf_bytes;

@@ -290,3 +290,28 @@ def test_device_decode_loop_equals_host_driven_steps(weights):
         assert g.status() == 0
     finally:
         g.close()
+
+
+def test_attention_merge_modes_agree_bit_for_bit(weights):
+    """Decode rows whose attention splits merge on chip (a batch of 4 rows) and through the global
+    workspace (the same rows plus two more) give bit-identical logits: a row's result does not depend on
+    the merge path nor on the other rows of the batch."""
+    from graph_replayed_decode_gb300.eng import StepArrays
+    g = _engine(weights)
+    try:
+        ctxs = [100, 37, 64, 17, 90, 50]                      # 2..7 blocks: several splits per row
+        blocks = [list(g.alloc(oracle.blocks_needed(c + 1))) for c in ctxs]
+        for l in range(S.layers):
+            for r, c in enumerate(ctxs):
+                g.fill_context(l, blocks[r], synth.kv_context(S, l, 200 + r, c))
+        bt = block_table(blocks, MBS)
+        ids = synth.decode_ids(6, S.vocab, 9)
+        pos = np.array(ctxs)
+        temps = np.zeros(6, dtype=np.float32)
+        a_ids, a_log = g.step(StepArrays(ids[:4], pos[:4], np.arange(5), bt[:4], pos[:4] + 1, temps[:4]))
+        b_ids, b_log = g.step(StepArrays(ids, pos, np.arange(7), bt, pos + 1, temps))
+        np.testing.assert_array_equal(a_log.view(np.uint32), b_log[:4].view(np.uint32))
+        np.testing.assert_array_equal(a_ids, b_ids[:4])
+        assert g.status() == 0
+    finally:
+        g.close()
