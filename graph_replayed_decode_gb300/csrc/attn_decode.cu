@@ -46,44 +46,68 @@ __host__ __device__ constexpr size_t attn_stage_bytes(int D) {
 template <int D, typename Get>
 ENG_DEVICE void merge_splits(const AttnDecodeParams& p, int nsplit, int G, size_t obase, float* s_w, float* s_inv,
                              Get get) {
+  // every value is loaded before the arithmetic starts (the partials may sit in L2: one round trip, not
+  // one per split); the sums still run in split order
   if (threadIdx.x < G) {
     const int hr = threadIdx.x;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, get(sp, hr, D));
-    float L = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float w = exp2f(get(sp, hr, D) - M);
-      s_w[sp * G + hr] = w;
-      L += get(sp, hr, D + 1) * w;
+    float ms[kMaxSplits], ls[kMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp) {
+      ms[sp] = sp < nsplit ? get(sp, hr, D) : -INFINITY;
+      ls[sp] = sp < nsplit ? get(sp, hr, D + 1) : 0.f;
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp)
+      if (sp < nsplit) M = fmaxf(M, ms[sp]);
+    float L = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp)
+      if (sp < nsplit) {
+        const float w = exp2f(ms[sp] - M);
+        s_w[sp * G + hr] = w;
+        L += ls[sp] * w;
+      }
     s_inv[hr] = 1.f / L;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int hr = i / D, dd = i - hr * D;
+    float v[kMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp) v[sp] = sp < nsplit ? get(sp, hr, dd) : 0.f;
     float O = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) O += get(sp, hr, dd) * s_w[sp * G + hr];
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp)
+      if (sp < nsplit) O += v[sp] * s_w[sp * G + hr];
     put_split(p.out_h, p.out_l, obase + hr * D + dd, O * s_inv[hr]);
   }
 }
 
-// CLUSTER: the splits of a (row, KV head) form a thread-block cluster and split 0 merges them from its
-// own shared memory (lowest latency; few rows).  Otherwise the global workspace and the last finisher.
+// Per-CTA scratch outside the dynamic K/V stages.
+struct AttnShared {
+  int last;
+  float w[kMaxSplits * 8];
+  float inv[8];
+};
+
+// One work item: split `split` of (row, KV head).  CLUSTER: the splits of a (row, KV head) are one
+// thread-block cluster and split 0 merges them from its own shared memory (lowest latency; few rows).
+// Otherwise partials go to the global workspace and the last split to finish merges them.
 template <int D, bool CLUSTER>
-__global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
+ENG_DEVICE void attn_item(const AttnDecodeParams& p, int row, int kvh, int split, uint8_t* smem, AttnShared& sh) {
   constexpr int NCH = D / 8;  // 16-byte chunks per key row
   constexpr int KS = D / 16;  // k-steps of Q K^T
   constexpr int TILE = 16 * D;
-  const int row = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int G = p.Hq / p.Hkv;
   const int h0 = kvh * G;
-  __shared__ int s_last;
-  __shared__ float s_w[kMaxSplits * 8], s_inv[8];
+  int& s_last = sh.last;
+  float* s_w = sh.w;
+  float* s_inv = sh.inv;
   cg::cluster_group cluster = cg::this_cluster();
 
-  if (threadIdx.x == 0 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
   // lengths and block tables are step inputs, final before the step's first kernel
   const int r = p.r0 + row;
   const int sl = p.seq_lens[r];
@@ -107,7 +131,6 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
     return;
   }
 
-  extern __shared__ __align__(16) uint8_t smem[];
   bf16* wbuf = reinterpret_cast<bf16*>(smem) + warp * (kStages * 2 * TILE);  // kStages x (K, V) per warp
 
   float o[D / 8][4];
@@ -115,8 +138,14 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   for (int c = 0; c < D / 8; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
   float m0 = -INFINITY, l0 = 0.f;  // running max / sum of head g (rows g and g + 8 are its two halves)
 
+  // this warp's blocks are b_begin + warp + 4 j; lane j holds the j-th one's pool id (block tables are
+  // step inputs), so issuing a copy needs no dependent load
+  const int nb = active && b_begin + warp < b_end ? (b_end - b_begin - warp + 3) / 4 : 0;
+  int my_blk = 0;
+  if (lane < nb) my_blk = p.bt[(size_t)r * p.mbs + b_begin + warp + 4 * lane];
   auto issue = [&](int b, int stage) {
-    int blk = p.bt[(size_t)r * p.mbs + b];
+    const int j = (b - b_begin - warp) >> 2;
+    int blk = j < 32 ? __shfl_sync(0xffffffffu, my_blk, j & 31) : p.bt[(size_t)r * p.mbs + b];
     if (blk < 0 || blk >= p.NB) {
       set_status(p.status, ST_BAD_BLOCK);
       blk = p.NB;
@@ -135,10 +164,9 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
     cp_async_commit();
   };
 
-  // this warp's blocks: b_begin + warp + 4 j, j < nb; up to kStages of them in flight.  Blocks already in
-  // the pool are fetched before the kernel waits for the preceding kernel; the block that holds this
-  // step's new token (the sequence's last block) only after.
-  const int nb = active && b_begin + warp < b_end ? (b_end - b_begin - warp + 3) / 4 : 0;
+  // up to kStages of this warp's blocks in flight.  Blocks already in the pool are fetched before the
+  // kernel waits for the preceding kernel; the block that holds this step's new token (the sequence's
+  // last block) only after.
   const int ahead = min(nb, kStages);
   int issued = 0;
   for (; issued < ahead; ++issued) {
@@ -349,19 +377,38 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecodeParams p) {
   if (threadIdx.x == 0) *counter = 0;  // ready for the next launch
 }
 
-template <int D, bool CLUSTER>
-static cudaError_t launch_mode(const AttnDecodeParams& p, cudaLaunchConfig_t cfg) {
-  static bool set = false;
-  if (!set) {
-    cudaFuncSetAttribute(k_attn_decode<D, CLUSTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    set = true;
+// Few rows: one CTA per (row, KV head, split), the splits of a (row, KV head) in one cluster.
+template <int D>
+__global__ void __launch_bounds__(128) k_attn_decode_cluster(AttnDecodeParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ AttnShared sh;
+  if (threadIdx.x == 0 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
+  attn_item<D, true>(p, blockIdx.x, blockIdx.y, blockIdx.z, smem, sh);
+}
+
+// Many rows: one CTA per (row, KV head, split) slot of the capture-frozen grid; slots past a row's length
+// exit at once, and partials merge through the global workspace.
+template <int D>
+__global__ void __launch_bounds__(128) k_attn_decode_global(AttnDecodeParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ AttnShared sh;
+  if (threadIdx.x == 0 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
+  attn_item<D, false>(p, blockIdx.x, blockIdx.y, blockIdx.z, smem, sh);
+}
+
+template <typename K>
+static cudaError_t launch_kernel(K kernel, cudaLaunchConfig_t& cfg, const AttnDecodeParams& p, bool* set) {
+  if (!*set) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    *set = true;
   }
-  return cudaLaunchKernelEx(&cfg, k_attn_decode<D, CLUSTER>, p);
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, cudaStream_t s) {
   if (p.rows <= 0) return cudaSuccess;
   if (p.max_splits < 1 || p.max_splits > kMaxSplits || p.Hq / p.Hkv > 8) return cudaErrorInvalidValue;
+  if (p.d != 64 && p.d != 128) return cudaErrorInvalidValue;
   // a few rows: merge on chip (a cluster per row and KV head); many rows: the global workspace, so that
   // splits past a short row's length leave their SM at once
   const bool cluster = p.rows <= 4 && p.max_splits <= kClusterSplits;
@@ -381,9 +428,12 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, c
   attr[1].val.clusterDim.z = p.max_splits;
   cfg.attrs = attr;
   cfg.numAttrs = cluster && p.max_splits > 1 ? 2 : 1;
-  if (p.d == 128) return cluster ? launch_mode<128, true>(p, cfg) : launch_mode<128, false>(p, cfg);
-  if (p.d == 64) return cluster ? launch_mode<64, true>(p, cfg) : launch_mode<64, false>(p, cfg);
-  return cudaErrorInvalidValue;
+  static bool c128 = false, c64 = false, g128 = false, g64 = false;
+  if (cluster)
+    return p.d == 128 ? launch_kernel(k_attn_decode_cluster<128>, cfg, p, &c128)
+                      : launch_kernel(k_attn_decode_cluster<64>, cfg, p, &c64);
+  return p.d == 128 ? launch_kernel(k_attn_decode_global<128>, cfg, p, &g128)
+                    : launch_kernel(k_attn_decode_global<64>, cfg, p, &g64);
 }
 
 }  // namespace grd
