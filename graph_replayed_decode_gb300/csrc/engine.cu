@@ -47,6 +47,13 @@ struct Layer {
   bf16* down = nullptr;       // packed [H][I]
   float* in_norm = nullptr;   // [H]
   float* post_norm = nullptr; // [H]
+  // tensor-core path (steps of kTcTokens tokens or more): row-major copies (gate|up rows interleaved as in
+  // the packed copy) and their tensor maps; null when the projection's shape does not allow it
+  bf16* qkv_rm = nullptr;
+  bf16* o_rm = nullptr;
+  bf16* gu_rm = nullptr;
+  bf16* down_rm = nullptr;
+  CUtensorMap m_qkv{}, m_o{}, m_gu{}, m_down{};
 };
 
 // Word offsets of the step inputs inside one staging slot (host) and the device input region.
@@ -63,8 +70,10 @@ struct GemmPlan {
 struct GemmSite {
   int N = 0, K = 0, rg_fixed = 0;
   GemmPlan plan[2];
+  bool tc = false;  // the tensor-core path serves steps of kTcTokens tokens or more
+  bool use_tc(int T) const { return tc && T >= kTcTokens; }
   const GemmPlan& for_tokens(int T) const { return plan[T >= kLargePlanTokens ? 1 : 0]; }
-  int groups(int T) const { return N / 16 / for_tokens(T).RG; }
+  int groups(int T) const { return use_tc(T) ? N / 128 : N / 16 / for_tokens(T).RG; }
   int max_groups() const { return std::max(N / 16 / plan[0].RG, N / 16 / plan[1].RG); }
 };
 
@@ -119,6 +128,7 @@ struct eng {
   int* done_counter = nullptr;
   int* status = nullptr;
   GemmSite g_qkv, g_o, g_gu, g_down, g_lm;
+  CUtensorMap m_xn_h{}, m_xn_l{}, m_attn_h{}, m_attn_l{}, m_act_h{}, m_act_l{};  // activation planes (TC path)
   int split_blocks = 4, max_splits = 1;
   float* attn_ws = nullptr;    // decode attention partials of multi-split rows
   int* attn_counters = nullptr;
@@ -243,6 +253,27 @@ static int load_f32(eng_t* e, const eng_tensor_t* t, float* dst, int64_t numel, 
   return ENG_OK;
 }
 
+// For a projection on the tensor-core path: keep a row-major copy of the fused matrix in `src` ([N][K];
+// with interleave_half > 0 the rows [A; B] are reordered as A rows 8i..8i+7 then B rows 8i..8i+7 per
+// 16-row group, like the packed copy) and encode its tensor map.  A map the driver refuses turns the
+// tensor-core path off for that projection.
+static int keep_row_major(eng_t* e, GemmSite& site, const bf16* src, bf16** dst, CUtensorMap* map, int N, int K,
+                          int interleave_half) {
+  if (!site.tc) return ENG_OK;
+  TRY(dev_alloc(e, dst, (size_t)N * K));
+  if (interleave_half > 0) {
+    const size_t row = (size_t)K * 2;
+    CUDA_OR_FAIL(e, cudaMemcpy2DAsync(*dst, 16 * row, src, 8 * row, 8 * row, interleave_half / 8,
+                                      cudaMemcpyDeviceToDevice, e->stream));
+    CUDA_OR_FAIL(e, cudaMemcpy2DAsync(*dst + (size_t)8 * K, 16 * row, src + (size_t)interleave_half * K, 8 * row,
+                                      8 * row, interleave_half / 8, cudaMemcpyDeviceToDevice, e->stream));
+  } else {
+    CUDA_OR_FAIL(e, cudaMemcpyAsync(*dst, src, (size_t)N * K * 2, cudaMemcpyDeviceToDevice, e->stream));
+  }
+  if (!make_tc_map(map, *dst, N, K, 128)) site.tc = false;
+  return ENG_OK;
+}
+
 static int load_weights(eng_t* e, const eng_tensor_t* w, int32_t n) {
   const eng_config_t& c = e->c;
   WeightMap wm;
@@ -301,6 +332,7 @@ static int load_weights(eng_t* e, const eng_tensor_t* w, int32_t n) {
     LW(copy_bf16(e, wm.get(nm("self_attn.v_proj.weight")), tmp + (size_t)(Hq + Hkv) * d * H, (int64_t)Hkv * d * H,
                  nm("self_attn.v_proj.weight").c_str()));
     if (launch_pack(tmp, L.qkv, QKV, H, 0, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+    LW(keep_row_major(e, e->g_qkv, tmp, &L.qkv_rm, &L.m_qkv, QKV, H, 0));
     if (c.qkv_bias) {
       LW(dev_alloc(e, &L.qkv_bias, QKV));
       cudaStreamSynchronize(e->stream);
@@ -324,16 +356,19 @@ static int load_weights(eng_t* e, const eng_tensor_t* w, int32_t n) {
     LW(dev_alloc(e, &L.o, (size_t)H * Hq * d));
     LW(copy_bf16(e, wm.get(nm("self_attn.o_proj.weight")), tmp, (int64_t)H * Hq * d, nm("self_attn.o_proj.weight").c_str()));
     if (launch_pack(tmp, L.o, H, Hq * d, 0, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+    LW(keep_row_major(e, e->g_o, tmp, &L.o_rm, &L.m_o, H, Hq * d, 0));
     cudaStreamSynchronize(e->stream);
     // fused gate|up, interleaved per 16-row tile for the SiLU epilogue
     LW(dev_alloc(e, &L.gu, (size_t)2 * I * H));
     LW(copy_bf16(e, wm.get(nm("mlp.gate_proj.weight")), tmp, (int64_t)I * H, nm("mlp.gate_proj.weight").c_str()));
     LW(copy_bf16(e, wm.get(nm("mlp.up_proj.weight")), tmp + (size_t)I * H, (int64_t)I * H, nm("mlp.up_proj.weight").c_str()));
     if (launch_pack(tmp, L.gu, 2 * I, H, I, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+    LW(keep_row_major(e, e->g_gu, tmp, &L.gu_rm, &L.m_gu, 2 * I, H, I));
     cudaStreamSynchronize(e->stream);
     LW(dev_alloc(e, &L.down, (size_t)H * I));
     LW(copy_bf16(e, wm.get(nm("mlp.down_proj.weight")), tmp, (int64_t)H * I, nm("mlp.down_proj.weight").c_str()));
     if (launch_pack(tmp, L.down, H, I, 0, e->stream) != cudaSuccess) return done(fail(e, ENG_ECUDA, "pack launch"));
+    LW(keep_row_major(e, e->g_down, tmp, &L.down_rm, &L.m_down, H, I, 0));
     LW(dev_alloc(e, &L.in_norm, H));
     LW(dev_alloc(e, &L.post_norm, H));
     cudaStreamSynchronize(e->stream);
@@ -419,6 +454,7 @@ static int setup_buffers(eng_t* e) {
     s.N = N;
     s.K = K;
     s.rg_fixed = rg_fixed;
+    s.tc = N % 128 == 0 && K % 64 == 0 && (rg_fixed == 0 || 128 % (16 * rg_fixed) == 0);
     gemm_plan(N, K, rg_fixed, &s.plan[0].RG, &s.plan[0].S, &s.plan[0].ktn);
     gemm_plan_large(N, K, rg_fixed, &s.plan[1].RG, &s.plan[1].S, &s.plan[1].ktn);
     return ENG_OK;
@@ -428,6 +464,14 @@ static int setup_buffers(eng_t* e) {
   TRY(site(e->g_gu, 2 * c.intermediate, H, 0, Tm));
   TRY(site(e->g_down, H, c.intermediate, 0, Tm));
   TRY(site(e->g_lm, c.vocab, H, 0, Rm));
+  e->g_lm.tc = false;  // the LM head gathers its rows and samples: warp-MMA path only
+  // tensor maps of the activation planes (64-token boxes); without them no projection takes the TC path
+  const bool maps_ok = make_tc_map(&e->m_xn_h, e->xn_h, Tm, H, 64) && make_tc_map(&e->m_xn_l, e->xn_l, Tm, H, 64) &&
+                       make_tc_map(&e->m_attn_h, e->attn_h, Tm, c.q_heads * d, 64) &&
+                       make_tc_map(&e->m_attn_l, e->attn_l, Tm, c.q_heads * d, 64) &&
+                       make_tc_map(&e->m_act_h, e->act_h, Tm, c.intermediate, 64) &&
+                       make_tc_map(&e->m_act_l, e->act_l, Tm, c.intermediate, 64);
+  if (!maps_ok) e->g_qkv.tc = e->g_o.tc = e->g_gu.tc = e->g_down.tc = false;
   e->sq_stride = std::max(e->g_o.max_groups(), e->g_down.max_groups());
   TRY(dev_alloc(e, &e->sq, (size_t)Tm * e->sq_stride));
 
@@ -496,6 +540,11 @@ static GemmParams gemm_params(eng_t* e, const GemmSite& s, const bf16* W, int T)
   p.RG = pl.RG;
   p.S = pl.S;
   p.kt_per_split = pl.ktn;
+  if (s.use_tc(T)) {  // tensor-core path: 128-row tiles, no K split
+    p.RG = 8;
+    p.S = 1;
+    p.kt_per_split = s.K / 32;
+  }
   p.ldo = s.N;
   p.eps = e->c.rms_eps;
   p.sq_stride = e->sq_stride;
@@ -511,13 +560,22 @@ static GemmParams gemm_params(eng_t* e, const GemmSite& s, const bf16* W, int T)
   return p;
 }
 
+// w, xh, xl: the tensor maps the tensor-core path would use (ignored when the step is too small for it).
 static cudaError_t gemm_launch(eng_t* e, const GemmParams& p, const GemmSite& s, int epi, bool norm_in, int kind,
-                               cudaStream_t st) {
+                               cudaStream_t st, const CUtensorMap* w = nullptr, const CUtensorMap* xh = nullptr,
+                               const CUtensorMap* xl = nullptr) {
   LaunchOpts o;
   o.pdl = e->pdl;
   e->launches++;
   prof_begin(e, st, kind, gemm_bytes(s, p.T, epi, norm_in));
-  const cudaError_t r = launch_gemm(p, epi, norm_in, o, st);
+  TcMaps tm;
+  const bool tc = s.use_tc(p.T) && w;
+  if (tc) {
+    tm.w = *w;
+    tm.xh = *xh;
+    tm.xl = *xl;
+  }
+  const cudaError_t r = launch_gemm(p, epi, norm_in, o, st, tc ? &tm : nullptr);
   prof_end(e, st);
   return r;
 }
@@ -589,7 +647,9 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     q.d = d;
     q.NB = c.num_blocks;
     set_prefetch(e, q.pf_ptr, q.pf_bytes, L.o, e->g_o);
-    if ((r = gemm_launch(e, q, e->g_qkv, EPI_QKV_ROPE, true, ENG_K_GEMM_QKV, st)) != cudaSuccess) return r;
+    if ((r = gemm_launch(e, q, e->g_qkv, EPI_QKV_ROPE, true, ENG_K_GEMM_QKV, st, &L.m_qkv, &e->m_xn_h, &e->m_xn_l)) !=
+        cudaSuccess)
+      return r;
 
     // ---- attention, split by kind inside the step
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)d);
@@ -658,7 +718,9 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     po.xh_out = e->xn_h;
     po.xl_out = e->xn_l;
     set_prefetch(e, po.pf_ptr, po.pf_bytes, L.down, e->g_down);
-    if ((r = gemm_launch(e, po, e->g_o, EPI_RESID, false, ENG_K_GEMM_O, st)) != cudaSuccess) return r;
+    if ((r = gemm_launch(e, po, e->g_o, EPI_RESID, false, ENG_K_GEMM_O, st, &L.m_o, &e->m_attn_h, &e->m_attn_l)) !=
+        cudaSuccess)
+      return r;
     sq_parts = e->g_o.groups(T);
 
     // ---- post-attention RMSNorm + fused gate|up projection + SiLU * up
@@ -670,7 +732,9 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     pg.xh_out = e->act_h;
     pg.xl_out = e->act_l;
     if (l + 1 < c.layers) set_prefetch(e, pg.pf_ptr, pg.pf_bytes, e->layers[l + 1].qkv, e->g_qkv);
-    if ((r = gemm_launch(e, pg, e->g_gu, EPI_SILU, true, ENG_K_GEMM_GATE_UP, st)) != cudaSuccess) return r;
+    if ((r = gemm_launch(e, pg, e->g_gu, EPI_SILU, true, ENG_K_GEMM_GATE_UP, st, &L.m_gu, &e->m_xn_h, &e->m_xn_l)) !=
+        cudaSuccess)
+      return r;
 
     // ---- down projection + residual
     GemmParams pd = gemm_params(e, e->g_down, L.down, T);
@@ -681,7 +745,9 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     pd.next_norm_w = l + 1 < c.layers ? e->layers[l + 1].in_norm : e->final_norm;
     pd.xh_out = e->xn_h;
     pd.xl_out = e->xn_l;
-    if ((r = gemm_launch(e, pd, e->g_down, EPI_RESID, false, ENG_K_GEMM_DOWN, st)) != cudaSuccess) return r;
+    if ((r = gemm_launch(e, pd, e->g_down, EPI_RESID, false, ENG_K_GEMM_DOWN, st, &L.m_down, &e->m_act_h,
+                         &e->m_act_l)) != cudaSuccess)
+      return r;
     sq_parts = e->g_down.groups(T);
   }
 

@@ -127,8 +127,23 @@ ENG_DEVICE void stage8(bf16* xs, bf16* xl, int idx, const float4 a, const float4
   *reinterpret_cast<uint4*>(xl + idx) = l;
 }
 
-template <int NT, int EPI, bool NORM_IN>
-__global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
+// Tensor-core path (TC): 64-token chunks against 128-row weight tiles, k-blocks of 64 through a ring of
+// kTcStages shared-memory stages (weight tile, hi tile, lo tile per stage, TMA tensor copies with 128-byte
+// swizzle); one thread issues two tcgen05 MMAs per 16 k (hi plane, lo plane) into a 128 x 64 fp32 TMEM
+// accumulator; the accumulator is read back into the same [rows][tokens] tile the epilogues use.
+static constexpr int kTcStages = 5;
+static constexpr uint32_t kTcA = 128 * 128;           // 128 weight rows x 64 bf16
+static constexpr uint32_t kTcB = 64 * 128;            // 64 tokens x 64 bf16, one plane
+static constexpr uint32_t kTcStage = kTcA + 2 * kTcB;
+static constexpr size_t kTcCsBytes = (size_t)64 * 128 * 4;  // QKV: the RoPE rows of the chunk's 64 tokens
+static constexpr size_t kTcSmem = (size_t)kTcStages * kTcStage + kTcCsBytes + 1024;  // + room to align to 1 KB
+
+ENG_DEVICE uint8_t* tc_ring(uint8_t* smem) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+template <int NT, int EPI, bool NORM_IN, bool TC>
+ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
   constexpr int kPre = NT <= 2 ? kPreMax / 2 : (NT == 4 ? kPreMax / 4 : kPreMax / 8);
   constexpr int kUnroll = NT >= 8 ? 2 : 4;  // weight k-tiles loaded per group (register budget)
   extern __shared__ __align__(16) uint8_t smem[];
@@ -140,6 +155,8 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
   __shared__ float s_qn[128], s_kn[128];   //          the QK-norm weights
   __shared__ float s_row[128];  // per output row of this CTA: bias (QKV, STORE) or next norm weight (RESID)
   __shared__ __align__(8) uint64_t s_wbar, s_xbar;
+  __shared__ __align__(8) uint64_t s_full[TC ? kTcStages : 1], s_empty[TC ? kTcStages : 1], s_done;
+  __shared__ uint32_t s_tmem;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rgi = blockIdx.x, split = blockIdx.y, chunk = blockIdx.z;
   const int S = p.S;
@@ -164,7 +181,23 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
   const uint4* wp = reinterpret_cast<const uint4*>(p.W) + ((size_t)row_tile * KT + kt0) * 64 + lane;
   const int pn0 = min(sm.piece, ktn);
   uint4 pre[kPre][2];
-  if (threadIdx.x == 0) {
+  const int nk = p.K >> 6;  // TC: k-blocks of 64
+  if constexpr (TC) {
+    // tensor memory for the accumulator, the stage barriers, and the weight tiles of the first stages
+    if (warp == 0) tmem_alloc<64>(&s_tmem);
+    if (threadIdx.x == 0) {
+      for (int st = 0; st < kTcStages; ++st) {
+        mbar_init(&s_full[st], 1);
+        mbar_init(&s_empty[st], 1);
+      }
+      mbar_init(&s_done, 1);
+      uint8_t* ring = tc_ring(smem);
+      for (int kb = 0; kb < min(kTcStages, nk); ++kb) {
+        mbar_expect_tx(&s_full[kb], kTcStage);
+        tma_tile_2d(ring + (size_t)kb * kTcStage, &tm->w, kb * 64, row0, &s_full[kb]);
+      }
+    }
+  } else if (threadIdx.x == 0) {
     mbar_init(&s_xbar, 1);
     if (sm.tma) {  // the CTA's whole slice (RG row tiles x ktn k-tiles, contiguous per row tile)
       mbar_init(&s_wbar, 1);
@@ -174,7 +207,7 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
                     (uint32_t)ktn * 1024u, &s_wbar);
     }
   }
-  if (!sm.tma) {
+  if (!TC && !sm.tma) {
 #pragma unroll
     for (int u = 0; u < kPre; ++u) {
       const int kt = kg + u * KG;
@@ -190,7 +223,7 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
   }
   if (threadIdx.x == 32 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
   // padding token rows of both planes are zero (the copies below fill rows < ntok only)
-  {
+  if constexpr (!TC) {
     const int pad = (NT * 8 - ntok) * xstride / 8;  // 16-byte chunks per plane
     uint4* zh = reinterpret_cast<uint4*>(xs + (size_t)ntok * xstride);
     uint4* zl = reinterpret_cast<uint4*>(xl + (size_t)ntok * xstride);
@@ -221,9 +254,19 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       s_pos[threadIdx.x] = (pos < 0 || pos >= p.max_pos) ? 0 : pos;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < min(nown, kCsTokens) * p.d; i += 256) {
-      const int k = i / p.d, j = i - k * p.d;
-      s_cs[k][j] = p.cos_sin[(size_t)s_pos[k] * p.d + j];
+    if constexpr (TC) {  // every owned token's RoPE row, copied asynchronously (landed before the epilogue)
+      float* cs_tab = reinterpret_cast<float*>(tc_ring(smem) + (size_t)kTcStages * kTcStage);
+      const int q4 = p.d / 4;
+      for (int i = threadIdx.x; i < nown * q4; i += 256) {
+        const int k = i / q4, c = i - k * q4;
+        cp_async16(cs_tab + (size_t)k * p.d + c * 4, p.cos_sin + (size_t)s_pos[k] * p.d + c * 4);
+      }
+      cp_async_commit();
+    } else {
+      for (int i = threadIdx.x; i < min(nown, kCsTokens) * p.d; i += 256) {
+        const int k = i / p.d, j = i - k * p.d;
+        s_cs[k][j] = p.cos_sin[(size_t)s_pos[k] * p.d + j];
+      }
     }
     if (threadIdx.x < p.d) {
       s_qn[threadIdx.x] = p.q_norm ? p.q_norm[threadIdx.x] : 1.f;
@@ -234,7 +277,9 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
     const float* rv = EPI == EPI_RESID ? p.next_norm_w : p.bias;
     s_row[threadIdx.x] = rv ? rv[row0 + threadIdx.x] : (EPI == EPI_RESID ? 1.f : 0.f);
   }
-  __syncthreads();        // barriers initialised, padding rows zeroed
+  if constexpr (TC) tc_fence_before();
+  __syncthreads();        // barriers initialised, padding rows zeroed (TC: tensor memory allocated)
+  if constexpr (TC) tc_fence_after();
   if (S > 1) cluster.sync();  // every CTA of the cluster has started before any pushes into its memory
   pdl_trigger();
   pdl_wait();
@@ -252,14 +297,25 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       }
     }
   };
-  issue_x(0, pn0);
+  if constexpr (TC) {
+    if (threadIdx.x == 0) {  // the activation tiles of the first stages
+      uint8_t* ring = tc_ring(smem);
+      for (int kb = 0; kb < min(kTcStages, nk); ++kb) {
+        tma_tile_2d(ring + (size_t)kb * kTcStage + kTcA, &tm->xh, kb * 64, n0, &s_full[kb]);
+        tma_tile_2d(ring + (size_t)kb * kTcStage + kTcA + kTcB, &tm->xl, kb * 64, n0, &s_full[kb]);
+      }
+    }
+  } else {
+    issue_x(0, pn0);
+  }
 
   // EPI_RESID: the residual values this thread updates in the epilogue (warps over its first two owned
   // tokens, lanes over up to four rows each), fetched now so the epilogue needs no further round trip
-  float h_old[2][4];
+  constexpr int kOldTok = TC ? 8 : 2;  // owned tokens per warp whose residual values are fetched here
+  float h_old[kOldTok][4];
   if (EPI == EPI_RESID) {
 #pragma unroll
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kOldTok; ++a) {
       const int k = warp + 8 * a;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
@@ -268,144 +324,226 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       }
     }
   }
-  if (NORM_IN) {  // 1 / rms of each staged token, from its producer's partial sums of squares
-    for (int r = warp; r < ntok; r += 8) {
-      const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
-      const float* part = p.sq_in + (size_t)src * p.sq_stride;
+  if (NORM_IN) {  // 1 / rms of each staged token, from its producer's partial sums of squares (a warp per
+                  // token; every load of the warp's tokens issued before the first reduction)
+    float part_ss[NT];
+#pragma unroll
+    for (int a = 0; a < NT; ++a) {
+      const int r = warp + 8 * a;
       float ss = 0.f;
-      for (int j = lane; j < p.sq_parts; j += 32) ss += part[j];
-      ss = warp_sum(ss);
-      if (lane == 0) s_rstd[r] = rsqrtf(ss / (float)p.K + p.eps);
+      if (r < ntok) {
+        const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
+        const float* part = p.sq_in + (size_t)src * p.sq_stride;
+        for (int j = lane; j < p.sq_parts; j += 32) ss += part[j];
+      }
+      part_ss[a] = ss;
     }
-  }
-
-  float acc[NT][4], accl[NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    accl[nt][0] = accl[nt][1] = accl[nt][2] = accl[nt][3] = 0.f;
+    for (int a = 0; a < NT; ++a) {
+      const int r = warp + 8 * a;
+      const float ss = warp_sum(part_ss[a]);
+      if (lane == 0 && r < ntok) s_rstd[r] = rsqrtf(ss / (float)p.K + p.eps);
+    }
   }
 
-  const uint4* ws = reinterpret_cast<const uint4*>(smem) + (size_t)rt * ktn * 64 + lane;  // tma: this warp's row tile
-  if (sm.tma && !mbar_wait(&s_wbar, 0, 1u << 26)) {
-    set_status(p.status, ST_TIMEOUT);
-    mbar_wait(&s_wbar, 0, 1u << 26);  // never leave while the copy may still write shared memory
-  }
-  int piece_no = 0;
-  for (int pc = 0; pc < ktn; pc += sm.piece, ++piece_no) {
-    const int pn = min(sm.piece, ktn - pc);
-    if (pc > 0) {  // every warp is done with the previous piece before its rows are overwritten
-      __syncthreads();
-      if (warp == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue_x(pc, pn);
+  float* ts;
+  constexpr int TS = NT * 8 + 1;  // token stride (padded)
+  if constexpr (!TC) {
+    float acc[NT][4], accl[NT][4];
+  #pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      accl[nt][0] = accl[nt][1] = accl[nt][2] = accl[nt][3] = 0.f;
     }
-    if (!mbar_wait(&s_xbar, piece_no & 1, 1u << 26)) {
+
+    const uint4* ws = reinterpret_cast<const uint4*>(smem) + (size_t)rt * ktn * 64 + lane;  // tma: this warp's row tile
+    if (sm.tma && !mbar_wait(&s_wbar, 0, 1u << 26)) {
       set_status(p.status, ST_TIMEOUT);
-      mbar_wait(&s_xbar, piece_no & 1, 1u << 26);
+      mbar_wait(&s_wbar, 0, 1u << 26);  // never leave while the copy may still write shared memory
     }
+    int piece_no = 0;
+    for (int pc = 0; pc < ktn; pc += sm.piece, ++piece_no) {
+      const int pn = min(sm.piece, ktn - pc);
+      if (pc > 0) {  // every warp is done with the previous piece before its rows are overwritten
+        __syncthreads();
+        if (warp == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_x(pc, pn);
+      }
+      if (!mbar_wait(&s_xbar, piece_no & 1, 1u << 26)) {
+        set_status(p.status, ST_TIMEOUT);
+        mbar_wait(&s_xbar, piece_no & 1, 1u << 26);
+      }
 
-    if (sm.tma) {
-      constexpr int UT = kUnroll;
-      for (int base = kg; base < pn; base += KG * UT) {
-        uint4 a[UT][2];
-#pragma unroll
-        for (int u = 0; u < UT; ++u) {
-          const int kt = base + u * KG;
-          if (kt < pn) {
-            a[u][0] = ws[(size_t)(pc + kt) * 64];
-            a[u][1] = ws[(size_t)(pc + kt) * 64 + 32];
+      if (sm.tma) {
+        constexpr int UT = kUnroll;
+        for (int base = kg; base < pn; base += KG * UT) {
+          uint4 a[UT][2];
+  #pragma unroll
+          for (int u = 0; u < UT; ++u) {
+            const int kt = base + u * KG;
+            if (kt < pn) {
+              a[u][0] = ws[(size_t)(pc + kt) * 64];
+              a[u][1] = ws[(size_t)(pc + kt) * 64 + 32];
+            }
+          }
+  #pragma unroll
+          for (int u = 0; u < UT; ++u) {
+            const int kt = base + u * KG;
+            if (kt < pn) mma_tile<NT>(acc, accl, a[u][0], a[u][1], xs, xl, xstride, kt, lane);
           }
         }
-#pragma unroll
-        for (int u = 0; u < UT; ++u) {
+        continue;
+      }
+      int first = kg;
+      if (pc == 0) {  // the fragments loaded before waiting
+  #pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+          const int kt = kg + u * KG;
+          if (kt < pn) mma_tile<NT>(acc, accl, pre[u][0], pre[u][1], xs, xl, xstride, kt, lane);
+        }
+        first = kg + kPre * KG;
+      }
+      constexpr int U = kUnroll;
+      for (int base = first; base < pn; base += KG * U) {
+        uint4 a[U][2];
+  #pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int kt = base + u * KG;
+          if (kt < pn) {
+            a[u][0] = ld_stream16(wp + (size_t)(pc + kt) * 64);
+            a[u][1] = ld_stream16(wp + (size_t)(pc + kt) * 64 + 32);
+          } else {
+            a[u][0] = a[u][1] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+  #pragma unroll
+        for (int u = 0; u < U; ++u) {
           const int kt = base + u * KG;
           if (kt < pn) mma_tile<NT>(acc, accl, a[u][0], a[u][1], xs, xl, xstride, kt, lane);
         }
       }
-      continue;
     }
-    int first = kg;
-    if (pc == 0) {  // the fragments loaded before waiting
-#pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        const int kt = kg + u * KG;
-        if (kt < pn) mma_tile<NT>(acc, accl, pre[u][0], pre[u][1], xs, xl, xstride, kt, lane);
-      }
-      first = kg + kPre * KG;
-    }
-    constexpr int U = kUnroll;
-    for (int base = first; base < pn; base += KG * U) {
-      uint4 a[U][2];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int kt = base + u * KG;
-        if (kt < pn) {
-          a[u][0] = ld_stream16(wp + (size_t)(pc + kt) * 64);
-          a[u][1] = ld_stream16(wp + (size_t)(pc + kt) * 64 + 32);
-        } else {
-          a[u][0] = a[u][1] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int kt = base + u * KG;
-        if (kt < pn) mma_tile<NT>(acc, accl, a[u][0], a[u][1], xs, xl, xstride, kt, lane);
-      }
-    }
-  }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[nt][j] += accl[nt][j];
+  #pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+      for (int j = 0; j < 4; ++j) acc[nt][j] += accl[nt][j];
 
-  // ---- this CTA's tile: sum the KG warps of each row tile in warp order
-  __syncthreads();
-  float4* red = reinterpret_cast<float4*>(area);
-  float* ts = reinterpret_cast<float*>(area + sm.red_bytes);
-  constexpr int TS = NT * 8 + 1;  // token stride (padded)
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-    red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-  __syncthreads();
-  for (int i = threadIdx.x; i < RG * NT * 32; i += 256) {
-    const int ln = i & 31, nt = (i >> 5) % NT, r_t = (i >> 5) / NT;
-    float4 v = red[((0 * RG + r_t) * NT + nt) * 32 + ln];
-    for (int j = 1; j < KG; ++j) {
-      const float4 w = red[((j * RG + r_t) * NT + nt) * 32 + ln];
-      v.x += w.x;
-      v.y += w.y;
-      v.z += w.z;
-      v.w += w.w;
-    }
-    const int r0 = r_t * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
-    ts[r0 * TS + c0] = v.x;
-    ts[r0 * TS + c0 + 1] = v.y;
-    ts[(r0 + 8) * TS + c0] = v.z;
-    ts[(r0 + 8) * TS + c0 + 1] = v.w;
-  }
-  __syncthreads();
-
-  // ---- split-K across the cluster: CTA `split` finishes tokens split, split + S, ... (sum in split order)
-  if (S > 1) {
-    // push this CTA's columns of the tokens CTA q finishes into q's receive buffer, then every CTA adds
-    // its received columns in split order (its own columns at its own position)
-    const int kmax = (NT * 8 + S - 1) / S;
-    float* recv = reinterpret_cast<float*>(area + sm.recv_off);  // [S][rows][kmax]
-    for (int i = threadIdx.x; i < rows * ntok; i += 256) {
-      const int tok = i / rows, r = i - tok * rows;
-      const int q = tok % S;
-      if (q == split) continue;
-      cluster.map_shared_rank(recv, q)[((size_t)split * rows + r) * kmax + tok / S] = ts[r * TS + tok];
-    }
-    cluster.sync();
-    for (int i = threadIdx.x; i < rows * nown; i += 256) {
-      const int k = i / rows, r = i - k * rows;
-      const int tok = tok_first + k * tok_step;
-      float v = 0.f;
-      for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kmax + k];
-      ts[r * TS + tok] = v;
+    // ---- this CTA's tile: sum the KG warps of each row tile in warp order
+    __syncthreads();
+    float4* red = reinterpret_cast<float4*>(area);
+    ts = reinterpret_cast<float*>(area + sm.red_bytes);
+  #pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+    __syncthreads();
+    for (int i = threadIdx.x; i < RG * NT * 32; i += 256) {
+      const int ln = i & 31, nt = (i >> 5) % NT, r_t = (i >> 5) / NT;
+      float4 v = red[((0 * RG + r_t) * NT + nt) * 32 + ln];
+      for (int j = 1; j < KG; ++j) {
+        const float4 w = red[((j * RG + r_t) * NT + nt) * 32 + ln];
+        v.x += w.x;
+        v.y += w.y;
+        v.z += w.z;
+        v.w += w.w;
+      }
+      const int r0 = r_t * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
+      ts[r0 * TS + c0] = v.x;
+      ts[r0 * TS + c0 + 1] = v.y;
+      ts[(r0 + 8) * TS + c0] = v.z;
+      ts[(r0 + 8) * TS + c0 + 1] = v.w;
     }
     __syncthreads();
+
+    // ---- split-K across the cluster: CTA `split` finishes tokens split, split + S, ... (sum in split order)
+    if (S > 1) {
+      // push this CTA's columns of the tokens CTA q finishes into q's receive buffer, then every CTA adds
+      // its received columns in split order (its own columns at its own position)
+      const int kmax = (NT * 8 + S - 1) / S;
+      float* recv = reinterpret_cast<float*>(area + sm.recv_off);  // [S][rows][kmax]
+      for (int i = threadIdx.x; i < rows * ntok; i += 256) {
+        const int tok = i / rows, r = i - tok * rows;
+        const int q = tok % S;
+        if (q == split) continue;
+        cluster.map_shared_rank(recv, q)[((size_t)split * rows + r) * kmax + tok / S] = ts[r * TS + tok];
+      }
+      cluster.sync();
+      for (int i = threadIdx.x; i < rows * nown; i += 256) {
+        const int k = i / rows, r = i - k * rows;
+        const int tok = tok_first + k * tok_step;
+        float v = 0.f;
+        for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kmax + k];
+        ts[r * TS + tok] = v;
+      }
+      __syncthreads();
+    }
+  } else {
+    // ---- tensor-core path: one thread issues every k-block's MMAs as its stage lands and refills the stage
+    // the previous k-block used once those MMAs are done
+    uint8_t* ring = tc_ring(smem);
+    // lane 0 of warp 0 issues; the rest of warp 0 waits at the warp barrier below, not on an mbarrier, so
+    // the issuing lane never shares its warp with lanes that spin
+    if (warp == 0 && lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(128, 64);
+      int issued = min(kTcStages, nk);  // k-blocks whose copies were issued
+      int kb = 0;
+      for (; kb < nk; ++kb) {
+        const int st = kb % kTcStages;
+        uint8_t* stage = ring + (size_t)st * kTcStage;
+        if (!mbar_wait(&s_full[st], (kb / kTcStages) & 1, 1u << 26)) {
+          set_status(p.status, ST_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(stage), bh = umma_desc_sw128(stage + kTcA),
+                       bl = umma_desc_sw128(stage + kTcA + kTcB);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          umma_bf16(s_tmem, ad + 2 * k, bh + 2 * k, idesc, (kb | k) != 0);
+          umma_bf16(s_tmem, ad + 2 * k, bl + 2 * k, idesc, 1u);
+        }
+        umma_commit(&s_empty[st]);
+        const int pk = kb - 1, nkb = pk + kTcStages;
+        if (pk >= 0 && nkb < nk) {
+          const int ps = pk % kTcStages;
+          if (!mbar_wait(&s_empty[ps], (pk / kTcStages) & 1, 1u << 26)) {
+            set_status(p.status, ST_TIMEOUT);
+            ++kb;
+            break;
+          }
+          uint8_t* pst = ring + (size_t)ps * kTcStage;
+          mbar_expect_tx(&s_full[ps], kTcStage);
+          tma_tile_2d(pst, &tm->w, nkb * 64, row0, &s_full[ps]);
+          tma_tile_2d(pst + kTcA, &tm->xh, nkb * 64, n0, &s_full[ps]);
+          tma_tile_2d(pst + kTcA + kTcB, &tm->xl, nkb * 64, n0, &s_full[ps]);
+          issued = nkb + 1;
+        }
+      }
+      // after a timeout, copies still in flight land before the ring is reused or the CTA exits
+      for (int q = kb; q < issued; ++q) mbar_wait(&s_full[q % kTcStages], (q / kTcStages) & 1, 1u << 26);
+      umma_commit(&s_done);
+    }
+    if (warp == 0) __syncwarp();
+    if (!mbar_wait(&s_done, 0, 1u << 26)) {
+      set_status(p.status, ST_TIMEOUT);
+      mbar_wait(&s_done, 0, 1u << 26);
+    }
+    tc_fence_after();
+    // warp w reads its TMEM lane quarter (rows 32 (w % 4) ..) and column half (tokens 32 (w / 4) ..)
+    ts = reinterpret_cast<float*>(ring);
+    {
+      float v[32];
+      tmem_ld32(s_tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * 32), v);
+      const int r = (warp & 3) * 32 + lane;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) ts[r * TS + (warp >> 2) * 32 + j] = v[j];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_free<64>(s_tmem);
+    if (EPI == EPI_QKV_ROPE) {  // the RoPE rows copied before the wait
+      cp_async_wait<0>();
+      __syncthreads();
+    }
   }
   if (NORM_IN) {  // RMSNorm(h) W^T = (1 / rms(h)) ((h * w) W^T)
     for (int i = threadIdx.x; i < rows * nown; i += 256) {
@@ -431,7 +569,7 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       float ss = 0.f;
       for (int r = lane; r < rows; r += 32) {
         const int a = k >> 3, b = r >> 5;
-        const float old = (a < 2 && b < 4) ? h_old[a & 1][b & 3] : hrow[r];
+        const float old = (a < kOldTok && b < 4) ? h_old[a % kOldTok][b & 3] : hrow[r];
         const float v = old + ts[r * TS + tok];
         hrow[r] = v;
         put_split(p.xh_out, p.xl_out, base + r, v * s_row[r]);
@@ -487,7 +625,8 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
           for (int e = 0; e < E; ++e) x[e] = x[e] * rs * nw[lane * E + e];
         }
         // rotate-half RoPE: element i < D/2 pairs with i + D/2, held by lane ^ 16
-        const float* cs = k < kCsTokens ? s_cs[k] : p.cos_sin + (size_t)s_pos[k] * D;  // [D/2][2]
+        const float* cs = TC ? reinterpret_cast<const float*>(tc_ring(smem) + (size_t)kTcStages * kTcStage) + (size_t)k * D
+                             : (k < kCsTokens ? s_cs[k] : p.cos_sin + (size_t)s_pos[k] * D);  // [D/2][2]
         float y[4];
         for (int e = 0; e < E; ++e) {
           const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
@@ -552,6 +691,18 @@ __global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
       if (threadIdx.x == 0) *p.done_counter = 0;
     }
   }
+}
+
+// Warp-MMA path (decode sizes and the LM head).
+template <int NT, int EPI, bool NORM_IN>
+__global__ void __launch_bounds__(256, 2) k_gemm(GemmParams p) {
+  gemm_body<NT, EPI, NORM_IN, false>(p, nullptr);
+}
+
+// Tensor-core path (steps of kTcTokens tokens or more).
+template <int EPI, bool NORM_IN>
+__global__ void __launch_bounds__(256, 1) k_gemm_tc(GemmParams p, const __grid_constant__ TcMaps tm) {
+  gemm_body<8, EPI, NORM_IN, true>(p, &tm);
 }
 
 // ------------------------------------------------------------------ host side
@@ -640,18 +791,21 @@ void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_sp
   *kt_per_split = KT / best_s;
 }
 
-template <int NT, int EPI, bool NORM_IN>
-static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, dim3 grid) {
-  const GemmSmem sm = gemm_smem(NT, p.RG, p.kt_per_split, p.S);
+template <int NT, int EPI, bool NORM_IN, bool TC>
+static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, dim3 grid, const TcMaps* tm) {
+  const size_t smem_bytes = TC ? kTcSmem : gemm_smem(NT, p.RG, p.kt_per_split, p.S).total;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(k_gemm<NT, EPI, NORM_IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if constexpr (TC)
+      cudaFuncSetAttribute(k_gemm_tc<EPI, NORM_IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    else
+      cudaFuncSetAttribute(k_gemm<NT, EPI, NORM_IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = sm.total;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -662,39 +816,69 @@ static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStrea
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.S > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_gemm<NT, EPI, NORM_IN>, p);
+  if constexpr (TC) return cudaLaunchKernelEx(&cfg, k_gemm_tc<EPI, NORM_IN>, p, *tm);
+  else return cudaLaunchKernelEx(&cfg, k_gemm<NT, EPI, NORM_IN>, p);
 }
 
 static int chunks_of(int T) { return (T + 63) / 64; }
 
 template <int EPI, bool NORM_IN>
-static cudaError_t launch_epi(const GemmParams& p, const LaunchOpts& o, cudaStream_t s) {
+static cudaError_t launch_epi(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, const TcMaps* tc) {
   const int nRG = p.N / 16 / p.RG;
   const dim3 grid(nRG, p.S, chunks_of(p.T));
+  if (tc) {
+    if (EPI == EPI_LMHEAD || p.RG != 8 || p.S != 1 || p.x_rows || p.N % 128 || p.K % 64) return cudaErrorInvalidValue;
+    if constexpr (EPI == EPI_LMHEAD) return cudaErrorInvalidValue;
+    else return launch_nt<8, EPI, NORM_IN, true>(p, o, s, grid, tc);
+  }
   const int ntiles = p.T >= 64 ? 8 : (p.T + 7) / 8;
-  if (ntiles <= 1) return launch_nt<1, EPI, NORM_IN>(p, o, s, grid);
-  if (ntiles <= 2) return launch_nt<2, EPI, NORM_IN>(p, o, s, grid);
-  if (ntiles <= 4) return launch_nt<4, EPI, NORM_IN>(p, o, s, grid);
-  return launch_nt<8, EPI, NORM_IN>(p, o, s, grid);
+  if (ntiles <= 1) return launch_nt<1, EPI, NORM_IN, false>(p, o, s, grid, nullptr);
+  if (ntiles <= 2) return launch_nt<2, EPI, NORM_IN, false>(p, o, s, grid, nullptr);
+  if (ntiles <= 4) return launch_nt<4, EPI, NORM_IN, false>(p, o, s, grid, nullptr);
+  return launch_nt<8, EPI, NORM_IN, false>(p, o, s, grid, nullptr);
 }
 
-cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const LaunchOpts& o, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const LaunchOpts& o, cudaStream_t s,
+                        const TcMaps* tc) {
   if (p.T <= 0) return cudaSuccess;
   if (p.S < 1 || p.S > kMaxCluster) return cudaErrorInvalidValue;
   if (norm_in) {
     switch (epi) {
-      case EPI_QKV_ROPE: return launch_epi<EPI_QKV_ROPE, true>(p, o, s);
-      case EPI_SILU: return launch_epi<EPI_SILU, true>(p, o, s);
-      case EPI_LMHEAD: return launch_epi<EPI_LMHEAD, true>(p, o, s);
-      case EPI_STORE_F32: return launch_epi<EPI_STORE_F32, true>(p, o, s);
+      case EPI_QKV_ROPE: return launch_epi<EPI_QKV_ROPE, true>(p, o, s, tc);
+      case EPI_SILU: return launch_epi<EPI_SILU, true>(p, o, s, tc);
+      case EPI_LMHEAD: return launch_epi<EPI_LMHEAD, true>(p, o, s, nullptr);
+      case EPI_STORE_F32: return launch_epi<EPI_STORE_F32, true>(p, o, s, tc);
     }
   } else {
     switch (epi) {
-      case EPI_RESID: return launch_epi<EPI_RESID, false>(p, o, s);
-      case EPI_STORE_F32: return launch_epi<EPI_STORE_F32, false>(p, o, s);
+      case EPI_RESID: return launch_epi<EPI_RESID, false>(p, o, s, tc);
+      case EPI_STORE_F32: return launch_epi<EPI_STORE_F32, false>(p, o, s, tc);
     }
   }
   return cudaErrorInvalidValue;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool make_tc_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  static EncodeTiledFn enc = nullptr;
+  if (!enc) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    enc = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace grd

@@ -2,6 +2,7 @@
 // Every launcher enqueues on `stream`, returns the launch's cudaError_t and never synchronises.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -95,6 +96,17 @@ struct GemmParams {
   int* out_ids;                 // [T]
   int* status;
 };
+// Tensor maps of the tensor-core (tcgen05) GEMM path: the weight as a row-major [N][K] bf16 matrix in
+// 128 x 64 boxes, and the activation planes [rows][K] in 64 x 64 boxes, all with 128-byte swizzle.
+struct TcMaps {
+  CUtensorMap w, xh, xl;
+};
+// Encodes a 2D bf16 tensor map over a row-major [rows][cols] matrix with boxes of box_rows x 64 columns
+// (128-byte swizzle; rows past the end read as zeros).  False when the driver refuses it.
+bool make_tc_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// Token count from which a projection runs on the tensor-core path (when its shape allows it).
+static constexpr int kTcTokens = 65;
+
 // Picks RG / S / kt_per_split for an [N][K] weight (independent of T, so every token count computes
 // each output with the same summation order).  rg_fixed > 0 forces the rows per CTA (whole heads).
 void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split);
@@ -102,7 +114,10 @@ void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split);
 void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split);
 // Token count from which a step uses the large plans.
 static constexpr int kLargePlanTokens = 9;
-cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const LaunchOpts& o, cudaStream_t s);
+// tc: the tensor maps of the tcgen05 path (then RG must be 8, S 1, no x_rows; N % 128 == 0, K % 64 == 0),
+// or null for the warp-MMA path.
+cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const LaunchOpts& o, cudaStream_t s,
+                        const TcMaps* tc = nullptr);
 
 // ------------------------------------------------------------------ attention (attn_decode.cu, attn_prefill.cu)
 struct AttnDecodeParams {

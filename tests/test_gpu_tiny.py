@@ -315,3 +315,35 @@ def test_attention_merge_modes_agree_bit_for_bit(weights):
         assert g.status() == 0
     finally:
         g.close()
+
+
+def test_tensor_core_prefill_chunks(weights):
+    """A packed prefill step of 127 tokens (two prompts of 70 and 57; two 64-token chunks, the second
+    ragged) runs its projections on the tcgen05 path; logits and slots match the oracle."""
+    from graph_replayed_decode_gb300.eng import StepArrays
+    import torch
+    from harness import device_view
+    g = _engine(weights)
+    try:
+        model = oracle.OracleModel(S, weights)
+        cache = oracle.PagedCache(S, NB)
+        lens = [70, 57]
+        blocks = [list(g.alloc(oracle.blocks_needed(n))) for n in lens]
+        for r, b in enumerate(blocks):
+            cache.set_block_table(r, b)
+        bt = block_table(blocks, MBS)
+        ids = np.concatenate([synth.prompt_ids(n, S.vocab, 40 + r) for r, n in enumerate(lens)])
+        pos = np.concatenate([np.arange(n) for n in lens])
+        cu = np.array([0, 70, 127])
+        temps = np.array([0.0, 0.9], dtype=np.float32)
+        gid, glog = g.step(StepArrays(ids, pos, cu, bt, np.array(lens), temps, seed=2, offset=0))
+        assert g.info().num_prefill == 2
+        olog = oracle.forward_step(model, cache, ids, pos, cu)
+        check_logits_and_ids(glog, gid, olog, temps, 2, 0)
+        sp, _ = g.eng.eng_debug_buffer(g.h, "slots")
+        slots = device_view(sp, 4 * len(ids), torch.int32).cpu().numpy()
+        want = [cache.slot(int(np.searchsorted(cu, t, side="right") - 1), int(pos[t])) for t in range(len(ids))]
+        np.testing.assert_array_equal(slots, want)
+        assert g.status() == 0
+    finally:
+        g.close()
