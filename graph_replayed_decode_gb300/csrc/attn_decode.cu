@@ -30,7 +30,7 @@ namespace cg = cooperative_groups;
 namespace grd {
 
 static constexpr int kStages = 2;    // K/V blocks in flight per warp
-static constexpr int kMaxSplits = 16;   // splits of one (row, KV head)
+static constexpr int kMaxSplits = 8;    // splits of one (row, KV head)
 static constexpr int kClusterSplits = 8;  // at most this many merge on chip (one thread-block cluster)
 
 // Per-warp K/V stages, reused for the warp merge afterwards ([4][16] M, [4][16] L, [4][16][D] O, [G][D+2]).
@@ -44,51 +44,38 @@ __host__ __device__ constexpr size_t attn_stage_bytes(int D) {
 // output projection's operand planes.  get(sp, head, j) reads partial sp's value j (j < D: O, D: M,
 // D + 1: L); the on-chip and the global-memory merges share this code, so they agree bit for bit.
 template <int D, typename Get>
-ENG_DEVICE void merge_splits(const AttnDecodeParams& p, int nsplit, int G, size_t obase, float* s_w, float* s_inv,
-                             Get get) {
-  // every value is loaded before the arithmetic starts (the partials may sit in L2: one round trip, not
-  // one per split); the sums still run in split order
-  if (threadIdx.x < G) {
-    const int hr = threadIdx.x;
-    float ms[kMaxSplits], ls[kMaxSplits];
+ENG_DEVICE void merge_splits(const AttnDecodeParams& p, int nsplit, int G, size_t obase, Get get) {
+  // one output element per thread and iteration: its head's maxima and sums and its own partial sums of
+  // every split are loaded together (one round trip when the partials sit in L2), then combined in split
+  // order: M = max M_s, w_s = 2^(M_s - M), L = sum L_s w_s, out = (sum O_s w_s) / L
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int hr = i / D, dd = i - hr * D;
+    float ms[kMaxSplits], ls[kMaxSplits], os[kMaxSplits];
 #pragma unroll
     for (int sp = 0; sp < kMaxSplits; ++sp) {
       ms[sp] = sp < nsplit ? get(sp, hr, D) : -INFINITY;
       ls[sp] = sp < nsplit ? get(sp, hr, D + 1) : 0.f;
+      os[sp] = sp < nsplit ? get(sp, hr, dd) : 0.f;
     }
     float M = -INFINITY;
 #pragma unroll
     for (int sp = 0; sp < kMaxSplits; ++sp)
       if (sp < nsplit) M = fmaxf(M, ms[sp]);
-    float L = 0.f;
+    float L = 0.f, O = 0.f;
 #pragma unroll
     for (int sp = 0; sp < kMaxSplits; ++sp)
       if (sp < nsplit) {
         const float w = exp2f(ms[sp] - M);
-        s_w[sp * G + hr] = w;
         L += ls[sp] * w;
+        O += os[sp] * w;
       }
-    s_inv[hr] = 1.f / L;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int hr = i / D, dd = i - hr * D;
-    float v[kMaxSplits];
-#pragma unroll
-    for (int sp = 0; sp < kMaxSplits; ++sp) v[sp] = sp < nsplit ? get(sp, hr, dd) : 0.f;
-    float O = 0.f;
-#pragma unroll
-    for (int sp = 0; sp < kMaxSplits; ++sp)
-      if (sp < nsplit) O += v[sp] * s_w[sp * G + hr];
-    put_split(p.out_h, p.out_l, obase + hr * D + dd, O * s_inv[hr]);
+    put_split(p.out_h, p.out_l, obase + hr * D + dd, O * (1.f / L));
   }
 }
 
 // Per-CTA scratch outside the dynamic K/V stages.
 struct AttnShared {
   int last;
-  float w[kMaxSplits * 8];
-  float inv[8];
 };
 
 // One work item: split `split` of (row, KV head).  CLUSTER: the splits of a (row, KV head) are one
@@ -104,8 +91,6 @@ ENG_DEVICE void attn_item(const AttnDecodeParams& p, int row, int kvh, int split
   const int G = p.Hq / p.Hkv;
   const int h0 = kvh * G;
   int& s_last = sh.last;
-  float* s_w = sh.w;
-  float* s_inv = sh.inv;
   cg::cluster_group cluster = cg::this_cluster();
 
   // lengths and block tables are step inputs, final before the step's first kernel
@@ -340,7 +325,7 @@ ENG_DEVICE void attn_item(const AttnDecodeParams& p, int row, int kvh, int split
     if (p.max_splits > 1) {
       cluster.sync();
       if (split == 0 && sl > 0 && nsplit > 1)
-        merge_splits<D>(p, nsplit, G, obase, s_w, s_inv,
+        merge_splits<D>(p, nsplit, G, obase,
                         [&](int sp, int hr, int j) { return recv[((size_t)sp * G + hr) * (D + 2) + j]; });
     }
     return;
@@ -372,7 +357,7 @@ ENG_DEVICE void attn_item(const AttnDecodeParams& p, int row, int kvh, int split
   if (!s_last) return;
   __threadfence();
   const float* parts = p.ws + ((size_t)row * p.Hkv + kvh) * p.max_splits * G * (D + 2);
-  merge_splits<D>(p, nsplit, G, obase, s_w, s_inv,
+  merge_splits<D>(p, nsplit, G, obase,
                   [&](int sp, int hr, int j) { return __ldcg(parts + ((size_t)sp * G + hr) * (D + 2) + j); });
   if (threadIdx.x == 0) *counter = 0;  // ready for the next launch
 }

@@ -475,9 +475,9 @@ static int setup_buffers(eng_t* e) {
   e->sq_stride = std::max(e->g_o.max_groups(), e->g_down.max_groups());
   TRY(dev_alloc(e, &e->sq, (size_t)Tm * e->sq_stride));
 
-  // decode attention splits: up to 8 per row for block tables of at most 128 blocks (a row's splits can
-  // then merge on chip), up to 16 beyond; fixed per engine, so eager and replayed steps agree bit for bit
-  e->split_blocks = c.max_blocks_per_seq <= 128 ? (c.max_blocks_per_seq + 7) / 8 : (c.max_blocks_per_seq + 15) / 16;
+  // decode attention splits: at most 8 per row (a small batch's splits then merge on chip); fixed per
+  // engine, so eager and replayed steps agree bit for bit
+  e->split_blocks = (c.max_blocks_per_seq + 7) / 8;
   e->max_splits = (c.max_blocks_per_seq + e->split_blocks - 1) / e->split_blocks;
   TRY(dev_alloc(e, &e->attn_ws, (size_t)Rm * c.kv_heads * e->max_splits * (c.q_heads / c.kv_heads) * (d + 2)));
   TRY(dev_alloc(e, &e->attn_counters, (size_t)Rm * c.kv_heads));

@@ -134,7 +134,7 @@ struct AttnDecodeParams {
   bf16* out_l;
   int Hq, Hkv, d, NB;
   int split_blocks;       // KV blocks per split
-  int max_splits;         // grid.z (<= 16)
+  int max_splits;         // grid.z (<= 8)
   float* ws;              // [rows][Hkv][max_splits][G][d + 2] partials of multi-split rows
   int* counters;          // [rows][Hkv] finished splits, zero between launches
   float scale_log2;       // log2(e) / sqrt(d)
