@@ -128,6 +128,7 @@ ENG_DEVICE void attn_item(const AttnDecodeParams& p, int row, int kvh, int split
   const int nb = active && b_begin + warp < b_end ? (b_end - b_begin - warp + 3) / 4 : 0;
   int my_blk = 0;
   if (lane < nb) my_blk = p.bt[(size_t)r * p.mbs + b_begin + warp + 4 * lane];
+  const uint64_t kv_pol = l2_evict_first();
   auto issue = [&](int b, int stage) {
     const int j = (b - b_begin - warp) >> 2;
     int blk = j < 32 ? __shfl_sync(0xffffffffu, my_blk, j & 31) : p.bt[(size_t)r * p.mbs + b];
@@ -143,8 +144,8 @@ ENG_DEVICE void attn_item(const AttnDecodeParams& p, int row, int kvh, int split
     for (int i = lane; i < 16 * NCH; i += 32) {
       const int rr = i / NCH, c = i % NCH;
       const int sw = (c ^ (rr & 7)) * 8;
-      cp_async16(kd + rr * D + sw, ks_ + rr * D + c * 8);
-      cp_async16(vd + rr * D + sw, vs_ + rr * D + c * 8);
+      cp_async16_hint(kd + rr * D + sw, ks_ + rr * D + c * 8, kv_pol);  // K/V are read once per step
+      cp_async16_hint(vd + rr * D + sw, vs_ + rr * D + c * 8, kv_pol);
     }
     cp_async_commit();
   };

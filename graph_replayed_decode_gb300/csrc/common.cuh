@@ -88,15 +88,39 @@ ENG_DEVICE uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to
 ENG_DEVICE void cp_async16(void* smem_dst, const void* gmem_src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src));
 }
+// The same with an L2 cache policy for the source line.
+ENG_DEVICE void cp_async16_hint(void* smem_dst, const void* gmem_src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src),
+               "l"(pol));
+}
 ENG_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
 template <int N>
 ENG_DEVICE void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N));
 }
 
+// ------------------------------------------------------------------ L2 cache policies
+// Data read once per step and never again in it (the K/V stream) is marked evict-first; weights
+// prefetched into L2 for a later kernel are marked evict-last, so that a large K/V stream in between
+// does not push them out.
+ENG_DEVICE uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+ENG_DEVICE uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // ------------------------------------------------------------------ L2 prefetch
 ENG_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+ENG_DEVICE void prefetch_l2_keep(const void* p, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(pol)
+               : "memory");
 }
 
 // This CTA's share of an L2 prefetch of `bytes` (a multiple of 16) at p, split evenly over the grid.
@@ -106,9 +130,10 @@ ENG_DEVICE void prefetch_share(const void* p, unsigned long long bytes) {
   const unsigned long long share = ((bytes + ctas - 1) / ctas + 15) & ~15ull;
   unsigned long long lo = id * share, hi = lo + share;
   if (hi > bytes) hi = bytes;
+  const uint64_t pol = l2_evict_last();
   for (unsigned long long o = lo; o < hi; o += 65536) {
     const unsigned long long n = hi - o < 65536 ? hi - o : 65536;
-    prefetch_l2(static_cast<const char*>(p) + o, (uint32_t)n);
+    prefetch_l2_keep(static_cast<const char*>(p) + o, (uint32_t)n, pol);
   }
 }
 
