@@ -281,7 +281,8 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
   __syncthreads();        // barriers initialised, padding rows zeroed (TC: tensor memory allocated)
   if constexpr (TC) tc_fence_after();
   if (S > 1) cluster.sync();  // every CTA of the cluster has started before any pushes into its memory
-  pdl_trigger();
+  // The next kernel may launch (and start its own early copies) only once this kernel's inputs have
+  // arrived (see the trigger below): its early copies would otherwise queue ahead of these critical loads.
   pdl_wait();
 
   // X piece [pc, pc + pn) k-tiles: one bulk copy per token row and plane, issued by warp 0
@@ -373,6 +374,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
         set_status(p.status, ST_TIMEOUT);
         mbar_wait(&s_xbar, piece_no & 1, 1u << 26);
       }
+      if (piece_no == 0) pdl_trigger();  // inputs in: the next kernel may launch
 
       if (sm.tma) {
         constexpr int UT = kUnroll;
@@ -480,6 +482,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     // ---- tensor-core path: one thread issues every k-block's MMAs as its stage lands and refills the stage
     // the previous k-block used once those MMAs are done
     uint8_t* ring = tc_ring(smem);
+    pdl_trigger();  // the first stages' copies are in flight: the next kernel may launch
     // lane 0 of warp 0 issues; the rest of warp 0 waits at the warp barrier below, not on an mbarrier, so
     // the issuing lane never shares its warp with lanes that spin
     if (warp == 0 && lane == 0) {
