@@ -23,8 +23,8 @@
 //     partial sums while the copies are in flight;
 //   * a CTA owns RG 16-row tiles and one of S K-ranges; its 8 warps split the K-range and sum in a fixed
 //     order; the S CTAs of a row group form a thread-block cluster and add their tiles through distributed
-//     shared memory, always in split order (each CTA finishing every S-th token) -- deterministic and
-//     independent of T, so graph replay and eager execution are bit-identical;
+//     shared memory, always in split order (each CTA finishing a block of consecutive tokens) --
+//     deterministic and independent of T, so graph replay and eager execution are bit-identical;
 //   * epilogues run over the finished [16 RG rows x tokens] tile in shared memory:
 //       EPI_STORE_F32  out = Y (+bias)
 //       EPI_RESID      h += Y, each token's sum of h^2 over this CTA's rows and the planes of h * w_next
@@ -68,6 +68,13 @@ struct GemmSmem {
 static constexpr size_t kTmaMaxBytes = 128 * 1024;
 static constexpr size_t kSmemBudget = 200 * 1024;  // dynamic shared memory a GEMM CTA may use
 
+// Split-K: CTA `split` of a cluster finishes the block of kblk consecutive tokens starting at split * kblk
+// (a multiple of 4, so that partial sums move between CTAs as 16-byte vectors).
+__host__ __device__ inline int gemm_kblk(int NT, int S) {
+  const int k = (NT * 8 + S - 1) / S;
+  return (k + 3) & ~3;
+}
+
 __host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn, int S) {
   GemmSmem m;
   const size_t whole = (size_t)2 * NT * 8 * (ktn * 32 + 8) * 2;
@@ -80,7 +87,7 @@ __host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn, int S) {
   m.ts_bytes = (size_t)16 * RG * (NT * 8 + 1) * 4;
   // split-K: every CTA pushes its tile's columns for the tokens another CTA finishes into that CTA's
   // receive buffer [S][16 RG rows][tokens per CTA]
-  m.recv_bytes = S > 1 ? (size_t)S * 16 * RG * ((NT * 8 + S - 1) / S) * 4 : 0;
+  m.recv_bytes = S > 1 ? (size_t)S * 16 * RG * gemm_kblk(NT, S) * 4 : 0;
   const size_t tail = m.red_bytes + m.ts_bytes;
   // the receive buffer gets its own space: peers push into it while this CTA may still be staging X or
   // reducing its own tile
@@ -230,10 +237,11 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     for (int i = threadIdx.x; i < pad; i += 256) zh[i] = zl[i] = make_uint4(0u, 0u, 0u, 0u);
   }
 
-  // tokens this CTA finishes: split, split + S, ... (all of them when S == 1)
-  const int tok_first = S > 1 ? split : 0;
-  const int tok_step = S;
-  const int nown = tok_first < ntok ? (ntok - tok_first + tok_step - 1) / tok_step : 0;
+  // tokens this CTA finishes: a block of kblk from split * kblk (all of them when S == 1)
+  const int kblk = S > 1 ? gemm_kblk(NT, S) : NT * 8;
+  const int tok_first = S > 1 ? split * kblk : 0;
+  const int tok_step = 1;
+  const int nown = max(0, min(kblk, ntok - tok_first));
   if (EPI == EPI_QKV_ROPE) {
     // step inputs (positions, lengths, block tables) are final before the step's first kernel: resolve
     // each token's KV slot and fetch its RoPE row while the preceding kernel still runs
@@ -332,10 +340,11 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     for (int a = 0; a < NT; ++a) {
       const int r = warp + 8 * a;
       float ss = 0.f;
-      if (r < ntok) {
+      if (r < ntok) {  // the first 32 parts with no loop, so that every token's load is issued at once
         const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
         const float* part = p.sq_in + (size_t)src * p.sq_stride;
-        for (int j = lane; j < p.sq_parts; j += 32) ss += part[j];
+        ss = lane < p.sq_parts ? part[lane] : 0.f;
+        for (int j = lane + 32; j < p.sq_parts; j += 32) ss += part[j];
       }
       part_ss[a] = ss;
     }
@@ -458,22 +467,26 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
 
     // ---- split-K across the cluster: CTA `split` finishes tokens split, split + S, ... (sum in split order)
     if (S > 1) {
-      // push this CTA's columns of the tokens CTA q finishes into q's receive buffer, then every CTA adds
-      // its received columns in split order (its own columns at its own position)
-      const int kmax = (NT * 8 + S - 1) / S;
-      float* recv = reinterpret_cast<float*>(area + sm.recv_off);  // [S][rows][kmax]
-      for (int i = threadIdx.x; i < rows * ntok; i += 256) {
-        const int tok = i / rows, r = i - tok * rows;
-        const int q = tok % S;
-        if (q == split) continue;
-        cluster.map_shared_rank(recv, q)[((size_t)split * rows + r) * kmax + tok / S] = ts[r * TS + tok];
+      // push this CTA's partial sums of the tokens CTA q finishes into q's receive buffer (4 tokens per
+      // 16-byte store), then every CTA adds its block's partials in split order (its own at its position)
+      float* recv = reinterpret_cast<float*>(area + sm.recv_off);  // [S][rows][kblk]
+      const int groups = kblk / 4;
+      for (int i = threadIdx.x; i < S * rows * groups; i += 256) {
+        const int q = i / (rows * groups), rem = i - q * rows * groups;
+        const int r = rem / groups, c = rem - r * groups;
+        const int t0 = q * kblk + 4 * c;
+        if (q == split || t0 >= ntok) continue;
+        const float* src = ts + r * TS + t0;
+        const float4 v = make_float4(src[0], t0 + 1 < ntok ? src[1] : 0.f, t0 + 2 < ntok ? src[2] : 0.f,
+                                     t0 + 3 < ntok ? src[3] : 0.f);
+        *reinterpret_cast<float4*>(cluster.map_shared_rank(recv, q) + ((size_t)split * rows + r) * kblk + 4 * c) = v;
       }
       cluster.sync();
       for (int i = threadIdx.x; i < rows * nown; i += 256) {
         const int k = i / rows, r = i - k * rows;
-        const int tok = tok_first + k * tok_step;
+        const int tok = tok_first + k;
         float v = 0.f;
-        for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kmax + k];
+        for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kblk + k];
         ts[r * TS + tok] = v;
       }
       __syncthreads();
