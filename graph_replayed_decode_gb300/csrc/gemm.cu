@@ -155,6 +155,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
   constexpr int kUnroll = NT >= 8 ? 2 : 4;  // weight k-tiles loaded per group (register budget)
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float s_rstd[64];
+  __shared__ int s_xrow[64];           // row of X of each staged token (x_rows, a step input, or the token)
   __shared__ int s_flag;
   __shared__ int s_slot[64];           // EPI_QKV_ROPE: KV slot of each finished token (-1 padding, -2 bad)
   __shared__ int s_pos[64];            //               and its position
@@ -237,6 +238,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     for (int i = threadIdx.x; i < pad; i += 256) zh[i] = zl[i] = make_uint4(0u, 0u, 0u, 0u);
   }
 
+  if (threadIdx.x < ntok) s_xrow[threadIdx.x] = p.x_rows ? p.x_rows[n0 + threadIdx.x] : n0 + threadIdx.x;
   // tokens this CTA finishes: a block of kblk from split * kblk (all of them when S == 1)
   const int kblk = S > 1 ? gemm_kblk(NT, S) : NT * 8;
   const int tok_first = S > 1 ? split * kblk : 0;
@@ -293,14 +295,25 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
   // arrived (see the trigger below): its early copies would otherwise queue ahead of these critical loads.
   pdl_wait();
 
-  // X piece [pc, pc + pn) k-tiles: one bulk copy per token row and plane, issued by warp 0
+  // X piece [pc, pc + pn) k-tiles.  A few token rows: one bulk copy per row and plane, issued by warp 0.
+  // More rows: the CTA's threads issue 16-byte asynchronous copies (bulk copies are issued one after
+  // another, and dozens of them take microseconds to issue).
+  const bool x_async = ntok > 4;
   auto issue_x = [&](int pc, int pn) {
-    if (warp == 0) {
+    if (x_async) {
+      const int cpr = pn * 4;  // 16-byte chunks of a row in one plane
+      for (int i = threadIdx.x; i < 2 * ntok * cpr; i += 256) {
+        const int plane = i >= ntok * cpr;
+        const int rem = i - plane * ntok * cpr, r = rem / cpr, c = rem - r * cpr;
+        const size_t off = (size_t)s_xrow[r] * p.ldx + (size_t)(kt0 + pc) * 32 + c * 8;
+        cp_async16((plane ? xl : xs) + (size_t)r * xstride + c * 8, (plane ? p.Xl : p.Xh) + off);
+      }
+      cp_async_commit();
+    } else if (warp == 0) {
       if (lane == 0) mbar_expect_tx(&s_xbar, (uint32_t)(ntok * pn * 64 * 2));
       __syncwarp();
       for (int r = lane; r < ntok; r += 32) {
-        const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
-        const size_t off = (size_t)src * p.ldx + (size_t)(kt0 + pc) * 32;
+        const size_t off = (size_t)s_xrow[r] * p.ldx + (size_t)(kt0 + pc) * 32;
         tma_load_1d(xs + (size_t)r * xstride, p.Xh + off, (uint32_t)pn * 64u, &s_xbar);
         tma_load_1d(xl + (size_t)r * xstride, p.Xl + off, (uint32_t)pn * 64u, &s_xbar);
       }
@@ -341,8 +354,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
       const int r = warp + 8 * a;
       float ss = 0.f;
       if (r < ntok) {  // the first 32 parts with no loop, so that every token's load is issued at once
-        const int src = p.x_rows ? p.x_rows[n0 + r] : n0 + r;
-        const float* part = p.sq_in + (size_t)src * p.sq_stride;
+        const float* part = p.sq_in + (size_t)s_xrow[r] * p.sq_stride;
         ss = lane < p.sq_parts ? part[lane] : 0.f;
         for (int j = lane + 32; j < p.sq_parts; j += 32) ss += part[j];
       }
@@ -379,7 +391,10 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
         if (warp == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         issue_x(pc, pn);
       }
-      if (!mbar_wait(&s_xbar, piece_no & 1, 1u << 26)) {
+      if (x_async) {
+        cp_async_wait<0>();
+        __syncthreads();
+      } else if (!mbar_wait(&s_xbar, piece_no & 1, 1u << 26)) {
         set_status(p.status, ST_TIMEOUT);
         mbar_wait(&s_xbar, piece_no & 1, 1u << 26);
       }
