@@ -70,8 +70,11 @@ struct GemmPlan {
 struct GemmSite {
   int N = 0, K = 0, rg_fixed = 0;
   GemmPlan plan[2];
-  bool tc = false;  // the tensor-core path serves steps of kTcTokens tokens or more
-  bool use_tc(int T) const { return tc && T >= kTcTokens; }
+  bool tc = false;      // the shape allows the tensor-core path (128-row tiles)
+  bool tc_mid = false;  //   and it serves steps of kTcTokens..kTcPrefillTokens-1 tokens too
+  int tc_S = 1;         //   with this many K splits there (prefill-sized steps: none)
+  bool use_tc(int T) const { return tc && (T >= kTcPrefillTokens || (tc_mid && T >= kTcTokens)); }
+  int tc_splits(int T) const { return T >= kTcPrefillTokens ? 1 : tc_S; }
   const GemmPlan& for_tokens(int T) const { return plan[T >= kLargePlanTokens ? 1 : 0]; }
   int groups(int T) const { return use_tc(T) ? N / 128 : N / 16 / for_tokens(T).RG; }
   int max_groups() const { return std::max(N / 16 / plan[0].RG, N / 16 / plan[1].RG); }
@@ -455,8 +458,16 @@ static int setup_buffers(eng_t* e) {
     s.K = K;
     s.rg_fixed = rg_fixed;
     s.tc = N % 128 == 0 && K % 64 == 0 && (rg_fixed == 0 || 128 % (16 * rg_fixed) == 0);
+    if (s.tc) {  // K splits for about one CTA per SM, dividing the k-blocks of 64
+      const int tiles = N / 128, nkb = K / 64;
+      int sp = std::min(8, std::max(1, (152 + tiles / 2) / tiles));
+      while (sp > 1 && (nkb % sp != 0 || sp > nkb || !tc_split_fits(sp))) --sp;
+      s.tc_S = sp;
+    }
     gemm_plan(N, K, rg_fixed, &s.plan[0].RG, &s.plan[0].S, &s.plan[0].ktn);
     gemm_plan_large(N, K, rg_fixed, &s.plan[1].RG, &s.plan[1].S, &s.plan[1].ktn);
+    // mid-sized steps take the tensor cores where the warp-MMA plan's weight slice is too large to stage
+    s.tc_mid = s.tc && !gemm_slice_fits(s.plan[1].RG, s.plan[1].ktn);
     return ENG_OK;
   };
   TRY(site(e->g_qkv, QKV, H, d / 16, Tm));  // a CTA owns one whole head (QK-norm and RoPE in the epilogue)
@@ -540,10 +551,10 @@ static GemmParams gemm_params(eng_t* e, const GemmSite& s, const bf16* W, int T)
   p.RG = pl.RG;
   p.S = pl.S;
   p.kt_per_split = pl.ktn;
-  if (s.use_tc(T)) {  // tensor-core path: 128-row tiles, no K split
+  if (s.use_tc(T)) {  // tensor-core path: 128-row tiles
     p.RG = 8;
-    p.S = 1;
-    p.kt_per_split = s.K / 32;
+    p.S = s.tc_splits(T);
+    p.kt_per_split = s.K / 32 / p.S;
   }
   p.ldo = s.N;
   p.eps = e->c.rms_eps;

@@ -138,12 +138,17 @@ ENG_DEVICE void stage8(bf16* xs, bf16* xl, int idx, const float4 a, const float4
 // kTcStages shared-memory stages (weight tile, hi tile, lo tile per stage, TMA tensor copies with 128-byte
 // swizzle); one thread issues two tcgen05 MMAs per 16 k (hi plane, lo plane) into a 128 x 64 fp32 TMEM
 // accumulator; the accumulator is read back into the same [rows][tokens] tile the epilogues use.
-static constexpr int kTcStages = 5;
+static constexpr int kTcStages = 4;
 static constexpr uint32_t kTcA = 128 * 128;           // 128 weight rows x 64 bf16
 static constexpr uint32_t kTcB = 64 * 128;            // 64 tokens x 64 bf16, one plane
 static constexpr uint32_t kTcStage = kTcA + 2 * kTcB;
 static constexpr size_t kTcCsBytes = (size_t)64 * 128 * 4;  // QKV: the RoPE rows of the chunk's 64 tokens
-static constexpr size_t kTcSmem = (size_t)kTcStages * kTcStage + kTcCsBytes + 1024;  // + room to align to 1 KB
+// dynamic shared memory of a TC launch with S K-splits: [ring][RoPE rows][split-K receive buffer] + 1 KB to
+// align the ring (the receive buffer is separate: peers push into it while this CTA still runs its ring)
+__host__ __device__ inline size_t tc_recv_bytes(int S) { return S > 1 ? (size_t)S * 128 * gemm_kblk(8, S) * 4 : 0; }
+__host__ __device__ inline size_t tc_smem(int S) {
+  return (size_t)kTcStages * kTcStage + kTcCsBytes + tc_recv_bytes(S) + 1024;
+}
 
 ENG_DEVICE uint8_t* tc_ring(uint8_t* smem) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -189,7 +194,8 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
   const uint4* wp = reinterpret_cast<const uint4*>(p.W) + ((size_t)row_tile * KT + kt0) * 64 + lane;
   const int pn0 = min(sm.piece, ktn);
   uint4 pre[kPre][2];
-  const int nk = p.K >> 6;  // TC: k-blocks of 64
+  const int nk = (p.K >> 6) / S;  // TC: k-blocks of 64 of this split
+  const int kb0 = split * nk;      //     starting here
   if constexpr (TC) {
     // tensor memory for the accumulator, the stage barriers, and the weight tiles of the first stages
     if (warp == 0) tmem_alloc<64>(&s_tmem);
@@ -202,7 +208,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
       uint8_t* ring = tc_ring(smem);
       for (int kb = 0; kb < min(kTcStages, nk); ++kb) {
         mbar_expect_tx(&s_full[kb], kTcStage);
-        tma_tile_2d(ring + (size_t)kb * kTcStage, &tm->w, kb * 64, row0, &s_full[kb]);
+        tma_tile_2d(ring + (size_t)kb * kTcStage, &tm->w, (kb0 + kb) * 64, row0, &s_full[kb]);
       }
     }
   } else if (threadIdx.x == 0) {
@@ -323,8 +329,8 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     if (threadIdx.x == 0) {  // the activation tiles of the first stages
       uint8_t* ring = tc_ring(smem);
       for (int kb = 0; kb < min(kTcStages, nk); ++kb) {
-        tma_tile_2d(ring + (size_t)kb * kTcStage + kTcA, &tm->xh, kb * 64, n0, &s_full[kb]);
-        tma_tile_2d(ring + (size_t)kb * kTcStage + kTcA + kTcB, &tm->xl, kb * 64, n0, &s_full[kb]);
+        tma_tile_2d(ring + (size_t)kb * kTcStage + kTcA, &tm->xh, (kb0 + kb) * 64, n0, &s_full[kb]);
+        tma_tile_2d(ring + (size_t)kb * kTcStage + kTcA + kTcB, &tm->xl, (kb0 + kb) * 64, n0, &s_full[kb]);
       }
     }
   } else {
@@ -480,32 +486,6 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     }
     __syncthreads();
 
-    // ---- split-K across the cluster: CTA `split` finishes tokens split, split + S, ... (sum in split order)
-    if (S > 1) {
-      // push this CTA's partial sums of the tokens CTA q finishes into q's receive buffer (4 tokens per
-      // 16-byte store), then every CTA adds its block's partials in split order (its own at its position)
-      float* recv = reinterpret_cast<float*>(area + sm.recv_off);  // [S][rows][kblk]
-      const int groups = kblk / 4;
-      for (int i = threadIdx.x; i < S * rows * groups; i += 256) {
-        const int q = i / (rows * groups), rem = i - q * rows * groups;
-        const int r = rem / groups, c = rem - r * groups;
-        const int t0 = q * kblk + 4 * c;
-        if (q == split || t0 >= ntok) continue;
-        const float* src = ts + r * TS + t0;
-        const float4 v = make_float4(src[0], t0 + 1 < ntok ? src[1] : 0.f, t0 + 2 < ntok ? src[2] : 0.f,
-                                     t0 + 3 < ntok ? src[3] : 0.f);
-        *reinterpret_cast<float4*>(cluster.map_shared_rank(recv, q) + ((size_t)split * rows + r) * kblk + 4 * c) = v;
-      }
-      cluster.sync();
-      for (int i = threadIdx.x; i < rows * nown; i += 256) {
-        const int k = i / rows, r = i - k * rows;
-        const int tok = tok_first + k;
-        float v = 0.f;
-        for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kblk + k];
-        ts[r * TS + tok] = v;
-      }
-      __syncthreads();
-    }
   } else {
     // ---- tensor-core path: one thread issues every k-block's MMAs as its stage lands and refills the stage
     // the previous k-block used once those MMAs are done
@@ -543,9 +523,9 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
           }
           uint8_t* pst = ring + (size_t)ps * kTcStage;
           mbar_expect_tx(&s_full[ps], kTcStage);
-          tma_tile_2d(pst, &tm->w, nkb * 64, row0, &s_full[ps]);
-          tma_tile_2d(pst + kTcA, &tm->xh, nkb * 64, n0, &s_full[ps]);
-          tma_tile_2d(pst + kTcA + kTcB, &tm->xl, nkb * 64, n0, &s_full[ps]);
+          tma_tile_2d(pst, &tm->w, (kb0 + nkb) * 64, row0, &s_full[ps]);
+          tma_tile_2d(pst + kTcA, &tm->xh, (kb0 + nkb) * 64, n0, &s_full[ps]);
+          tma_tile_2d(pst + kTcA + kTcB, &tm->xl, (kb0 + nkb) * 64, n0, &s_full[ps]);
           issued = nkb + 1;
         }
       }
@@ -575,6 +555,33 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
       cp_async_wait<0>();
       __syncthreads();
     }
+  }
+  // ---- split-K across the cluster: CTA `split` finishes its block of tokens (sums in split order)
+  if (S > 1) {
+    // push this CTA's partial sums of the tokens CTA q finishes into q's receive buffer (4 tokens per
+    // 16-byte store), then every CTA adds its block's partials in split order (its own at its position)
+    float* recv = TC ? reinterpret_cast<float*>(tc_ring(smem) + (size_t)kTcStages * kTcStage + kTcCsBytes)
+                    : reinterpret_cast<float*>(area + sm.recv_off);  // [S][rows][kblk]
+    const int groups = kblk / 4;
+    for (int i = threadIdx.x; i < S * rows * groups; i += 256) {
+      const int q = i / (rows * groups), rem = i - q * rows * groups;
+      const int r = rem / groups, c = rem - r * groups;
+      const int t0 = q * kblk + 4 * c;
+      if (q == split || t0 >= ntok) continue;
+      const float* src = ts + r * TS + t0;
+      const float4 v = make_float4(src[0], t0 + 1 < ntok ? src[1] : 0.f, t0 + 2 < ntok ? src[2] : 0.f,
+                                   t0 + 3 < ntok ? src[3] : 0.f);
+      *reinterpret_cast<float4*>(cluster.map_shared_rank(recv, q) + ((size_t)split * rows + r) * kblk + 4 * c) = v;
+    }
+    cluster.sync();
+    for (int i = threadIdx.x; i < rows * nown; i += 256) {
+      const int k = i / rows, r = i - k * rows;
+      const int tok = tok_first + k;
+      float v = 0.f;
+      for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kblk + k];
+      ts[r * TS + tok] = v;
+    }
+    __syncthreads();
   }
   if (NORM_IN) {  // RMSNorm(h) W^T = (1 / rms(h)) ((h * w) W^T)
     for (int i = threadIdx.x; i < rows * nown; i += 256) {
@@ -824,7 +831,7 @@ void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_sp
 
 template <int NT, int EPI, bool NORM_IN, bool TC>
 static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, dim3 grid, const TcMaps* tm) {
-  const size_t smem_bytes = TC ? kTcSmem : gemm_smem(NT, p.RG, p.kt_per_split, p.S).total;
+  const size_t smem_bytes = TC ? tc_smem(p.S) : gemm_smem(NT, p.RG, p.kt_per_split, p.S).total;
   static bool attr_set = false;
   if (!attr_set) {
     if constexpr (TC)
@@ -858,7 +865,9 @@ static cudaError_t launch_epi(const GemmParams& p, const LaunchOpts& o, cudaStre
   const int nRG = p.N / 16 / p.RG;
   const dim3 grid(nRG, p.S, chunks_of(p.T));
   if (tc) {
-    if (EPI == EPI_LMHEAD || p.RG != 8 || p.S != 1 || p.x_rows || p.N % 128 || p.K % 64) return cudaErrorInvalidValue;
+    if (EPI == EPI_LMHEAD || p.RG != 8 || p.x_rows || p.N % 128 || p.K % 64 || (p.K / 64) % p.S ||
+        tc_smem(p.S) > kSmemBudget)
+      return cudaErrorInvalidValue;
     if constexpr (EPI == EPI_LMHEAD) return cudaErrorInvalidValue;
     else return launch_nt<8, EPI, NORM_IN, true>(p, o, s, grid, tc);
   }
@@ -888,6 +897,10 @@ cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const Launch
   }
   return cudaErrorInvalidValue;
 }
+
+bool gemm_slice_fits(int RG, int ktn) { return (size_t)RG * ktn * 1024 <= kTmaMaxBytes; }
+
+bool tc_split_fits(int S) { return S >= 1 && S <= kMaxCluster && tc_smem(S) <= kSmemBudget; }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

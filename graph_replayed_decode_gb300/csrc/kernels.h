@@ -104,8 +104,18 @@ struct TcMaps {
 // Encodes a 2D bf16 tensor map over a row-major [rows][cols] matrix with boxes of box_rows x 64 columns
 // (128-byte swizzle; rows past the end read as zeros).  False when the driver refuses it.
 bool make_tc_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
-// Token count from which a projection runs on the tensor-core path (when its shape allows it).
-static constexpr int kTcTokens = 65;
+// True when a tensor-core launch with S K-splits fits the shared-memory budget (its split-K receive buffer
+// grows with S).
+bool tc_split_fits(int S);
+// True when a warp-MMA plan's weight slice (RG row tiles x kt_per_split k-tiles) is small enough to be
+// bulk-copied into shared memory before the kernel waits; larger slices stream through registers.
+bool gemm_slice_fits(int RG, int ktn);
+// Token classes of the tensor-core path (when a projection's shape allows it): from kTcTokens tokens when
+// the warp-MMA large plan's weight slice is too large to stage (with K splits), and always from
+// kTcPrefillTokens (prefill chunks, no K split).  The boundaries coincide with the plan classes, so an
+// eager step and its padded bucket take the same path.
+static constexpr int kTcTokens = 9;
+static constexpr int kTcPrefillTokens = 65;
 
 // Picks RG / S / kt_per_split for an [N][K] weight (independent of T, so every token count computes
 // each output with the same summation order).  rg_fixed > 0 forces the rows per CTA (whole heads).
