@@ -24,6 +24,7 @@ __global__ void k_advance(AdvanceParams p) {
       id = 0;
     }
     if (step < p.ring_cap) p.ring[(size_t)step * p.rows + r] = id;
+    if (p.prev_row) p.prev_row[r] = -1;  // the next step's input is set here, not gathered
     if (s >= p.max_pos) {
       set_status(p.status, ST_BAD_POSITION);
       continue;

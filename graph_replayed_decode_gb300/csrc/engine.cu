@@ -58,7 +58,7 @@ struct Layer {
 
 // Word offsets of the step inputs inside one staging slot (host) and the device input region.
 struct InLayout {
-  size_t ids, pos, tok2req, cu, seq, last, invt, rng, wlog, step, items, bt, words;
+  size_t ids, pos, prev, tok2req, cu, seq, last, invt, rng, wlog, step, items, bt, words;
 };
 
 // One projection of the step with its two launch plans: [0] for steps of at most 8 tokens, [1] for
@@ -140,6 +140,7 @@ struct eng {
 
   // the decode batch that eng_decode continues (host mirror of its lengths)
   int dec_R = 0, dec_rows = 0, dec_bt_stride = 0;
+  int prev_rows = 0;  // requests of the last step (rows an async step may gather sampled ids from)
   std::vector<int> dec_seq;
 
   // per-launch event timing (eng_profile)
@@ -416,6 +417,7 @@ static int setup_buffers(eng_t* e) {
   size_t o = 0;
   L.ids = o; o += Tm;
   L.pos = o; o += Tm;
+  L.prev = o; o += Tm;
   L.tok2req = o; o += Tm;
   L.cu = o; o += Rm + 1;
   L.seq = o; o += Rm;
@@ -615,6 +617,9 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
   ep.sq_out = e->sq;
   ep.sq_stride = e->sq_stride;
   ep.norm_w = e->layers[0].in_norm;
+  ep.prev_row = in + e->in.prev;
+  ep.prev_ids = e->ids;
+  ep.prev_rows = c.max_reqs;
   ep.xh_out = e->xn_h;
   ep.xl_out = e->xn_l;
   ep.rows = T;
@@ -775,6 +780,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     AdvanceParams ad{};
     ad.sampled = e->ids;
     ad.ids = in + e->in.ids;
+    ad.prev_row = in + e->in.prev;
     ad.pos = in + e->in.pos;
     ad.seq = in + e->in.seq;
     ad.rng = reinterpret_cast<uint32_t*>(in + e->in.rng);
@@ -819,6 +825,7 @@ static void stage_padding(eng_t* e, int* h, int size) {
   for (int i = 0; i < size; ++i) {
     h[L.ids + i] = 0;
     h[L.pos + i] = 0;
+    h[L.prev + i] = -1;
     h[L.tok2req + i] = i;
     h[L.seq + i] = 0;
     h[L.last + i] = i;
@@ -983,6 +990,7 @@ int eng_capture(eng_t* e, const int32_t* sizes, int32_t n) {
     if (i && v[i] == v[i - 1]) return fail(e, ENG_EINVAL, "duplicate capture size");
   }
   CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+  e->prev_rows = 0;  // the warm-ups below overwrite the sampled ids: nothing to gather from afterwards
   for (auto it = v.rbegin(); it != v.rend(); ++it) {  // largest first
     const int size = *it;
     if (e->graphs.count(size)) {
@@ -1019,7 +1027,8 @@ int eng_capture(eng_t* e, const int32_t* sizes, int32_t n) {
   return ENG_OK;
 }
 
-int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_logits_dev) {
+static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int32_t* out_ids_dev,
+                     float* out_logits_dev) {
   if (!e) return ENG_EINVAL;
   if (!s || !out_ids_dev) return fail(e, ENG_EINVAL, "null step or out_ids");
   const eng_config_t& c = e->c;
@@ -1051,8 +1060,11 @@ int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_log
     for (int i = 0; i < ql; ++i) {
       if (s->positions[cu[r] + i] != sl - ql + i)
         return fail(e, ENG_EINVAL, "positions of a request must be consecutive and end at seq_len - 1");
+      const int src = prev_row ? prev_row[cu[r] + i] : -1;
+      if (src < -1 || src >= e->prev_rows)
+        return fail(e, ENG_EINVAL, "prev_row entry outside [-1, num_reqs of the previous step)");
       const int id = s->token_ids[cu[r] + i];
-      if (id < 0 || id >= c.vocab) return fail(e, ENG_EINVAL, "token id outside [0, vocab)");
+      if (src < 0 && (id < 0 || id >= c.vocab)) return fail(e, ENG_EINVAL, "token id outside [0, vocab)");
     }
     for (int b = 0; b < (sl + 15) / 16; ++b) {
       const int blk = s->block_tables[(size_t)r * bs + b];
@@ -1079,8 +1091,10 @@ int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_log
   const InLayout& L = e->in;
   float* hf = reinterpret_cast<float*>(h);
   for (int t = 0; t < T; ++t) {
-    h[L.ids + t] = s->token_ids[t];
+    const int src = prev_row ? prev_row[t] : -1;
+    h[L.ids + t] = src < 0 ? s->token_ids[t] : 0;
     h[L.pos + t] = s->positions[t];
+    h[L.prev + t] = src;
   }
   for (int r = 0; r < R; ++r) {
     for (int t = cu[r]; t < cu[r + 1]; ++t) h[L.tok2req + t] = r;
@@ -1096,6 +1110,7 @@ int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_log
   for (int r = R; r < rows; ++r) {  // bucket padding: token 0, position 0, length 0
     h[L.ids + r] = 0;
     h[L.pos + r] = 0;
+    h[L.prev + r] = -1;
     h[L.tok2req + r] = r;
     h[L.cu + r + 1] = r + 1;
     h[L.seq + r] = 0;
@@ -1153,7 +1168,18 @@ int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_log
   } else {
     e->dec_R = 0;
   }
+  e->prev_rows = R;
   return ENG_OK;
+}
+
+int eng_step(eng_t* e, const eng_step_t* s, int32_t* out_ids_dev, float* out_logits_dev) {
+  return step_impl(e, s, nullptr, out_ids_dev, out_logits_dev);
+}
+
+int eng_step_async(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int32_t* out_ids_dev,
+                   float* out_logits_dev) {
+  if (e && !prev_row) return fail(e, ENG_EINVAL, "null prev_row");
+  return step_impl(e, s, prev_row, out_ids_dev, out_logits_dev);
 }
 
 static int decode_capacity_check(eng_t* e, int n) {

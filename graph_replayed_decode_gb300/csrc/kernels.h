@@ -32,6 +32,9 @@ struct EmbedParams {
   float* sq_out;         // sum of squares of each row -> sq_out[row * sq_stride]
   int sq_stride;
   const float* norm_w;   // the first layer's input-norm weight [H]
+  const int* prev_row;   // [rows]: -1, or the previous step's request row whose sampled id is this token's
+  const int* prev_ids;   // the previous step's sampled ids [previous num_reqs]
+  int prev_rows;         // capacity of prev_ids (the host checks gathers against the previous step's rows)
   bf16* xh_out;          // operand planes of h * norm_w [rows][H] (see GemmParams)
   bf16* xl_out;
   int rows, H, V;
@@ -175,6 +178,7 @@ cudaError_t launch_attn_prefill(const AttnPrefillParams& p, const LaunchOpts& o,
 struct AdvanceParams {
   const int* sampled;  // [rows] ids sampled by this step
   int* ids;            // static inputs, advanced in place
+  int* prev_row;       // the token-to-previous-row map of the step inputs: reset to -1 for advanced rows
   int* pos;
   int* seq;
   uint32_t* rng;       // [4]: seed_lo, seed_hi, offset_lo, offset_hi (offset += 1)

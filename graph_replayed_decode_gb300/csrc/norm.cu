@@ -1,6 +1,7 @@
 // norm.cu -- embedding gather of layer 0 into the fp32 residual stream.
 //
-// h[t] = E[id[t]] (the embedding is stored packed; packed_offset finds each element), the row's sum of
+// h[t] = E[id[t]] (the embedding is stored packed; packed_offset finds each element; id[t] optionally
+// gathered from the previous step's sampled ids), the row's sum of
 // squares, and the first QKV GEMM's operand planes of h * w_in, which that GEMM turns into its input
 // RMSNorm by scaling with 1 / rms(h) ("33. Removing overhead", section "Fewer, larger matmuls": add_norm
 // does a residual update and the next norm in one pass; here every norm is folded into the GEMM that
@@ -20,6 +21,10 @@ __global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
   const int H = p.H;
   __shared__ float red[8];
   int id = p.ids[row];
+  // async scheduling: a token whose id the host did not know yet takes the id the previous step sampled
+  // for the given request row ("33. Removing overhead", section on async scheduling)
+  const int src = p.prev_row ? p.prev_row[row] : -1;
+  if (src >= 0) id = src < p.prev_rows ? p.prev_ids[src] : -1;
   if (id < 0 || id >= p.V) {
     set_status(p.status, ST_NAN);
     id = 0;

@@ -79,6 +79,8 @@ SIGNATURES = [
                                   ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
     ("eng_capture", ctypes.c_int, [ctypes.c_void_p, _I32P, ctypes.c_int32]),
     ("eng_step", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_t), ctypes.c_void_p, ctypes.c_void_p]),
+    ("eng_step_async", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_t), ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p]),
     ("eng_last_step_info", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_info_t)]),
     ("eng_decode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     ("eng_profile", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P, _F32P, ctypes.POINTER(ctypes.c_int64),
@@ -207,6 +209,14 @@ def eng_capture(e, sizes: Sequence[int]) -> None:
 
 def eng_step(e, step: StepArrays, out_ids_dev: int, out_logits_dev: int | None = None) -> None:
     _check(e, lib().eng_step(e, ctypes.byref(step.step), out_ids_dev, out_logits_dev))
+
+
+def eng_step_async(e, step: StepArrays, prev_row, out_ids_dev: int, out_logits_dev: int | None = None) -> None:
+    """eng_step where token t with prev_row[t] = r >= 0 takes the id the previous step sampled for row r."""
+    pr = np.ascontiguousarray(prev_row, dtype=np.int32)
+    if pr.shape != (step.step.num_tokens,):
+        raise ValueError("prev_row needs one entry per token")
+    _check(e, lib().eng_step_async(e, ctypes.byref(step.step), pr.ctypes.data, out_ids_dev, out_logits_dev))
 
 
 def eng_last_step_info(e) -> eng_step_info_t:

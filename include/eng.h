@@ -171,6 +171,20 @@ int eng_capture(eng_t* e, const int32_t* sizes, int32_t n);
  */
 int eng_step(eng_t* e, const eng_step_t* step, int32_t* out_ids_dev, float* out_logits_dev);
 
+/*
+ * eng_step_async -- eng_step for a scheduler that prepares step N+1 while step N still runs ("33.
+ * Removing overhead", the async-scheduling section: the next step's inputs are staged before the
+ * previous step's sampled tokens reach the host).  prev_row: host int32[num_tokens]; -1 takes
+ * step->token_ids[t] as usual; r >= 0 takes, on the device, the id the previous step sampled for its
+ * request row r (step->token_ids[t] is then ignored).  The previous step is the last eng_step,
+ * eng_step_async, eng_decode or eng_profile step of this engine since the last eng_capture.  The ids are
+ * gathered inside the step's first kernel, so a decode-only step still replays its graph.  A later
+ * eng_decode continues the batch as usual.  Errors: those of eng_step, and ENG_EINVAL when prev_row is
+ * NULL or an entry is outside [-1, previous num_reqs).
+ */
+int eng_step_async(eng_t* e, const eng_step_t* step, const int32_t* prev_row, int32_t* out_ids_dev,
+                   float* out_logits_dev);
+
 /* eng_last_step_info -- what the last successful eng_step (or eng_decode) did. */
 int eng_last_step_info(const eng_t* e, eng_step_info_t* info);
 

@@ -89,6 +89,16 @@ class GpuEngine:
         logits = self.logits_dev[:R].cpu().numpy().copy() if want_logits else None
         return ids, logits
 
+    def step_async(self, step, prev_row, want_logits: bool = True):
+        torch = self.torch
+        R = len(step.cu_seqlens) - 1
+        self.eng.eng_step_async(self.h, step, prev_row, self.ids_dev.data_ptr(),
+                                self.logits_dev.data_ptr() if want_logits else None)
+        torch.cuda.synchronize()
+        ids = self.ids_dev[:R].cpu().numpy().copy()
+        logits = self.logits_dev[:R].cpu().numpy().copy() if want_logits else None
+        return ids, logits
+
     def info(self):
         return self.eng.eng_last_step_info(self.h)
 

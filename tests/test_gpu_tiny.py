@@ -347,3 +347,78 @@ def test_tensor_core_prefill_chunks(weights):
         assert g.status() == 0
     finally:
         g.close()
+
+
+def test_async_step_gathers_the_previous_steps_ids(weights):
+    """eng_step_async: tokens whose ids the host does not know yet take, on the device, the ids the previous
+    step sampled.  Two engines run the same steps, one with the ids read back on the host (eng_step), one
+    with placeholders and a row map (eng_step_async): ids and logits agree bit for bit, in a replayed decode
+    step, in a mixed step (a new prompt chunk plus gathered decode rows), and in a device-resident step
+    after an async one."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    from graph_replayed_decode_gb300.eng import StepArrays
+    a, b = _engine(weights), _engine(weights)
+    try:
+        for g in (a, b):
+            g.capture([1, 2, 4, 8])
+        lens = [16, 9, 20]
+        blocks = [list(a.alloc(3)) for _ in lens] + [list(a.alloc(2))]
+        assert [list(b.alloc(3)) for _ in lens] + [list(b.alloc(2))] == blocks
+        bt = block_table(blocks, MBS)
+        temps = np.array([0.0, 0.9, 0.7], dtype=np.float32)
+        ids = np.concatenate([synth.prompt_ids(n, S.vocab, 60 + r) for r, n in enumerate(lens)])
+        pos = np.concatenate([np.arange(n) for n in lens])
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        st1 = StepArrays(ids, pos, cu, bt[:3], np.array(lens), temps, seed=4, offset=0)
+        ia, _ = a.step(st1)
+        ib, _ = b.step(st1)
+        np.testing.assert_array_equal(ia, ib)
+        # decode step: explicit ids on engine a, placeholders (invalid ids, ignored) gathered on engine b
+        p2 = np.array(lens)
+        ia2, la2 = a.step(StepArrays(ia, p2, np.arange(4), bt[:3], p2 + 1, temps, seed=4, offset=1))
+        ib2, lb2 = b.step_async(StepArrays(np.full(3, -5), p2, np.arange(4), bt[:3], p2 + 1, temps, seed=4, offset=1),
+                                [0, 1, 2])
+        assert b.info().replayed == 1
+        np.testing.assert_array_equal(ia2, ib2)
+        np.testing.assert_array_equal(la2.view(np.uint32), lb2.view(np.uint32))
+        # mixed step: a new 5-token prompt chunk (explicit ids) first, then the three decode rows; row 1's id
+        # given explicitly, rows 0 and 2 gathered from the previous step's rows 0 and 2
+        newp = synth.prompt_ids(5, S.vocab, 70)
+        p3 = p2 + 1
+        ids_a = np.concatenate([newp, ia2])
+        ids_b = np.concatenate([newp, [-1, ia2[1], -1]])
+        prev = np.concatenate([np.full(5, -1), [0, -1, 2]])
+        pos3 = np.concatenate([np.arange(5), p3])
+        cu3 = np.array([0, 5, 6, 7, 8])
+        bt3 = np.concatenate([bt[3:4], bt[:3]])
+        seq3 = np.concatenate([[5], p3 + 1])
+        t3 = np.concatenate([[0.0], temps]).astype(np.float32)
+        ia3, la3 = a.step(StepArrays(ids_a, pos3, cu3, bt3, seq3, t3, seed=4, offset=2))
+        ib3, lb3 = b.step_async(StepArrays(ids_b, pos3, cu3, bt3, seq3, t3, seed=4, offset=2), prev)
+        np.testing.assert_array_equal(ia3, ib3)
+        np.testing.assert_array_equal(la3.view(np.uint32), lb3.view(np.uint32))
+        # an async decode step, then the device-resident loop continues the batch on both engines
+        p4 = p3 + 1
+        a.step(StepArrays(ia3[1:], p4, np.arange(4), bt[:3], p4 + 1, temps, seed=4, offset=3))
+        b.step_async(StepArrays(np.zeros(3), p4, np.arange(4), bt[:3], p4 + 1, temps, seed=4, offset=3), [1, 2, 3])
+        ring_a = torch.zeros((2, 3), dtype=torch.int32, device="cuda")
+        ring_b = torch.zeros((2, 3), dtype=torch.int32, device="cuda")
+        eng.eng_decode(a.h, 2, ring_a.data_ptr())
+        eng.eng_decode(b.h, 2, ring_b.data_ptr())
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(ring_a.cpu().numpy(), ring_b.cpu().numpy())
+        assert a.status() == 0 and b.status() == 0
+        # a row outside the previous step's requests, and any gather right after a capture, are refused
+        p6 = p4 + 3
+        bad = StepArrays(np.zeros(3), p6, np.arange(4), bt[:3], p6 + 1, temps, seed=4, offset=6)
+        with pytest.raises(eng.EngError) as ei:
+            b.step_async(bad, [0, 1, 3])
+        assert ei.value.code == eng.ENG_EINVAL
+        b.capture([1, 2, 4, 8])
+        with pytest.raises(eng.EngError) as ei:
+            b.step_async(bad, [0, 1, 2])
+        assert ei.value.code == eng.ENG_EINVAL
+    finally:
+        a.close()
+        b.close()
