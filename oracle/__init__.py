@@ -44,11 +44,18 @@ from .sampler import (
     sample,
     sample_row,
 )
+from .filters import (
+    exp_f32,
+    sample_filtered,
+    sample_row_filtered,
+    survivor_counts,
+)
 from .pool import BlockPool, PoolExhausted, blocks_needed
 
 __all__ = [
     "OracleModel", "ContiguousCache", "PagedCache", "widen_bf16", "round_bf16", "rms_norm", "silu", "rope_inv_freq",
     "apply_rope", "attend_one", "attend_rows", "attend_packed", "forward_step", "fused_qkv",
     "fused_gate_up", "philox4x32_10", "uniforms", "ln_f32", "gumbel_f32", "sample", "sample_row",
+    "exp_f32", "sample_filtered", "sample_row_filtered", "survivor_counts",
     "BlockPool", "PoolExhausted", "blocks_needed",
 ]
