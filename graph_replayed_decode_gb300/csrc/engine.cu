@@ -1340,4 +1340,65 @@ int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, con
   return ENG_OK;
 }
 
+// top-p in units of 2^-24: 0 (off) unless 0 < p < 1; at least 1 unit; 2^24 units (p rounds to 1) is off.
+static int top_p_units(float p) {
+  if (!(p > 0.f && p < 1.f)) return 0;
+  const float units = std::rint(p * 16777216.0f);  // exact scaling; rint rounds half to even
+  if (units >= 16777216.0f) return 0;
+  return units < 1.0f ? 1 : (int)units;
+}
+
+int eng_sample_filtered(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature,
+                        const int32_t* top_k, const float* top_p, uint64_t seed, uint64_t offset, int32_t* out_ids_dev,
+                        int32_t* out_kept_dev, void* stream) {
+  if (rows < 0 || vocab < 1 || (rows > 0 && (!logits_dev || !temperature || !out_ids_dev)))
+    return fail(nullptr, ENG_EINVAL, "bad eng_sample_filtered arguments");
+  if (rows == 0) return ENG_OK;
+  // per-call device block: [inv_temp rows][top_k rows][top-p units rows][seed_lo, seed_hi, offset_lo, offset_hi]
+  std::vector<uint32_t> hbuf((size_t)rows * 3 + 4);
+  for (int r = 0; r < rows; ++r) {
+    if (!(temperature[r] >= 0.f) || !std::isfinite(temperature[r]))
+      return fail(nullptr, ENG_EINVAL, "temperature must be finite and >= 0");
+    if (top_p && !std::isfinite(top_p[r])) return fail(nullptr, ENG_EINVAL, "top_p must be finite");
+    const float it = inv_temperature(temperature[r]);
+    memcpy(&hbuf[r], &it, 4);
+    hbuf[(size_t)rows + r] = top_k ? (uint32_t)top_k[r] : 0u;
+    hbuf[(size_t)rows * 2 + r] = top_p ? (uint32_t)top_p_units(top_p[r]) : 0u;
+  }
+  const size_t rb = (size_t)rows * 3;
+  hbuf[rb + 0] = (uint32_t)seed;
+  hbuf[rb + 1] = (uint32_t)(seed >> 32);
+  hbuf[rb + 2] = (uint32_t)offset;
+  hbuf[rb + 3] = (uint32_t)(offset >> 32);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* d = nullptr;
+  if (cudaMallocAsync(&d, hbuf.size() * 4, st) != cudaSuccess) return fail(nullptr, ENG_ENOMEM, "cudaMallocAsync");
+  int rc = ENG_OK;
+  cudaError_t ce = cudaMemcpyAsync(d, hbuf.data(), hbuf.size() * 4, cudaMemcpyHostToDevice, st);
+  if (ce == cudaSuccess) {
+    const uint32_t* w = static_cast<const uint32_t*>(d);
+    FilterParams fp{};
+    fp.logits = logits_dev;
+    fp.vocab = vocab;
+    fp.inv_temp = reinterpret_cast<const float*>(w);
+    fp.top_k = reinterpret_cast<const int*>(w + rows);
+    fp.p_units = reinterpret_cast<const int*>(w + (size_t)rows * 2);
+    fp.rng = w + rb;
+    fp.out_ids = out_ids_dev;
+    fp.out_kept = out_kept_dev;
+    fp.status = nullptr;
+    fp.only_filtered = 0;
+    ce = launch_sample_filtered(fp, rows, st);
+  }
+  if (ce != cudaSuccess) rc = fail(nullptr, ENG_ECUDA, std::string("eng_sample_filtered: ") + cudaGetErrorString(ce));
+  if (cudaStreamSynchronize(st) != cudaSuccess && rc == ENG_OK) rc = ENG_ECUDA;  // hbuf is pageable host memory
+  cudaFreeAsync(d, st);
+  return rc;
+}
+
+int eng_exp_f32(const float* d_dev, float* out_dev, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!d_dev || !out_dev))) return ENG_EINVAL;
+  return launch_exp_rn(d_dev, out_dev, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ENG_OK : ENG_ECUDA;
+}
+
 }  // extern "C"

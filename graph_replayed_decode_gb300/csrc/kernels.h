@@ -196,6 +196,21 @@ cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int
 cudaError_t launch_gumbel(const float* u, float* g, int64_t n, cudaStream_t s);
 cudaError_t launch_sample(const float* logits, int rows, int vocab, const float* inv_temp, const uint32_t* rng,
                           unsigned long long* best, int* out_ids, int* status, cudaStream_t s);
+// Top-k / top-p filtered draw (sample_filter.cu): one CTA per row over float32 logits [rows][vocab].
+struct FilterParams {
+  const float* logits;
+  int vocab;
+  const float* inv_temp;  // [rows]; 0 = greedy
+  const int* top_k;       // [rows] or null; <= 0 or >= vocab: off
+  const int* p_units;     // [rows] or null; top-p in units of 2^-24, 0 (or >= 2^24): off
+  const uint32_t* rng;    // seed_lo, seed_hi, offset_lo, offset_hi
+  int* out_ids;           // [rows]
+  int* out_kept;          // [rows] survivor counts, or null
+  int* status;            // or null
+  int only_filtered;      // 1: rows with no filter (or temperature 0) are left untouched
+};
+cudaError_t launch_sample_filtered(const FilterParams& p, int rows, cudaStream_t s);
+cudaError_t launch_exp_rn(const float* d, float* out, int64_t n, cudaStream_t s);
 // Fixed device array for eng_sample_noalloc: [inverse temperatures of up to noalloc_max_rows() rows][4 words].
 int noalloc_max_rows();
 cudaError_t noalloc_scratch(uint32_t** out);

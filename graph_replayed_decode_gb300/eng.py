@@ -103,6 +103,10 @@ SIGNATURES = [
                                   ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]),
     ("eng_sample_noalloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, _F32P, ctypes.c_uint64,
                                           ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]),
+    ("eng_sample_filtered", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, _F32P,
+                                           _I32P, _F32P, ctypes.c_uint64, ctypes.c_uint64,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    ("eng_exp_f32", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
 ]
 
 
@@ -316,3 +320,19 @@ def eng_sample_noalloc(logits_dev: int, rows: int, vocab: int, temperature, seed
     t = np.ascontiguousarray(temperature, dtype=np.float32)
     _check(None, lib().eng_sample_noalloc(logits_dev, rows, vocab, t.ctypes.data_as(_F32P), seed, offset,
                                           out_ids_dev, stream))
+
+
+def eng_sample_filtered(logits_dev: int, rows: int, vocab: int, temperature, top_k, top_p, seed: int, offset: int,
+                        out_ids_dev: int, out_kept_dev: int | None = None, stream: int | None = None):
+    """eng_sample with top-k / top-p filters; top_k or top_p None disables that filter for every row."""
+    t = np.ascontiguousarray(temperature, dtype=np.float32)
+    k = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32)
+    p = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32)
+    _check(None, lib().eng_sample_filtered(
+        logits_dev, rows, vocab, t.ctypes.data_as(_F32P),
+        None if k is None else _ptr_i32(k),
+        None if p is None else p.ctypes.data_as(_F32P), seed, offset, out_ids_dev, out_kept_dev, stream))
+
+
+def eng_exp_f32(d_dev: int, out_dev: int, n: int, stream: int | None = None):
+    _check(None, lib().eng_exp_f32(d_dev, out_dev, n, stream))

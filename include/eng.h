@@ -323,6 +323,37 @@ int eng_sample(const float* logits_dev, int32_t rows, int32_t vocab, const float
 int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature,
                        uint64_t seed, uint64_t offset, int32_t* out_ids_dev, void* stream);
 
+/*
+ * eng_sample_filtered -- the sampler with top-k and top-p filters ahead of the draw ("19. Fast decode",
+ * section "Sampling without the CPU": filtered logits become -inf before the argmax; a fixed k and a
+ * sort-and-mask top-p keep the shapes static).  Per row r, with s = logits[r][v] * (1/T_r) in float32:
+ *   - rank order: larger logit first, equal logits (+0 and -0 equal) by increasing index;
+ *   - top-k keeps the first top_k[r] entries of that order (top_k[r] <= 0 or >= vocab: no filter);
+ *   - top-p keeps, among the top-k survivors, the shortest prefix of the order whose softmax(s) mass
+ *     reaches p = top_p[r] (no filter unless 0 < p < 1).  The cut is exact integer arithmetic: weights
+ *     w_v = floor(e^(s_v - s_max) * 2^32) with the library's own float32 exp (eng_exp_f32), p rounded
+ *     to units of 2^-24 (at least one), and entry v survives iff the weight ahead of it, times 2^24, is
+ *     below p_units * (total weight).  The top entry always survives.
+ *   - out_ids[r] = argmax over the survivors of s + g, g the Gumbel noise of eng_sample (same seed, offset
+ *     and row), ties to the lowest index; temperature 0 takes the plain argmax (no filter can drop it).
+ * logits_dev: device float[rows][vocab], finite (a non-finite logit is skipped; it never survives);
+ * z / T must stay finite.  temperature: host float[rows], finite, >= 0.  top_k: host int32[rows] or NULL
+ * (no top-k).  top_p: host float[rows], finite, or NULL (no top-p).  out_ids_dev: device int32[rows].
+ * out_kept_dev: device int32[rows] or NULL; receives each row's survivor count (1 at temperature 0).
+ * The call allocates a small device block for the per-row parameters and synchronises `stream` before it
+ * returns.  Errors: ENG_EINVAL (arguments, with a message), ENG_ENOMEM, ENG_ECUDA.
+ */
+int eng_sample_filtered(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature,
+                        const int32_t* top_k, const float* top_p, uint64_t seed, uint64_t offset, int32_t* out_ids_dev,
+                        int32_t* out_kept_dev, void* stream);
+
+/*
+ * eng_exp_f32 -- out[i] = e^d[i] for float32 d[i] <= 0, the exp of eng_sample_filtered's top-p weights:
+ * n = rint(d / ln 2), r = d - n ln2_hi - n ln2_lo, e^r by its Taylor series to r^7/7! (Horner), times 2^n;
+ * every step one correctly rounded float32 operation; 0 for d < -23.  d_dev, out_dev: device float[n].
+ */
+int eng_exp_f32(const float* d_dev, float* out_dev, int64_t n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
