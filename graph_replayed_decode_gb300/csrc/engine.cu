@@ -58,7 +58,7 @@ struct Layer {
 
 // Word offsets of the step inputs inside one staging slot (host) and the device input region.
 struct InLayout {
-  size_t ids, pos, prev, tok2req, cu, seq, last, invt, rng, wlog, step, items, bt, words;
+  size_t ids, pos, prev, tok2req, cu, seq, last, invt, topk, punit, rng, wlog, step, items, bt, words;
 };
 
 // One projection of the step with its two launch plans: [0] for steps of at most 8 tokens, [1] for
@@ -214,6 +214,7 @@ static std::string check_config(const eng_config_t& c) {
   if (c.num_blocks < 1 || c.max_reqs < 1 || c.max_tokens < c.max_reqs || c.max_blocks_per_seq < 1)
     return "bad engine capacity (num_blocks, max_reqs <= max_tokens, max_blocks_per_seq)";
   if (!(c.rms_eps > 0.f) || !(c.rope_theta > 0.0)) return "rms_eps and rope_theta must be positive";
+  if (c.sampling_filters != 0 && c.sampling_filters != 1) return "sampling_filters must be 0 or 1";
   return "";
 }
 
@@ -423,6 +424,8 @@ static int setup_buffers(eng_t* e) {
   L.seq = o; o += Rm;
   L.last = o; o += Rm;
   L.invt = o; o += Rm;
+  L.topk = o; o += Rm;
+  L.punit = o; o += Rm;
   L.rng = o; o += 4;
   L.wlog = o; o += 2;
   L.step = o; o += 2;
@@ -776,6 +779,27 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
   pl.x_rows = in + e->in.last;
   if ((r = gemm_launch(e, pl, e->g_lm, EPI_LMHEAD, true, ENG_K_LM_HEAD, st)) != cudaSuccess) return r;
 
+  // ---- top-k / top-p: rows with a filter redraw from the logits the LM head wrote (the others keep the
+  // fused draw); a plain launch, so it starts after the LM head has finished
+  if (c.sampling_filters) {
+    FilterParams fp{};
+    fp.logits = e->logits;
+    fp.vocab = c.vocab;
+    fp.inv_temp = reinterpret_cast<const float*>(in + e->in.invt);
+    fp.top_k = in + e->in.topk;
+    fp.p_units = in + e->in.punit;
+    fp.rng = reinterpret_cast<const uint32_t*>(in + e->in.rng);
+    fp.out_ids = e->ids;
+    fp.out_kept = nullptr;
+    fp.status = e->status;
+    fp.only_filtered = 1;
+    e->launches++;
+    prof_begin(e, st, ENG_K_SAMPLE_FILTER, (int64_t)R * c.vocab * 4);
+    r = launch_sample_filtered(fp, R, st);
+    prof_end(e, st);
+    if (r != cudaSuccess) return r;
+  }
+
   if (advance) {
     AdvanceParams ad{};
     ad.sampled = e->ids;
@@ -804,6 +828,14 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
 
 static float inv_temperature(float T) { return T == 0.f ? 0.f : 1.0f / T; }
 
+// top-p in units of 2^-24: 0 (off) unless 0 < p < 1; at least 1 unit; 2^24 units (p rounds to 1) is off.
+static int top_p_units(float p) {
+  if (!(p > 0.f && p < 1.f)) return 0;
+  const float units = std::rint(p * 16777216.0f);  // exact scaling; rint rounds half to even
+  if (units >= 16777216.0f) return 0;
+  return units < 1.0f ? 1 : (int)units;
+}
+
 // Waits (rarely) for the copy that last used this staging slot, then returns it cleared.
 static int* take_slot(eng_t* e, int* slot_index) {
   const int k = e->slot;
@@ -830,6 +862,8 @@ static void stage_padding(eng_t* e, int* h, int size) {
     h[L.seq + i] = 0;
     h[L.last + i] = i;
     reinterpret_cast<float*>(h)[L.invt + i] = 0.f;
+    h[L.topk + i] = 0;
+    h[L.punit + i] = 0;
   }
   for (int i = 0; i <= size; ++i) h[L.cu + i] = i;
   h[L.rng + 0] = h[L.rng + 1] = h[L.rng + 2] = h[L.rng + 3] = 0;
@@ -1041,7 +1075,7 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
   const int32_t* cu = s->cu_seqlens;
   if (cu[0] != 0 || cu[R] != T) return fail(e, ENG_EINVAL, "cu_seqlens must start at 0 and end at num_tokens");
   int P = 0;
-  bool seen_decode = false;
+  bool seen_decode = false, any_filter = false;
   for (int r = 0; r < R; ++r) {
     const int ql = cu[r + 1] - cu[r];
     if (ql < 1) return fail(e, ENG_EINVAL, "every request needs at least one token");
@@ -1072,6 +1106,12 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
     }
     const float tp = s->temperature[r];
     if (!(tp >= 0.f) || !std::isfinite(tp)) return fail(e, ENG_EINVAL, "temperature must be finite and >= 0");
+    if (s->top_p && !std::isfinite(s->top_p[r])) return fail(e, ENG_EINVAL, "top_p must be finite");
+    const bool filtered = (s->top_k && s->top_k[r] > 0 && s->top_k[r] < c.vocab) ||
+                          (s->top_p && top_p_units(s->top_p[r]) > 0);
+    if (filtered && !c.sampling_filters)
+      return fail(e, ENG_EINVAL, "top_k / top_p need an engine created with sampling_filters = 1");
+    any_filter = any_filter || filtered;
   }
 
   const bool decode_only = (T == R);
@@ -1102,6 +1142,8 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
     h[L.seq + r] = s->seq_lens[r];
     h[L.last + r] = cu[r + 1] - 1;
     hf[L.invt + r] = inv_temperature(s->temperature[r]);
+    h[L.topk + r] = s->top_k ? s->top_k[r] : 0;
+    h[L.punit + r] = s->top_p ? top_p_units(s->top_p[r]) : 0;
     int* row = h + L.bt + (size_t)r * c.max_blocks_per_seq;
     memcpy(row, s->block_tables + (size_t)r * bs, (size_t)bs * 4);
     if (bs < c.max_blocks_per_seq) memset(row + bs, 0, (size_t)(c.max_blocks_per_seq - bs) * 4);
@@ -1116,12 +1158,14 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
     h[L.seq + r] = 0;
     h[L.last + r] = r;
     hf[L.invt + r] = 0.f;
+    h[L.topk + r] = 0;
+    h[L.punit + r] = 0;
   }
   h[L.rng + 0] = (int)(uint32_t)s->seed;
   h[L.rng + 1] = (int)(uint32_t)(s->seed >> 32);
   h[L.rng + 2] = (int)(uint32_t)s->offset;
   h[L.rng + 3] = (int)(uint32_t)(s->offset >> 32);
-  h[L.wlog] = out_logits_dev ? 1 : 0;
+  h[L.wlog] = (out_logits_dev || any_filter) ? 1 : 0;  // the filter kernel reads the logits
 
   // prefill work items: (request, first token, count <= 64)
   int n_items = 0;
@@ -1338,14 +1382,6 @@ int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, con
                       out_ids_dev, nullptr, st);
   if (r != cudaSuccess) return fail(nullptr, ENG_ECUDA, std::string("eng_sample_noalloc: ") + cudaGetErrorString(r));
   return ENG_OK;
-}
-
-// top-p in units of 2^-24: 0 (off) unless 0 < p < 1; at least 1 unit; 2^24 units (p rounds to 1) is off.
-static int top_p_units(float p) {
-  if (!(p > 0.f && p < 1.f)) return 0;
-  const float units = std::rint(p * 16777216.0f);  // exact scaling; rint rounds half to even
-  if (units >= 16777216.0f) return 0;
-  return units < 1.0f ? 1 : (int)units;
 }
 
 int eng_sample_filtered(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature,

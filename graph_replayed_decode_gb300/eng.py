@@ -42,6 +42,7 @@ class eng_config_t(ctypes.Structure):
         ("qk_norm", ctypes.c_int32), ("qkv_bias", ctypes.c_int32), ("tie_embeddings", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
         ("max_reqs", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+        ("sampling_filters", ctypes.c_int32),
     ]
 
 
@@ -57,7 +58,8 @@ _F32P = ctypes.POINTER(ctypes.c_float)
 class eng_step_t(ctypes.Structure):
     _fields_ = [("num_tokens", ctypes.c_int32), ("num_reqs", ctypes.c_int32), ("bt_stride", ctypes.c_int32),
                 ("token_ids", _I32P), ("positions", _I32P), ("cu_seqlens", _I32P), ("block_tables", _I32P),
-                ("seq_lens", _I32P), ("temperature", _F32P), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+                ("seq_lens", _I32P), ("temperature", _F32P), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+                ("top_k", _I32P), ("top_p", _F32P)]
 
 
 class eng_step_info_t(ctypes.Structure):
@@ -144,14 +146,16 @@ def _ptr_i32(a: np.ndarray):
 # ------------------------------------------------------------------ marshalling helpers
 
 
-def make_config(shape, num_blocks: int, max_reqs: int, max_tokens: int, max_blocks_per_seq: int) -> eng_config_t:
+def make_config(shape, num_blocks: int, max_reqs: int, max_tokens: int, max_blocks_per_seq: int,
+                sampling_filters: bool = False) -> eng_config_t:
     """eng_config_t from a model shape (any object with the synth.ModelShape fields)."""
     return eng_config_t(
         layers=shape.layers, hidden=shape.hidden, q_heads=shape.q_heads, kv_heads=shape.kv_heads,
         head_dim=shape.head_dim, intermediate=shape.intermediate, vocab=shape.vocab, rms_eps=shape.rms_eps,
         rope_theta=shape.rope_theta, qk_norm=int(shape.qk_norm), qkv_bias=int(shape.qkv_bias),
         tie_embeddings=int(shape.tie_embeddings), dtype=ENG_DTYPE_BF16, block_size=16, num_blocks=num_blocks,
-        max_reqs=max_reqs, max_tokens=max_tokens, max_blocks_per_seq=max_blocks_per_seq)
+        max_reqs=max_reqs, max_tokens=max_tokens, max_blocks_per_seq=max_blocks_per_seq,
+        sampling_filters=int(sampling_filters))
 
 
 class TensorList:
@@ -179,7 +183,7 @@ class StepArrays:
     """eng_step_t over host arrays (kept alive by this object)."""
 
     def __init__(self, token_ids, positions, cu_seqlens, block_tables, seq_lens, temperature, seed: int = 0,
-                 offset: int = 0):
+                 offset: int = 0, top_k=None, top_p=None):
         self.token_ids = _i32(token_ids)
         self.positions = _i32(positions)
         self.cu_seqlens = _i32(cu_seqlens)
@@ -187,13 +191,17 @@ class StepArrays:
         self.block_tables = np.ascontiguousarray(bt)
         self.seq_lens = _i32(seq_lens)
         self.temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+        self.top_k = None if top_k is None else _i32(top_k)
+        self.top_p = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32)
         R = len(self.cu_seqlens) - 1
         self.step = eng_step_t(
             num_tokens=len(self.token_ids), num_reqs=R, bt_stride=self.block_tables.shape[1],
             token_ids=_ptr_i32(self.token_ids), positions=_ptr_i32(self.positions),
             cu_seqlens=_ptr_i32(self.cu_seqlens), block_tables=_ptr_i32(self.block_tables),
             seq_lens=_ptr_i32(self.seq_lens), temperature=self.temperature.ctypes.data_as(_F32P),
-            seed=int(seed), offset=int(offset))
+            seed=int(seed), offset=int(offset),
+            top_k=None if self.top_k is None else _ptr_i32(self.top_k),
+            top_p=None if self.top_p is None else self.top_p.ctypes.data_as(_F32P))
 
 
 # ------------------------------------------------------------------ entry points
@@ -234,7 +242,7 @@ def eng_decode(e, n_steps: int, out_ids_dev: int) -> None:
 
 
 KERNEL_KINDS = ["embed_norm", "norm", "gemm_qkv", "rope_kv", "attn_decode", "attn_prefill", "gemm_o",
-                "gemm_gate_up", "gemm_down", "lm_head", "advance"]
+                "gemm_gate_up", "gemm_down", "lm_head", "advance", "sample_filter"]
 
 
 def eng_profile(e, capacity: int = 4096):

@@ -75,6 +75,8 @@ typedef struct {
   int32_t tie_embeddings; /* 1: the LM head is the embedding matrix */
   int32_t dtype;          /* ENG_DTYPE_BF16 */
   int32_t block_size, num_blocks, max_reqs, max_tokens, max_blocks_per_seq;
+  int32_t sampling_filters; /* 1: steps may ask for top-k / top-p (eng_step_t.top_k, .top_p); every step and
+                               every captured graph then also writes the logits and runs the filter kernel */
 } eng_config_t;
 
 /*
@@ -110,7 +112,10 @@ typedef struct {
  *     (bt_stride <= max_blocks_per_seq columns; unused entries are ignored);
  *   seq_lens[num_reqs]: keys visible to request r's last query = its position + 1;
  *   temperature[num_reqs]: 0 selects greedy argmax, > 0 Gumbel-max at that temperature;
- *   seed, offset: Philox key and counter words of this step's Gumbel noise.
+ *   seed, offset: Philox key and counter words of this step's Gumbel noise;
+ *   top_k[num_reqs], top_p[num_reqs] (each may be NULL: no such filter): the filters of
+ *     eng_sample_filtered ahead of request r's draw (top_k <= 0 or >= vocab, top_p outside (0, 1): off;
+ *     top_p finite); an engine created with sampling_filters = 0 rejects any active filter (ENG_EINVAL).
  * A request's positions must be consecutive and end at seq_lens[r] - 1.
  */
 typedef struct {
@@ -122,6 +127,8 @@ typedef struct {
   const int32_t* seq_lens;
   const float* temperature;
   uint64_t seed, offset;
+  const int32_t* top_k;
+  const float* top_p;
 } eng_step_t;
 
 /* What the last eng_step did (for tests and benchmarks). */
@@ -215,6 +222,7 @@ int eng_decode(eng_t* e, int32_t n_steps, int32_t* out_ids_dev);
 #define ENG_K_GEMM_DOWN 8
 #define ENG_K_LM_HEAD 9
 #define ENG_K_ADVANCE 10
+#define ENG_K_SAMPLE_FILTER 11
 
 /*
  * eng_profile -- time every kernel of one further decode step of the current batch (as eng_decode with

@@ -37,14 +37,14 @@ class GpuEngine:
     """One engine over synth weights; outputs come back as numpy arrays."""
 
     def __init__(self, s: synth.ModelShape, weights, num_blocks: int, max_reqs: int, max_tokens: int,
-                 max_blocks_per_seq: int, stream=None):
+                 max_blocks_per_seq: int, stream=None, sampling_filters: bool = False):
         import torch
         self.eng = ensure_built()
         self.torch = torch
         self.s = s
         self.num_blocks = num_blocks
         self.max_blocks_per_seq = max_blocks_per_seq
-        cfg = self.eng.make_config(s, num_blocks, max_reqs, max_tokens, max_blocks_per_seq)
+        cfg = self.eng.make_config(s, num_blocks, max_reqs, max_tokens, max_blocks_per_seq, sampling_filters)
         tl = self.eng.TensorList(weights.items())
         self.stream = stream
         self.h = self.eng.eng_create(cfg, tl, None if stream is None else stream.cuda_stream)

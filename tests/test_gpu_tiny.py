@@ -422,3 +422,67 @@ def test_async_step_gathers_the_previous_steps_ids(weights):
     finally:
         a.close()
         b.close()
+
+
+def test_top_k_top_p_inside_eager_replayed_and_device_loop_steps(weights):
+    """Per-request filters in the step ("19. Fast decode", §Sampling without the CPU): eager prefill,
+    graph-replayed decode and the device-resident loop; every id equals the oracle's filtered draw from the
+    step's own logits, bit for bit, rows without a filter keep the fused draw, greedy rows the argmax."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    from graph_replayed_decode_gb300.eng import StepArrays
+    g = GpuEngine(S, weights, num_blocks=NB, max_reqs=8, max_tokens=128, max_blocks_per_seq=MBS,
+                  sampling_filters=True)
+    try:
+        g.capture([1, 2, 4, 8])
+        R, P, steps = 5, 12, 5
+        blocks = [list(g.alloc(oracle.blocks_needed(P + steps + 2))) for _ in range(R)]
+        bt = block_table(blocks, MBS)
+        temps = np.array([1.0, 1.5, 0.0, 1.2, 0.9], np.float32)
+        ks = np.array([20, 0, 5, 1, 0], np.int32)
+        ps = np.array([1.0, 0.6, 0.5, 0.9, 1.0], np.float32)       # row 4: no filter
+        ids = np.concatenate([synth.prompt_ids(P, S.vocab, 40 + r) for r in range(R)])
+        pos = np.concatenate([np.arange(P)] * R)
+        cu = np.arange(R + 1) * P
+        host, changed = [], 0
+        for k in range(steps):
+            seq = np.array([pos[cu[r + 1] - 1] + 1 for r in range(R)])
+            gid, glog = g.step(StepArrays(ids, pos, cu, bt, seq, temps, seed=9, offset=k, top_k=ks, top_p=ps))
+            assert g.info().replayed == int(k > 0)
+            np.testing.assert_array_equal(gid, oracle.sample_filtered(glog, temps, ks, ps, 9, k))
+            changed += int(np.any(gid != oracle.sample(glog, temps, 9, k)))
+            host.append(gid.copy())
+            ids, pos, cu = gid.copy(), seq.copy(), np.arange(R + 1)
+        assert changed > 0                                          # the filters did act on some draw
+        # redo step steps-2 without asking for logits (the filters still need them), then the device loop
+        k = steps - 2
+        again, _ = g.step(StepArrays(host[k - 1], np.full(R, P + k - 1), np.arange(R + 1), bt, np.full(R, P + k),
+                                     temps, seed=9, offset=k, top_k=ks, top_p=ps), want_logits=False)
+        np.testing.assert_array_equal(again, host[k])
+        ring = torch.zeros((1, R), dtype=torch.int32, device="cuda")
+        eng.eng_decode(g.h, 1, ring.data_ptr())
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(ring[0].cpu().numpy(), host[k + 1])
+        assert g.status() == 0
+    finally:
+        g.close()
+
+
+def test_filters_need_an_engine_created_for_them(weights):
+    from graph_replayed_decode_gb300 import eng
+    from graph_replayed_decode_gb300.eng import StepArrays
+    g = _engine(weights)
+    try:
+        blocks = [list(g.alloc(1))]
+        bt = block_table(blocks, MBS)
+        t = np.array([1.0], np.float32)
+        base = dict(token_ids=[3], positions=[0], cu_seqlens=[0, 1], block_tables=bt, seq_lens=[1], temperature=t)
+        g.step(StepArrays(**base, top_k=[0], top_p=[1.0]))           # inactive filters are fine
+        with pytest.raises(eng.EngError, match="sampling_filters"):
+            g.step(StepArrays(**base, top_k=[5]))
+        with pytest.raises(eng.EngError, match="sampling_filters"):
+            g.step(StepArrays(**base, top_p=[0.5]))
+        with pytest.raises(eng.EngError, match="finite"):
+            g.step(StepArrays(**base, top_p=[float("nan")]))
+    finally:
+        g.close()
