@@ -217,8 +217,10 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
 
     weights = synth.make_weights(s, seed=0, cache=False)
     stream = torch.cuda.Stream()
-    h = eng.eng_create(eng.make_config(s, nb, 64, max_tokens, mbs), eng.TensorList(weights.items()),
-                       stream.cuda_stream)
+    filters = args.top_k > 0 or 0.0 < args.top_p < 1.0
+    h = eng.eng_create(eng.make_config(s, nb, 64, max_tokens, mbs, sampling_filters=filters),
+                       eng.TensorList(weights.items()), stream.cuda_stream)
+    fk = dict(top_k=np.full(B, args.top_k, np.int32), top_p=np.full(B, args.top_p, np.float32)) if filters else {}
     del weights
     ids_dev = torch.zeros(64, dtype=torch.int32, device="cuda")
     temps = np.full(B, wl["temperature"], dtype=np.float32)
@@ -231,7 +233,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     if wl["prefill"]:
         assert B == 1
         prompt = synth.prompt_ids(ctxs[0], s.vocab, 0)
-        st = eng.StepArrays(prompt, np.arange(ctxs[0]), [0, ctxs[0]], bt, [ctxs[0]], temps, seed=0, offset=0)
+        st = eng.StepArrays(prompt, np.arange(ctxs[0]), [0, ctxs[0]], bt, [ctxs[0]], temps, seed=0, offset=0, **fk)
         eng.eng_step(h, st, ids_dev.data_ptr(), None)   # warm-up: same prompt, same blocks, same K/V written
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -249,7 +251,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     eng.eng_capture(h, CAPTURE_SIZES)
 
     pos = np.array(ctxs, dtype=np.int32)
-    st = eng.StepArrays(first, pos, np.arange(B + 1), bt, pos + 1, temps, seed=0, offset=1)
+    st = eng.StepArrays(first, pos, np.arange(B + 1), bt, pos + 1, temps, seed=0, offset=1, **fk)
     eng.eng_step(h, st, ids_dev.data_ptr(), None)           # first decode step (host inputs)
     launches_per_step = eng.eng_last_step_info(h).launches
     ring = torch.zeros((max(K, W, 1), B), dtype=torch.int32, device="cuda")
@@ -286,7 +288,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     h2d = 0
     t0 = time.perf_counter()
     for k in range(K):
-        st = eng.StepArrays(ids_h, pos, np.arange(B + 1), bt, pos + 1, temps, seed=0, offset=10_000 + k)
+        st = eng.StepArrays(ids_h, pos, np.arange(B + 1), bt, pos + 1, temps, seed=0, offset=10_000 + k, **fk)
         eng.eng_step(h, st, ids_dev.data_ptr(), None)
         with torch.cuda.stream(stream):
             pinned.copy_(ids_dev[:B], non_blocking=True)
@@ -341,6 +343,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
         "data": "synthetic",
         "config": {"workload": wl["text"], "batch": B, "context_start": ctxs if B <= 4 else "seeded draw",
                    "temperature": wl["temperature"], "capture_sizes": CAPTURE_SIZES,
+                   **({"top_k": args.top_k, "top_p": args.top_p} if filters else {}),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {roofline.weight_bytes(s) / 1e9:.3f} GB of weights read per step"},
         "step_roofline": {"bytes_per_step": int(step_b), "t_roof_ms": t_roof * 1e3, "frac": t_roof / step_s,
@@ -399,6 +402,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_0p6b_b1")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--top-k", type=int, default=0, help="top-k filter on every row (0: off)")
+    ap.add_argument("--top-p", type=float, default=1.0, help="top-p filter on every row (1: off)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     wl = WORKLOADS[args.workload]
