@@ -1271,6 +1271,62 @@ int eng_decode(eng_t* e, int32_t n_steps, int32_t* out_ids_dev) {
   return ENG_OK;
 }
 
+int eng_generate(eng_t* e, int32_t max_steps, int32_t check_every, const int32_t* stop_ids, int32_t n_stop,
+                 int32_t* out_tokens, int32_t* out_lengths) {
+  if (!e) return ENG_EINVAL;
+  if (max_steps < 0 || check_every < 1 || n_stop < 0 || (n_stop > 0 && !stop_ids) ||
+      (max_steps > 0 && (!out_tokens || !out_lengths)))
+    return fail(e, ENG_EINVAL, "bad eng_generate arguments");
+  if (e->dec_R <= 0) return fail(e, ENG_ESTATE, "no decode batch to continue (the last eng_step was not decode-only)");
+  const int R = e->dec_R;
+  if (max_steps == 0) return 0;
+  TRY(decode_capacity_check(e, max_steps));
+  std::vector<int32_t> stops(stop_ids, stop_ids + n_stop);
+  std::sort(stops.begin(), stops.end());
+  const int group = std::min(check_every, max_steps);
+  int32_t* d_buf = nullptr;
+  int32_t* h_buf = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&d_buf), (size_t)group * R * 4, e->stream) != cudaSuccess)
+    return fail(e, ENG_ENOMEM, "eng_generate: device buffer");
+  if (cudaMallocHost(reinterpret_cast<void**>(&h_buf), (size_t)group * R * 4) != cudaSuccess) {
+    cudaFreeAsync(d_buf, e->stream);
+    return fail(e, ENG_ENOMEM, "eng_generate: pinned host buffer");
+  }
+  std::vector<int32_t> len(R, -1);  // tokens up to and including the first stop id; -1: none met yet
+  int produced = 0, rc = ENG_OK;
+  while (produced < max_steps) {
+    const int steps = std::min(group, max_steps - produced);
+    if ((rc = eng_decode(e, steps, d_buf)) != ENG_OK) break;
+    // the one synchronisation of the group
+    if (cudaMemcpyAsync(h_buf, d_buf, (size_t)steps * R * 4, cudaMemcpyDeviceToHost, e->stream) != cudaSuccess ||
+        cudaStreamSynchronize(e->stream) != cudaSuccess) {
+      rc = fail(e, ENG_ECUDA, "eng_generate: reading a group's ids");
+      break;
+    }
+    int alive = 0;
+    for (int r = 0; r < R; ++r) {
+      for (int k = 0; k < steps; ++k) {
+        const int32_t tok = h_buf[(size_t)k * R + r];
+        out_tokens[(size_t)r * max_steps + produced + k] = tok;
+        if (len[r] < 0 && std::binary_search(stops.begin(), stops.end(), tok)) len[r] = produced + k + 1;
+      }
+      alive += len[r] < 0;
+    }
+    produced += steps;
+    if (alive == 0) break;
+  }
+  cudaFreeAsync(d_buf, e->stream);
+  cudaStreamSynchronize(e->stream);  // h_buf is freed below
+  cudaFreeHost(h_buf);
+  if (rc != ENG_OK) return rc;
+  for (int r = 0; r < R; ++r) {  // trim what follows a stop (and the steps never run)
+    const int n = len[r] < 0 ? produced : len[r];
+    out_lengths[r] = n;
+    for (int k = n; k < max_steps; ++k) out_tokens[(size_t)r * max_steps + k] = -1;
+  }
+  return produced;
+}
+
 int eng_profile(eng_t* e, int32_t capacity, int32_t* kinds, float* ms, int64_t* bytes, int32_t* count) {
   if (!e) return ENG_EINVAL;
   if (capacity < 1 || !kinds || !ms || !bytes || !count) return fail(e, ENG_EINVAL, "bad eng_profile arguments");

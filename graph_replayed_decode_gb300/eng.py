@@ -109,6 +109,8 @@ SIGNATURES = [
                                            _I32P, _F32P, ctypes.c_uint64, ctypes.c_uint64,
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("eng_exp_f32", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
+    ("eng_generate", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, _I32P, ctypes.c_int32, _I32P,
+                                    _I32P]),
 ]
 
 
@@ -344,3 +346,14 @@ def eng_sample_filtered(logits_dev: int, rows: int, vocab: int, temperature, top
 
 def eng_exp_f32(d_dev: int, out_dev: int, n: int, stream: int | None = None):
     _check(None, lib().eng_exp_f32(d_dev, out_dev, n, stream))
+
+
+def eng_generate(e, num_reqs: int, max_steps: int, check_every: int, stop_ids=()):
+    """Decode steps with a stop check every check_every steps; returns (tokens [R, max_steps], lengths [R],
+    steps run).  Tokens past a request's length are -1."""
+    stops = _i32(list(stop_ids))
+    toks = np.full((num_reqs, max_steps), -2, dtype=np.int32)
+    lens = np.zeros(num_reqs, dtype=np.int32)
+    n = _check(e, lib().eng_generate(e, max_steps, check_every, _ptr_i32(stops) if len(stops) else None, len(stops),
+                                     _ptr_i32(toks), _ptr_i32(lens)))
+    return toks, lens, n

@@ -37,7 +37,7 @@ extern "C" {
 #define ENG_EINVAL (-1)    /* bad argument, shape or request order (the pages raise ValueError) */
 #define ENG_ECAPACITY (-2) /* a position at or past max_blocks_per_seq * block_size ("19. Fast decode",
                               StaticKVCache: prompt plus new tokens exceed the capacity) */
-#define ENG_ENOMEM (-3)    /* a device or pinned-host allocation failed (eng_create only) */
+#define ENG_ENOMEM (-3)    /* a device or pinned-host allocation failed */
 #define ENG_EPOOL (-4)     /* the KV block pool has fewer free blocks than requested */
 #define ENG_ECUDA (-5)     /* a CUDA runtime call failed (no device, launch failure, ...) */
 #define ENG_EDEVICE (-6)   /* a kernel-side check failed; see eng_status */
@@ -209,6 +209,24 @@ int eng_last_step_info(const eng_t* e, eng_step_info_t* info);
  * (a sequence would outgrow its block-table row or max_blocks_per_seq * 16), ENG_EINVAL, ENG_ECUDA.
  */
 int eng_decode(eng_t* e, int32_t n_steps, int32_t* out_ids_dev);
+
+/*
+ * eng_generate -- eng_decode with stop tokens checked once every check_every steps ("19. Fast decode",
+ * the section on syncs: one synchronisation per check; tokens generated after a stop are trimmed
+ * afterwards, so at most check_every - 1 steps are wasted).  Continues the decode batch of the last
+ * eng_step like eng_decode, in groups of min(check_every, steps left) device-resident steps; after each
+ * group one copy brings the group's ids to the host, where each request's first stop id is found.  The
+ * call ends when every request has met a stop id or max_steps steps have run.  Requests that stopped keep
+ * decoding (shapes stay static) until the call ends; their later tokens are trimmed.
+ * stop_ids: host int32[n_stop] (may be NULL when n_stop = 0).  out_tokens: host int32[num_reqs][max_steps]:
+ * request r's tokens, -1 past out_lengths[r].  out_lengths: host int32[num_reqs]: tokens up to and
+ * including the first stop id, or every step run when there is none.  Returns the number of steps run
+ * (>= 0; a multiple of check_every unless max_steps cut the last group), or ENG_EINVAL, ENG_ESTATE,
+ * ENG_ECAPACITY (checked for all max_steps before any step runs), ENG_ENOMEM, ENG_ECUDA.  The engine's
+ * batch continues after the steps that ran.
+ */
+int eng_generate(eng_t* e, int32_t max_steps, int32_t check_every, const int32_t* stop_ids, int32_t n_stop,
+                 int32_t* out_tokens, int32_t* out_lengths);
 
 /* Kernel kinds reported by eng_profile. */
 #define ENG_K_EMBED_NORM 0

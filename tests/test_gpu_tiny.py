@@ -486,3 +486,53 @@ def test_filters_need_an_engine_created_for_them(weights):
             g.step(StepArrays(**base, top_p=[float("nan")]))
     finally:
         g.close()
+
+
+def test_generate_checks_stop_ids_once_per_group(weights):
+    """eng_generate ("19. Fast decode": stop tokens checked every check_every steps, one sync per check,
+    tokens after a stop trimmed) against eng_decode on an identical engine: the same tokens, each length at
+    the request's first stop id, and the steps run end at the first group boundary where all have stopped."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    from graph_replayed_decode_gb300.eng import StepArrays
+    steps, group, R, P = 24, 4, 3, 10
+    engines = []
+    try:
+        for _ in range(2):
+            g = _engine(weights)
+            engines.append(g)
+            g.capture([1, 2, 4, 8])
+            blocks = [list(g.alloc(oracle.blocks_needed(P + steps + 4))) for _ in range(R)]
+            bt = block_table(blocks, MBS)
+            temps = np.array([0.9, 1.1, 0.0], np.float32)
+            ids = np.concatenate([synth.prompt_ids(P, S.vocab, 60 + r) for r in range(R)])
+            pos = np.concatenate([np.arange(P)] * R)
+            gid, _ = g.step(StepArrays(ids, pos, np.arange(R + 1) * P, bt, np.full(R, P), temps, seed=4, offset=0))
+            g.step(StepArrays(gid, np.full(R, P), np.arange(R + 1), bt, np.full(R, P + 1), temps, seed=4, offset=1))
+        a, b = engines
+        ring = torch.zeros((steps, R), dtype=torch.int32, device="cuda")
+        eng.eng_decode(b.h, steps, ring.data_ptr())
+        torch.cuda.synchronize()
+        full = ring.cpu().numpy().T                                   # [R, steps]
+        stops = sorted({int(full[0, 5]), int(full[1, 13])})
+        first = [next((k + 1 for k in range(steps) if full[r, k] in stops), None) for r in range(R)]
+        toks, lens, n = eng.eng_generate(a.h, R, steps, group, stops)
+        assert n == (steps if None in first else min(steps, -(-max(first) // group) * group))
+        for r in range(R):
+            L = first[r] if first[r] is not None else n
+            assert lens[r] == L
+            np.testing.assert_array_equal(toks[r, :L], full[r, :L])
+            assert (toks[r, L:] == -1).all()
+        if n < steps:                                                  # the batch continues where it stopped
+            nxt = torch.zeros((1, R), dtype=torch.int32, device="cuda")
+            eng.eng_decode(a.h, 1, nxt.data_ptr())
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(nxt[0].cpu().numpy(), full[:, n])
+        toks, lens, n2 = eng.eng_generate(a.h, R, 3, 8, [])           # no stop ids: every step runs
+        assert n2 == 3 and (lens == 3).all()
+        with pytest.raises(eng.EngError):
+            eng.eng_generate(a.h, R, 4, 0, [1])                         # check_every must be >= 1
+        assert a.status() == 0
+    finally:
+        for g in engines:
+            g.close()
