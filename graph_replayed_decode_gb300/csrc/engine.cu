@@ -58,7 +58,7 @@ struct Layer {
 
 // Word offsets of the step inputs inside one staging slot (host) and the device input region.
 struct InLayout {
-  size_t ids, pos, prev, tok2req, cu, seq, last, invt, topk, punit, rng, wlog, step, items, bt, words;
+  size_t ids, pos, prev, tok2req, cu, seq, last, invt, topk, punit, rng, wlog, wkey, step, items, bt, words;
 };
 
 // One projection of the step with its two launch plans: [0] for steps of at most 8 tokens, [1] for
@@ -128,6 +128,8 @@ struct eng {
   int* ids = nullptr;      // [Rm]
   int* slots = nullptr;    // [Tm]
   unsigned long long* best = nullptr;
+  float* keys = nullptr;            // [Rm][V] sampling keys from the LM head (engines with sampling filters)
+  unsigned int* row_ext = nullptr;  // [Rm][2] the LM head's logit extremes, reset by the filter kernel
   int* done_counter = nullptr;
   int* status = nullptr;
   GemmSite g_qkv, g_o, g_gu, g_down, g_lm;
@@ -427,7 +429,8 @@ static int setup_buffers(eng_t* e) {
   L.topk = o; o += Rm;
   L.punit = o; o += Rm;
   L.rng = o; o += 4;
-  L.wlog = o; o += 2;
+  L.wlog = o; o += 1;
+  L.wkey = o; o += 1;
   L.step = o; o += 2;
   o = (o + 3) & ~(size_t)3;
   L.items = o; o += (size_t)4 * e->max_items;
@@ -454,6 +457,10 @@ static int setup_buffers(eng_t* e) {
   TRY(dev_alloc(e, &e->ids, Rm));
   TRY(dev_alloc(e, &e->slots, Tm));
   TRY(dev_alloc(e, &e->best, Rm));
+  if (c.sampling_filters) {
+    TRY(dev_alloc(e, &e->keys, (size_t)Rm * c.vocab));
+    TRY(dev_alloc(e, &e->row_ext, (size_t)Rm * 2));
+  }
   TRY(dev_alloc(e, &e->done_counter, 4));
   TRY(dev_alloc(e, &e->status, 4));
   TRY(dev_alloc(e, &e->ring, (size_t)e->ring_cap * Rm));
@@ -777,6 +784,9 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
   pl.sq_in = e->sq;
   pl.sq_parts = sq_parts;
   pl.x_rows = in + e->in.last;
+  pl.keys_out = e->keys;  // (null unless the engine has sampling filters)
+  pl.write_keys = in + e->in.wkey;
+  pl.row_ext = e->row_ext;
   if ((r = gemm_launch(e, pl, e->g_lm, EPI_LMHEAD, true, ENG_K_LM_HEAD, st)) != cudaSuccess) return r;
 
   // ---- top-k / top-p: rows with a filter redraw from the logits the LM head wrote (the others keep the
@@ -793,6 +803,9 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     fp.out_kept = nullptr;
     fp.status = e->status;
     fp.only_filtered = 1;
+    fp.keys = e->keys;
+    fp.keys_valid = in + e->in.wkey;
+    fp.row_ext = e->row_ext;
     e->launches++;
     prof_begin(e, st, ENG_K_SAMPLE_FILTER, (int64_t)R * c.vocab * 4);
     r = launch_sample_filtered(fp, R, st);
@@ -868,6 +881,7 @@ static void stage_padding(eng_t* e, int* h, int size) {
   for (int i = 0; i <= size; ++i) h[L.cu + i] = i;
   h[L.rng + 0] = h[L.rng + 1] = h[L.rng + 2] = h[L.rng + 3] = 0;
   h[L.wlog] = 0;
+  h[L.wkey] = 0;
 }
 
 // ------------------------------------------------------------------ C ABI
@@ -1075,7 +1089,7 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
   const int32_t* cu = s->cu_seqlens;
   if (cu[0] != 0 || cu[R] != T) return fail(e, ENG_EINVAL, "cu_seqlens must start at 0 and end at num_tokens");
   int P = 0;
-  bool seen_decode = false, any_filter = false;
+  bool seen_decode = false, any_filter = false, need_keys = false;
   for (int r = 0; r < R; ++r) {
     const int ql = cu[r + 1] - cu[r];
     if (ql < 1) return fail(e, ENG_EINVAL, "every request needs at least one token");
@@ -1112,6 +1126,9 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
     if (filtered && !c.sampling_filters)
       return fail(e, ENG_EINVAL, "top_k / top_p need an engine created with sampling_filters = 1");
     any_filter = any_filter || filtered;
+    // rows whose draw may run over the whole row: the LM head then stores every key for the filter kernel
+    const int tk = s->top_k ? s->top_k[r] : 0;
+    if (s->top_p && top_p_units(s->top_p[r]) > 0 && (tk <= 0 || tk > kFilterGatherCap)) need_keys = true;
   }
 
   const bool decode_only = (T == R);
@@ -1166,6 +1183,7 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
   h[L.rng + 2] = (int)(uint32_t)s->offset;
   h[L.rng + 3] = (int)(uint32_t)(s->offset >> 32);
   h[L.wlog] = (out_logits_dev || any_filter) ? 1 : 0;  // the filter kernel reads the logits
+  h[L.wkey] = need_keys ? 1 : 0;
 
   // prefill work items: (request, first token, count <= 64)
   int n_items = 0;

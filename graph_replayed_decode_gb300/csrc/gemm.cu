@@ -687,17 +687,27 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     }
   } else if (EPI == EPI_LMHEAD) {
     const bool wl = *p.write_logits != 0;
+    const bool wk = wl && p.keys_out && *p.write_keys != 0, we = wl && p.row_ext;  // (uniform)
     const uint32_t rng[4] = {p.rng[0], p.rng[1], p.rng[2], p.rng[3]};
     for (int k = warp; k < nown; k += 8) {
       const int tok = tok_first + k * tok_step;
       const int tkn = n0 + tok;
       const float it = p.inv_temp[tkn];
       unsigned long long best = 0ull;
+      uint32_t omax = 0u, omin_inv = 0u;  // extremes of the finite logits, as order-preserving bits
       for (int r = lane; r < rows; r += 32) {
         const int v = row0 + r;
         const float z = ts[r * TS + tok];
         if (wl) p.logits[(size_t)tkn * p.N + v] = z;
         const float key = sample_key(z, it, rng, (uint32_t)tkn, (uint32_t)v);
+        if (wk) p.keys_out[(size_t)tkn * p.N + v] = key;
+        if (we && (__float_as_uint(z) & 0x7F800000u) != 0x7F800000u) {
+          uint32_t f = __float_as_uint(z);
+          if (f == 0x80000000u) f = 0u;  // -0 orders as +0
+          const uint32_t o = (f & 0x80000000u) ? ~f : (f | 0x80000000u);
+          omax = o > omax ? o : omax;
+          omin_inv = ~o > omin_inv ? ~o : omin_inv;
+        }
         if (key != key) {
           set_status(p.status, ST_NAN);
         } else {
@@ -711,6 +721,14 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
         best = x > best ? x : best;
       }
       if (lane == 0 && best) atomicMax(p.best + tkn, best);
+      if (we) {
+        omax = __reduce_max_sync(0xffffffffu, omax);
+        omin_inv = __reduce_max_sync(0xffffffffu, omin_inv);
+        if (lane == 0 && omax) {
+          atomicMax(p.row_ext + 2 * tkn, omax);
+          atomicMax(p.row_ext + 2 * tkn + 1, omin_inv);
+        }
+      }
     }
     __threadfence();
     __syncthreads();

@@ -92,6 +92,10 @@ struct GemmParams {
   // EPI_LMHEAD: logits and sampling
   float* logits;                // [T][N] when *write_logits != 0
   const int* write_logits;      // device flag
+  float* keys_out;              // or null: [T][N] sampling keys (logit / T + Gumbel noise), when *write_keys
+  const int* write_keys;        // device flag (with keys_out)
+  unsigned int* row_ext;        // or null: [T][2] order-preserving bits of the row's largest finite logit
+                                //   and their complement for the smallest (atomicMax), with the logits
   const float* inv_temp;        // [T]; 0 = greedy
   const uint32_t* rng;          // device [4]: seed_lo, seed_hi, offset_lo, offset_hi
   unsigned long long* best;     // [T] packed (key, ~index), zero between launches
@@ -208,8 +212,15 @@ struct FilterParams {
   int* out_kept;          // [rows] survivor counts, or null
   int* status;            // or null
   int only_filtered;      // 1: rows with no filter (or temperature 0) are left untouched
+  const float* keys;      // or null: the rows' sampling keys, already formed when *keys_valid (else computed)
+  const int* keys_valid;  // device flag (with keys)
+  unsigned int* row_ext;  // or null: the rows' logit extremes, already formed (else found here); reset to 0
+                          //   by this kernel for every row it is launched over
 };
 cudaError_t launch_sample_filtered(const FilterParams& p, int rows, cudaStream_t s);
+// Top-k candidates up to this many are sorted in shared memory and drawn from there (no key needed from the
+// producer of the logits); rows past it (and top-p without top-k) draw over a pass of the whole row.
+constexpr int kFilterGatherCap = 8192;
 cudaError_t launch_exp_rn(const float* d, float* out, int64_t n, cudaStream_t s);
 // Fixed device array for eng_sample_noalloc: [inverse temperatures of up to noalloc_max_rows() rows][4 words].
 int noalloc_max_rows();

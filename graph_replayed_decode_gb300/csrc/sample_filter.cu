@@ -33,7 +33,7 @@ namespace {
 constexpr int kFThreads = 1024;
 constexpr int kFWarps = kFThreads / 32;
 constexpr int kBuckets = 2048;
-constexpr int kGatherCap = 8192;
+constexpr int kGatherCap = kFilterGatherCap;
 constexpr int kMaxCluster = 8;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -498,9 +498,23 @@ __global__ void __launch_bounds__(kFThreads, 1) k_sample_filtered(FilterParams p
   const unsigned long long P = p.p_units ? (unsigned long long)(uint32_t)p.p_units[r] : 0ull;
   bool kon = top_k > 0 && top_k < V;
   const bool pon = P > 0ull && P < (1ull << 24);
-  if (p.only_filtered && (it == 0.0f || (!kon && !pon))) return;  // the caller's draw stands (whole cluster)
-  cl_arrive();  // every CTA of the cluster has started before any write into its shared memory
+  if (p.only_filtered && (it == 0.0f || (!kon && !pon))) {  // the caller's draw stands (whole cluster)
+    if (p.row_ext && w.me == 0 && threadIdx.x == 0) {
+      p.row_ext[2 * r] = 0u;
+      p.row_ext[2 * r + 1] = 0u;
+    }
+    return;
+  }
+  // extremes formed by the producer of the logits (sampled rows only: greedy rows need the argmax index)
+  const bool given_ext = p.row_ext && it != 0.0f;
+  uint32_t ext_max = 0u, ext_min_inv = 0u;
+  if (given_ext) {
+    ext_max = p.row_ext[2 * r];
+    ext_min_inv = p.row_ext[2 * r + 1];
+  }
+  cl_arrive();  // every CTA has started (and read the extremes) before any write into shared memory
   const uint32_t rng[4] = {p.rng[0], p.rng[1], p.rng[2], p.rng[3]};
+  const float* keys = (p.keys && *p.keys_valid) ? p.keys : nullptr;
   const int Vc = (((V + w.C - 1) / w.C) + 3) & ~3;
   w.sl.z = z;
   w.sl.lo = w.me * Vc < V ? w.me * Vc : V;
@@ -510,44 +524,54 @@ __global__ void __launch_bounds__(kFThreads, 1) k_sample_filtered(FilterParams p
   // extremes of the finite logits of the row (order-preserving bits; with the index for greedy rows),
   // flagging non-finite ones
   unsigned long long kmax = 0ull, kmin_inv = 0ull;
-  bool bad = false;
-  if (it == 0.0f) {
-    visit(w.sl, [&](int v, float x, bool valid) {
-      if (!valid) return;
-      if (!finite(x)) {
-        bad = true;
-        return;
-      }
-      const unsigned long long k = rank_key(x, (uint32_t)v);
-      kmax = k > kmax ? k : kmax;
-    });
+  if (given_ext) {
+    kmax = (unsigned long long)ext_max << 32;
+    kmin_inv = (unsigned long long)ext_min_inv << 32;
+    cl_wait();
   } else {
-    uint32_t omax = 0u, omin_inv = 0u;
-    visit(w.sl, [&](int v, float x, bool valid) {
-      if (!valid) return;
-      if (!finite(x)) {
-        bad = true;
-        return;
-      }
-      const uint32_t o = ord_bits(x);
-      omax = o > omax ? o : omax;
-      omin_inv = ~o > omin_inv ? ~o : omin_inv;
-    });
-    kmax = (unsigned long long)omax << 32;
-    kmin_inv = (unsigned long long)omin_inv << 32;
+    bool bad = false;
+    if (it == 0.0f) {
+      visit(w.sl, [&](int v, float x, bool valid) {
+        if (!valid) return;
+        if (!finite(x)) {
+          bad = true;
+          return;
+        }
+        const unsigned long long k = rank_key(x, (uint32_t)v);
+        kmax = k > kmax ? k : kmax;
+      });
+    } else {
+      uint32_t omax = 0u, omin_inv = 0u;
+      visit(w.sl, [&](int v, float x, bool valid) {
+        if (!valid) return;
+        if (!finite(x)) {
+          bad = true;
+          return;
+        }
+        const uint32_t o = ord_bits(x);
+        omax = o > omax ? o : omax;
+        omin_inv = ~o > omin_inv ? ~o : omin_inv;
+      });
+      kmax = (unsigned long long)omax << 32;
+      kmin_inv = (unsigned long long)omin_inv << 32;
+    }
+    if (bad) set_status(p.status, ST_NAN);
+    kmax = block_reduce<true>(kmax, sh.red);
+    kmin_inv = block_reduce<true>(kmin_inv, sh.red);
+    cl_wait();
+    if (threadIdx.x < (unsigned)w.C) {
+      at_rank(w, &sh.xchg[0][0], threadIdx.x)[w.me] = kmax;
+      at_rank(w, &sh.xchg[1][0], threadIdx.x)[w.me] = kmin_inv;
+    }
+    cl_sync();
+    for (int t = 0; t < w.C; ++t) {
+      kmax = sh.xchg[0][t] > kmax ? sh.xchg[0][t] : kmax;
+      kmin_inv = sh.xchg[1][t] > kmin_inv ? sh.xchg[1][t] : kmin_inv;
+    }
   }
-  if (bad) set_status(p.status, ST_NAN);
-  kmax = block_reduce<true>(kmax, sh.red);
-  kmin_inv = block_reduce<true>(kmin_inv, sh.red);
-  cl_wait();
-  if (threadIdx.x < (unsigned)w.C) {
-    at_rank(w, &sh.xchg[0][0], threadIdx.x)[w.me] = kmax;
-    at_rank(w, &sh.xchg[1][0], threadIdx.x)[w.me] = kmin_inv;
-  }
-  cl_sync();
-  for (int t = 0; t < w.C; ++t) {
-    kmax = sh.xchg[0][t] > kmax ? sh.xchg[0][t] : kmax;
-    kmin_inv = sh.xchg[1][t] > kmin_inv ? sh.xchg[1][t] : kmin_inv;
+  if (p.row_ext && w.me == 0 && threadIdx.x == 0) {  // every CTA has read them: ready for the next step
+    p.row_ext[2 * r] = 0u;
+    p.row_ext[2 * r + 1] = 0u;
   }
   if (kmax == 0ull || it == 0.0f) {  // no finite logit / greedy: neither filter can drop the top entry
     if (w.me == 0 && threadIdx.x == 0) {
@@ -646,7 +670,8 @@ __global__ void __launch_bounds__(kFThreads, 1) k_sample_filtered(FilterParams p
         for (int i = w.me * kFThreads + threadIdx.x; i < n_keep; i += w.C * kFThreads) {
           const unsigned long long k = w.keys[i];
           const uint32_t v = ~(uint32_t)(k & 0xFFFFFFFFull);
-          const float key = sample_key(from_ord((uint32_t)(k >> 32)), it, rng, (uint32_t)r, v);
+          const float key = keys ? keys[(size_t)r * V + v]
+                                   : sample_key(from_ord((uint32_t)(k >> 32)), it, rng, (uint32_t)r, v);
           const unsigned long long pk = pack_key_index(key, v);
           best = pk > best ? pk : best;
         }
@@ -714,7 +739,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_sample_filtered(FilterParams p
     visit(w.sl, [&](int v, float x, bool valid) {
       if (!valid || !finite(x) || rank_key(x, (uint32_t)v) < threshold) return;
       ++kept;
-      const float key = sample_key(x, it, rng, (uint32_t)r, (uint32_t)v);
+      const float key = keys ? keys[(size_t)r * V + v] : sample_key(x, it, rng, (uint32_t)r, (uint32_t)v);
       const unsigned long long pk = pack_key_index(key, (uint32_t)v);
       best = pk > best ? pk : best;
     });

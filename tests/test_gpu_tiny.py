@@ -424,10 +424,13 @@ def test_async_step_gathers_the_previous_steps_ids(weights):
         b.close()
 
 
-def test_top_k_top_p_inside_eager_replayed_and_device_loop_steps(weights):
+@pytest.mark.parametrize("ks,ps", [([20, 0, 5, 1, 0], [1.0, 0.6, 0.5, 0.9, 1.0]),    # a top-p-only row: keys stored
+                                   ([20, 3, 5, 1, 0], [1.0, 0.6, 0.5, 0.9, 1.0])])   # none: keys drawn in the filter
+def test_top_k_top_p_inside_eager_replayed_and_device_loop_steps(weights, ks, ps):
     """Per-request filters in the step ("19. Fast decode", §Sampling without the CPU): eager prefill,
     graph-replayed decode and the device-resident loop; every id equals the oracle's filtered draw from the
-    step's own logits, bit for bit, rows without a filter keep the fused draw, greedy rows the argmax."""
+    step's own logits, bit for bit, rows without a filter keep the fused draw, greedy rows the argmax.  A
+    step with a top-p row that has no top-k makes the LM head store every sampling key for the filter."""
     import torch
     from graph_replayed_decode_gb300 import eng
     from graph_replayed_decode_gb300.eng import StepArrays
@@ -439,8 +442,8 @@ def test_top_k_top_p_inside_eager_replayed_and_device_loop_steps(weights):
         blocks = [list(g.alloc(oracle.blocks_needed(P + steps + 2))) for _ in range(R)]
         bt = block_table(blocks, MBS)
         temps = np.array([1.0, 1.5, 0.0, 1.2, 0.9], np.float32)
-        ks = np.array([20, 0, 5, 1, 0], np.int32)
-        ps = np.array([1.0, 0.6, 0.5, 0.9, 1.0], np.float32)       # row 4: no filter
+        ks = np.array(ks, np.int32)
+        ps = np.array(ps, np.float32)                               # row 4: no filter
         ids = np.concatenate([synth.prompt_ids(P, S.vocab, 40 + r) for r in range(R)])
         pos = np.concatenate([np.arange(P)] * R)
         cu = np.arange(R + 1) * P
