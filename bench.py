@@ -196,6 +196,33 @@ def fill_synthetic_kv(h, s, nb: int, blocks, ctxs) -> None:
     torch.cuda.synchronize()
 
 
+# ------------------------------------------------------------------ ranks (one replica per GPU)
+#
+# N GPUs run N independent replicas of the workload: no data moves between ranks. The only collective
+# work is a barrier on both sides of the timed region and the maximum of the timings over the ranks.
+
+def rank_barrier(world: int) -> None:
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+
+
+def max_over_ranks(values, world: int, device: str = "cuda") -> list[float]:
+    """Each entry's largest value over all ranks (an all-reduce with MAX); unchanged for one rank."""
+    values = [float(v) for v in values]
+    if world <= 1:
+        return values
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu().tolist()]
+
+
+def whole_job_rate(world: int, rows_per_rank: int, steps: int, seconds: float) -> float:
+    """Tokens per second of the whole job: every rank samples rows_per_rank tokens per step."""
+    return world * rows_per_rank * steps / seconds
+
+
 def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | None:
     import torch
     torch.cuda.set_device(local_rank)
@@ -203,8 +230,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     if not os.path.exists(eng.LIB_PATH):
         if rank == 0:
             build.build()
-        if world > 1:
-            torch.distributed.barrier()
+        rank_barrier(world)
     s = synth.shape(wl["shape"])
     B = wl["batch"]
     ctxs = workload_contexts(wl)
@@ -261,8 +287,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     time.sleep(0.3)
     eng.eng_decode(h, W, ring.data_ptr())                     # warm-up replays
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    rank_barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.nvtx.range_push("timed")
@@ -273,8 +298,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t_dev = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        torch.distributed.barrier()
+    rank_barrier(world)
     seq_timed = [c + 1 + W + k + 1 for c in ctxs for k in range(K)]    # keys seen by each timed step's rows
 
     # ---- per-kernel timing of one more step (CUDA events around every launch on the engine stream)
@@ -302,12 +326,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     eng.eng_destroy(h)
 
     # ---- max over ranks
-    times = np.array([t_dev, t_e2e], dtype=np.float64)
-    if world > 1:
-        tt = torch.from_numpy(times).cuda()
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        times = tt.cpu().numpy()
-    t_dev, t_e2e = float(times[0]), float(times[1])
+    t_dev, t_e2e = max_over_ranks([t_dev, t_e2e], world)
     if rank != 0:
         return None
 
@@ -330,7 +349,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     traffic = load_traffic(wl_name=args.workload, kind=dk)
     result = {
         "metric": METRIC,
-        "value": world * B * K / t_dev,
+        "value": whole_job_rate(world, B, K, t_dev),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
@@ -353,7 +372,7 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
                      "share_of_step": dms / sum(a[1] for a in agg.values()), "of": peaks["source"]},
         "kernels": {k: {"launches": v[0], "ms": round(v[1], 4), "gbs": round(v[2] / (v[1] / 1e3) / 1e9, 1)}
                     for k, v in sorted(agg.items(), key=lambda kv: -kv[1][1])},
-        "e2e": {"value": world * B * K / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": whole_job_rate(world, B, K, t_e2e), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": 4 * B},
         "gpu_launches": K * launches_per_step,
         "clocks": clk,
