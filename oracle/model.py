@@ -49,6 +49,42 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
 
 
+def widen_f16(bits: np.ndarray) -> np.ndarray:
+    """Exact value of IEEE binary16 bit patterns as float64, from the format's definition.
+
+    Sign bit 15, exponent bits 14..10 (bias 15), 10 fraction bits: a normal number is
+    (1 + f/1024) * 2^(e - 15), a subnormal (e = 0) is f/1024 * 2^-14, e = 31 is inf (f = 0) or NaN.
+    Pinned against numpy's half-precision type on all 65,536 patterns.
+    """
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where(b >> 15, -1.0, 1.0)
+    e = (b >> 10) & 31
+    f = (b & 1023).astype(np.float64)
+    normal = np.ldexp(1.0 + f / 1024.0, (e - 15).astype(np.int32))
+    sub = np.ldexp(f / 1024.0, -14)
+    special = np.where(f == 0, np.inf, np.nan)
+    return sign * np.where(e == 0, sub, np.where(e == 31, special, normal))
+
+
+F16_MAX = 65504.0
+
+
+def round_f16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest IEEE binary16 value, ties to even.
+
+    From the format's definition: at and above 2^-14 a value has 11 significant bits, so with
+    x = m * 2^e (0.5 <= |m| < 1) the significand is rint(m * 2^11) (numpy's rint rounds half to
+    even); below 2^-14 the spacing is the fixed 2^-24 of the subnormals.  Results past the largest
+    finite value (65504) are infinite.  Pinned against numpy's float64 -> float16 conversion.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    normal = np.ldexp(np.rint(np.ldexp(m, 11)), e - 11)
+    sub = np.ldexp(np.rint(np.ldexp(x, 24)), -24)
+    r = np.where(np.abs(x) >= 2.0 ** -14, normal, sub)
+    return np.where(np.abs(r) > F16_MAX, np.copysign(np.inf, x), r)
+
+
 def rms_norm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
     """RMSNorm over the last axis.
 
@@ -264,24 +300,29 @@ def attend_packed(s: ModelShape, cache, layer: int, q: np.ndarray, r: int, posit
 
 
 class OracleModel:
-    """Float64 view of bf16 weights given by Hugging Face tensor name.
+    """Float64 view of bf16 (or fp16) weights given by Hugging Face tensor name.
 
-    ``weights`` maps a name to a uint16 bf16 bit array (for example the lazy
-    ``synth`` generator).  Widened tensors are cached per layer when
+    ``weights`` maps a name to a uint16 bit array (for example the lazy
+    ``synth`` generator); ``dtype`` names the 16-bit format of those bits
+    ("bf16" or "f16").  Widened tensors are cached per layer when
     ``cache_layers`` is true; otherwise they are widened on every use, which
     keeps the memory of large shapes bounded.
     """
 
-    def __init__(self, s: ModelShape, weights, cache_layers: bool = True):
+    def __init__(self, s: ModelShape, weights, cache_layers: bool = True, dtype: str = "bf16"):
+        if dtype not in ("bf16", "f16"):
+            raise ValueError(f"dtype must be 'bf16' or 'f16', not {dtype!r}")
         self.s = s
         self.w = weights
         self.cache_layers = cache_layers
+        self.dtype = dtype
+        self._widen = widen_bf16 if dtype == "bf16" else widen_f16
         self._memo: dict[str, np.ndarray] = {}
 
     def get(self, name: str) -> np.ndarray:
         if name in self._memo:
             return self._memo[name]
-        a = widen_bf16(self.w[name])
+        a = self._widen(self.w[name])
         if self.cache_layers:
             self._memo[name] = a
         return a
@@ -330,11 +371,12 @@ def forward_step(model: OracleModel, cache, token_ids, positions, cu_seqlens, re
     projections, the attention softmax and weighted sum, the residual stream that
     accumulates every layer's output) stay in float64.  The QK-norm, RoPE and
     SiLU-and-mul act on the unrounded projection sums, as they do when fused into
-    the projection that produces them.
+    the projection that produces them.  activations="f16" is the same with IEEE
+    binary16 in place of bf16 (the fp16 variant of a model).
     """
-    if activations not in ("f64", "bf16"):
-        raise ValueError(f"activations must be 'f64' or 'bf16', not {activations!r}")
-    act = round_bf16 if activations == "bf16" else (lambda a: a)
+    if activations not in ("f64", "bf16", "f16"):
+        raise ValueError(f"activations must be 'f64', 'bf16' or 'f16', not {activations!r}")
+    act = {"bf16": round_bf16, "f16": round_f16}.get(activations, lambda a: a)
     s = model.s
     token_ids = np.asarray(token_ids, dtype=np.int64)
     positions = np.asarray(positions, dtype=np.int64)

@@ -11,6 +11,7 @@ from .inputs import (
     bf16_bits_from_f32,
     f32_from_bf16_bits,
     normal_bf16,
+    normal_f16,
     make_weights,
     weight_names,
     prompt_ids,
@@ -22,6 +23,6 @@ from .inputs import (
 
 __all__ = [
     "CONFIGS", "ModelShape", "shape", "Streams", "bf16_bits_from_f32", "f32_from_bf16_bits",
-    "normal_bf16", "make_weights", "weight_names", "prompt_ids", "decode_ids", "context_lengths", "kv_context",
+    "normal_bf16", "normal_f16", "make_weights", "weight_names", "prompt_ids", "decode_ids", "context_lengths", "kv_context",
     "mixed_chunk_prompts",
 ]

@@ -8,7 +8,9 @@ Recipe (the pages run real checkpoints; these stand in for them):
   * matrices and biases ~ N(0, 0.02), bf16: a 16-bit uniform integer indexes a
     table of bf16-rounded normal quantiles at (k + 0.5) / 65536, so the values
     follow N(0, 0.02) truncated at about 4.2 sigma, at a cost of one table
-    lookup per weight;
+    lookup per weight; with dtype "f16" the same integers index a table of
+    fp16-rounded quantiles (the fp16 variant of a shape: the same draws,
+    rounded to the other 16-bit format);
   * RMSNorm and QK-norm weights = 1.0 (N(0, 0.02) norm weights would drive
     every activation towards zero);
   * prompt ids uniform over the vocabulary;
@@ -53,14 +55,38 @@ def _quantile_table(scale: float) -> np.ndarray:
     return bf16_bits_from_f32(q.astype(np.float32))
 
 
+@functools.lru_cache(maxsize=8)
+def _quantile_table_f16(scale: float) -> np.ndarray:
+    k = np.arange(65536, dtype=np.float64)
+    q = ndtri((k + 0.5) / 65536.0) * scale
+    return q.astype(np.float16).view(np.uint16)
+
+
+def _table_indices(rng: np.random.Generator, n: int) -> np.ndarray:
+    words = rng.integers(0, 2 ** 32, size=(n + 1) // 2, dtype=np.uint32)
+    return words.view(np.uint16)[:n]
+
+
 def normal_bf16(rng: np.random.Generator, n: int, scale: float) -> np.ndarray:
     """n bf16 values ~ N(0, scale^2) (16-bit quantile table), as uint16 bits."""
-    words = rng.integers(0, 2 ** 32, size=(n + 1) // 2, dtype=np.uint32)
-    idx = words.view(np.uint16)[:n]
-    return _quantile_table(float(scale))[idx]
+    return _quantile_table(float(scale))[_table_indices(rng, n)]
+
+
+def normal_f16(rng: np.random.Generator, n: int, scale: float) -> np.ndarray:
+    """n IEEE fp16 values ~ N(0, scale^2) from the same draws as normal_bf16, as uint16 bits."""
+    return _quantile_table_f16(float(scale))[_table_indices(rng, n)]
+
+
+def _normal(dtype: str):
+    if dtype == "bf16":
+        return normal_bf16
+    if dtype == "f16":
+        return normal_f16
+    raise ValueError(f"dtype must be 'bf16' or 'f16', not {dtype!r}")
 
 
 BF16_ONE = np.uint16(0x3F80)
+F16_ONE = np.uint16(0x3C00)
 
 
 def weight_names(s: ModelShape) -> list[tuple[str, tuple[int, ...]]]:
@@ -91,15 +117,18 @@ def weight_names(s: ModelShape) -> list[tuple[str, tuple[int, ...]]]:
 
 
 class Weights:
-    """Lazily generated bf16 weights (uint16 bit arrays) keyed by tensor name.
+    """Lazily generated bf16 (or fp16) weights, uint16 bit arrays keyed by tensor name.
 
     Tensor ``i`` of ``weight_names`` is drawn from stream ``[seed, WEIGHTS, i]``,
     so any tensor can be produced alone and in any order with the same bits.
     """
 
-    def __init__(self, s: ModelShape, seed: int = 0, cache: bool = True):
+    def __init__(self, s: ModelShape, seed: int = 0, cache: bool = True, dtype: str = "bf16"):
         self.shape = s
         self.seed = seed
+        self.dtype = dtype
+        self._draw = _normal(dtype)
+        self._one = BF16_ONE if dtype == "bf16" else F16_ONE
         self._spec = weight_names(s)
         self._index = {name: i for i, (name, _) in enumerate(self._spec)}
         self._cache: dict[str, np.ndarray] | None = {} if cache else None
@@ -120,10 +149,10 @@ class Weights:
         dims = self._spec[i][1]
         n = int(np.prod(dims))
         if name.endswith("norm.weight") or name.endswith("layernorm.weight"):
-            arr = np.full(dims, BF16_ONE, dtype=np.uint16)
+            arr = np.full(dims, self._one, dtype=np.uint16)
         else:
             rng = np.random.default_rng([self.seed, Streams.WEIGHTS, i])
-            arr = normal_bf16(rng, n, 0.02).reshape(dims)
+            arr = self._draw(rng, n, 0.02).reshape(dims)
         if self._cache is not None:
             self._cache[name] = arr
         return arr
@@ -137,8 +166,8 @@ class Weights:
             self._cache.pop(name, None)
 
 
-def make_weights(s: ModelShape, seed: int = 0, cache: bool = True) -> Weights:
-    return Weights(s, seed, cache)
+def make_weights(s: ModelShape, seed: int = 0, cache: bool = True, dtype: str = "bf16") -> Weights:
+    return Weights(s, seed, cache, dtype)
 
 
 def prompt_ids(n: int, vocab: int, key: int, seed: int = 0) -> np.ndarray:
@@ -160,15 +189,16 @@ def context_lengths(n: int, choices, key: int = 0, seed: int = 0) -> np.ndarray:
     return c[rng.integers(0, len(c), size=n)].astype(np.int32)
 
 
-def kv_context(s: ModelShape, layer: int, request_key: int, ctx: int, seed: int = 0) -> np.ndarray:
-    """Synthetic cached K and V for one request and layer: uint16 bf16 bits [2, kv_heads, ctx, head_dim].
+def kv_context(s: ModelShape, layer: int, request_key: int, ctx: int, seed: int = 0,
+               dtype: str = "bf16") -> np.ndarray:
+    """Synthetic cached K and V for one request and layer: uint16 bf16 (or fp16) bits [2, kv_heads, ctx, head_dim].
 
     Position p of request ``request_key`` holds the same values whatever the
     block layout, so a paged pool and a contiguous cache can be filled alike.
     """
     rng = np.random.default_rng([seed, Streams.KV, layer, request_key])
     n = 2 * s.kv_heads * ctx * s.head_dim
-    return normal_bf16(rng, n, 1.0).reshape(2, s.kv_heads, ctx, s.head_dim)
+    return _normal(dtype)(rng, n, 1.0).reshape(2, s.kv_heads, ctx, s.head_dim)
 
 
 def mixed_chunk_prompts(budget: int = 512, choices=(16, 64, 256, 1024, 4096), key: int = 0,
