@@ -62,3 +62,28 @@ CONFIGS = {
 
 def shape(name: str) -> ModelShape:
     return CONFIGS[name]
+
+
+@dataclass(frozen=True)
+class MoeShape:
+    """One mixture-of-experts MLP: E experts of SwiGLU width `intermediate`, k experts per token."""
+    name: str
+    hidden: int
+    experts: int
+    top_k: int
+    intermediate: int
+
+    def as_dict(self) -> dict:
+        return asdict(self)
+
+
+# The pages name Qwen3-30B-A3B (128 experts); its published layer widths are hidden 2048, 8 experts per token
+# and expert width 768.  The tiny shape is for the oracle's own tests.
+MOE_CONFIGS = {
+    "tiny_moe": MoeShape("tiny_moe", hidden=64, experts=8, top_k=2, intermediate=32),
+    "qwen3_30b_a3b_moe": MoeShape("qwen3_30b_a3b_moe", hidden=2048, experts=128, top_k=8, intermediate=768),
+}
+
+
+def moe_shape(name: str) -> MoeShape:
+    return MOE_CONFIGS[name]

@@ -24,7 +24,7 @@ from typing import Iterator
 import numpy as np
 from scipy.special import ndtri
 
-from .configs import ModelShape
+from .configs import ModelShape, MoeShape
 
 
 class Streams:
@@ -34,6 +34,7 @@ class Streams:
     KV = 4
     CHUNK = 5
     DECODE_IDS = 6
+    MOE = 7
 
 
 def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
@@ -218,3 +219,22 @@ def mixed_chunk_prompts(budget: int = 512, choices=(16, 64, 256, 1024, 4096), ke
         out.append((plen, take))
         left -= take
     return out
+
+
+def moe_weights(m: MoeShape, seed: int = 0, dtype: str = "bf16") -> dict[str, np.ndarray]:
+    """One MoE layer's weights as 16-bit patterns: the router [E, D], the experts' gate|up [E, 2I, D]
+    (gate rows first, then up rows) and down [E, D, I], all ~ N(0, 0.02), one stream per tensor."""
+    draw = _normal(dtype)
+    dims = {"router": (m.experts, m.hidden), "gate_up": (m.experts, 2 * m.intermediate, m.hidden),
+            "down": (m.experts, m.hidden, m.intermediate)}
+    out = {}
+    for i, (name, d) in enumerate(dims.items()):
+        rng = np.random.default_rng([seed, Streams.MOE, i])
+        out[name] = draw(rng, int(np.prod(d)), 0.02).reshape(d)
+    return out
+
+
+def moe_tokens(n: int, hidden: int, key: int = 0, seed: int = 0, dtype: str = "bf16") -> np.ndarray:
+    """n normed token rows entering a MoE layer, ~ N(0, 1), as 16-bit patterns [n, hidden]."""
+    rng = np.random.default_rng([seed, Streams.MOE, 100 + key])
+    return _normal(dtype)(rng, n * hidden, 1.0).reshape(n, hidden)
