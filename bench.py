@@ -171,7 +171,22 @@ def oracle_decode_rate(wl: dict, budget_s: float, max_steps: int | None = None, 
             break
     tokens = done * len(rows)
     return {"value": tokens / t_meas, "steps": done, "rows": len(rows), "seconds": t_meas,
-            "cores": os.cpu_count() or 1}
+            "cores": blas_threads()}
+
+
+def blas_threads() -> int:
+    """Threads the oracle's numpy linear algebra runs on (its matrix products are where it spends its time)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads", 0) for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
 
 
 # ------------------------------------------------------------------ our arm
@@ -441,7 +456,11 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["seconds"] / max(r["steps"], 1) * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": {"workload": wl["text"] + " (CPU oracle on a bounded sample)"},
+                "data": "synthetic",
+                "config": {"workload": wl["text"], "batch": wl["batch"],
+                           "context_start": workload_contexts(wl) if wl["batch"] <= 4 else "seeded draw",
+                           "temperature": wl["temperature"],
+                           "sample": f"CPU oracle, {r['rows']} of the batch's rows per step"},
                 "cpu_baseline": {"value": r["value"], "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
                                  "sample": f"{r['steps']} timed decode steps x {r['rows']} row(s), float64 numpy"},
                 "e2e": {"value": r["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
