@@ -7,7 +7,7 @@ its own stream and any single tensor can be regenerated without the others.
 Recipe (the pages run real checkpoints; these stand in for them):
   * matrices and biases ~ N(0, 0.02), bf16: a 16-bit uniform integer indexes a
     table of bf16-rounded normal quantiles at (k + 0.5) / 65536, so the values
-    follow N(0, 0.02) truncated at about 4.2 sigma, at a cost of one table
+    follow N(0, 0.02) truncated at about 4.3 sigma, at a cost of one table
     lookup per weight; with dtype "f16" the same integers index a table of
     fp16-rounded quantiles (the fp16 variant of a shape: the same draws,
     rounded to the other 16-bit format);
