@@ -53,11 +53,12 @@ from .filters import (
     survivor_counts,
 )
 from .pool import BlockPool, PoolExhausted, blocks_needed
+from .scheduling import gather_input_ids, stop_trim
 
 __all__ = [
     "OracleModel", "ContiguousCache", "PagedCache", "widen_bf16", "round_bf16", "widen_f16", "round_f16", "rms_norm", "silu", "rope_inv_freq",
     "apply_rope", "attend_one", "attend_rows", "attend_packed", "forward_step", "fused_qkv",
     "fused_gate_up", "philox4x32_10", "uniforms", "ln_f32", "gumbel_f32", "sample", "sample_row",
     "exp_f32", "sample_filtered", "sample_row_filtered", "survivor_counts",
-    "BlockPool", "PoolExhausted", "blocks_needed",
+    "BlockPool", "PoolExhausted", "blocks_needed", "gather_input_ids", "stop_trim",
 ]

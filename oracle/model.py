@@ -13,7 +13,7 @@ SiLU, the product, the down projection and a second residual add.  The oracle
 keeps the projections separate (unfused) and computes in float64 from the
 exact float64 widening of the bf16 weights.
 
-Readings where the pages are silent (all listed in the design notes):
+Readings where the pages are silent:
   * RMSNorm: x / sqrt(mean(x^2) + eps) * w.
   * QK-norm: the same RMSNorm over each head's head_dim values with one shared
     [head_dim] weight, applied before RoPE; absent on QKV-bias models.

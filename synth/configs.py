@@ -4,7 +4,7 @@ The shapes follow the workloads the pages measure: a Qwen3-0.6B-shaped decoder
 ("19. Fast decode", §Where the time goes: 28 layers, BF16), a Qwen2.5-1.5B-shaped
 decoder ("One forward per step", setup paragraph of §What changed), an 8B-shaped
 dense decoder and a tiny two-layer test model.  Values the pages leave open are
-fixed here and listed in the design notes: eps 1e-6, RoPE theta 1e6, QK-norm on
+fixed here: eps 1e-6, RoPE theta 1e6, QK-norm on
 the Qwen3-style shapes (tiny, 0.6B, 8B), QKV bias on the Qwen2.5 shape, tied
 embeddings everywhere except the 8B shape.
 """
