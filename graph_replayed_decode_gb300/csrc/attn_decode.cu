@@ -383,11 +383,9 @@ __global__ void __launch_bounds__(128) k_attn_decode_global(AttnDecodeParams p) 
 }
 
 template <typename K>
-static cudaError_t launch_kernel(K kernel, cudaLaunchConfig_t& cfg, const AttnDecodeParams& p, bool* set) {
-  if (!*set) {
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    *set = true;
-  }
+static cudaError_t launch_kernel(K kernel, cudaLaunchConfig_t& cfg, const AttnDecodeParams& p) {
+  const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kernel), 200 * 1024);
+  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
@@ -414,12 +412,11 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, c
   attr[1].val.clusterDim.z = p.max_splits;
   cfg.attrs = attr;
   cfg.numAttrs = cluster && p.max_splits > 1 ? 2 : 1;
-  static bool c128 = false, c64 = false, g128 = false, g64 = false;
   if (cluster)
-    return p.d == 128 ? launch_kernel(k_attn_decode_cluster<128>, cfg, p, &c128)
-                      : launch_kernel(k_attn_decode_cluster<64>, cfg, p, &c64);
-  return p.d == 128 ? launch_kernel(k_attn_decode_global<128>, cfg, p, &g128)
-                    : launch_kernel(k_attn_decode_global<64>, cfg, p, &g64);
+    return p.d == 128 ? launch_kernel(k_attn_decode_cluster<128>, cfg, p)
+                      : launch_kernel(k_attn_decode_cluster<64>, cfg, p);
+  return p.d == 128 ? launch_kernel(k_attn_decode_global<128>, cfg, p)
+                    : launch_kernel(k_attn_decode_global<64>, cfg, p);
 }
 
 }  // namespace grd

@@ -218,11 +218,8 @@ cudaError_t launch_attn_prefill(const AttnPrefillParams& p, const LaunchOpts& o,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p.d == 128) {
-    static bool set = false;
-    if (!set) {
-      cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-      set = true;
-    }
+    const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k_attn_prefill<128>), 96 * 1024);
+    if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, k_attn_prefill<128>, p);
   }
   if (p.d == 64) return cudaLaunchKernelEx(&cfg, k_attn_prefill<64>, p);

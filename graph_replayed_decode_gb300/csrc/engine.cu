@@ -85,6 +85,7 @@ struct GemmSite {
 struct eng {
   eng_config_t c{};
   int device = 0;
+  int sms = 0;  // SM count of the device (grid sizing)
   cudaStream_t stream = nullptr;
   bool own_stream = false;
   cudaStream_t cap_stream = nullptr;
@@ -472,12 +473,12 @@ static int setup_buffers(eng_t* e) {
     s.tc = N % 128 == 0 && K % 64 == 0 && (rg_fixed == 0 || 128 % (16 * rg_fixed) == 0);
     if (s.tc) {  // K splits for about one CTA per SM, dividing the k-blocks of 64
       const int tiles = N / 128, nkb = K / 64;
-      int sp = std::min(8, std::max(1, (152 + tiles / 2) / tiles));
+      int sp = std::min(8, std::max(1, (e->sms + tiles / 2) / tiles));
       while (sp > 1 && (nkb % sp != 0 || sp > nkb || !tc_split_fits(sp))) --sp;
       s.tc_S = sp;
     }
-    gemm_plan(N, K, rg_fixed, &s.plan[0].RG, &s.plan[0].S, &s.plan[0].ktn);
-    gemm_plan_large(N, K, rg_fixed, &s.plan[1].RG, &s.plan[1].S, &s.plan[1].ktn);
+    gemm_plan(N, K, rg_fixed, e->sms, &s.plan[0].RG, &s.plan[0].S, &s.plan[0].ktn);
+    gemm_plan_large(N, K, rg_fixed, e->sms, &s.plan[1].RG, &s.plan[1].S, &s.plan[1].ktn);
     // mid-sized steps take the tensor cores where the warp-MMA plan's weight slice is too large to stage
     s.tc_mid = s.tc && !gemm_slice_fits(s.plan[1].RG, s.plan[1].ktn);
     return ENG_OK;
@@ -908,7 +909,9 @@ int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_w
     e->l2_prefetch = !(w && w[0] == '0');
   }
   cudaGetDevice(&e->device);
+  e->sms = device_sm_count();
   int rc = ENG_OK;
+  if (e->sms < 1) rc = fail(e, ENG_ECUDA, "cannot read the device's SM count");
   if (cuda_stream) {
     e->stream = static_cast<cudaStream_t>(cuda_stream);
   } else {
@@ -1426,9 +1429,8 @@ int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, con
                        uint64_t seed, uint64_t offset, int32_t* out_ids_dev, void* stream) {
   if (rows < 0 || vocab < 1 || (rows > 0 && (!logits_dev || !temperature || !out_ids_dev)))
     return fail(nullptr, ENG_EINVAL, "bad eng_sample_noalloc arguments");
-  const int max_rows = noalloc_max_rows();
-  if (rows > max_rows)
-    return fail(nullptr, ENG_EINVAL, "eng_sample_noalloc takes at most " + std::to_string(max_rows) +
+  if (rows > kNoAllocMaxRows)
+    return fail(nullptr, ENG_EINVAL, "eng_sample_noalloc takes at most " + std::to_string(kNoAllocMaxRows) +
                                          " rows per call (got " + std::to_string(rows) + ")");
   if (rows == 0) return ENG_OK;
   uint32_t* scratch = nullptr;
@@ -1436,24 +1438,15 @@ int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, con
   if (se != cudaSuccess)
     return fail(nullptr, ENG_ECUDA, std::string("cudaGetSymbolAddress of the sampler scratch failed: ") +
                                         cudaGetErrorString(se));
-  // [inverse temperatures][seed_lo, seed_hi, offset_lo, offset_hi]: every word is rewritten by each call
-  uint32_t words[4096 + 4];
+  std::vector<float> inv_temp((size_t)rows);  // host memory only: the staging kernel's parameters carry it
   for (int r = 0; r < rows; ++r) {
     if (!(temperature[r] >= 0.f) || !std::isfinite(temperature[r]))
       return fail(nullptr, ENG_EINVAL, "temperature must be finite and >= 0");
-    const float it = inv_temperature(temperature[r]);
-    memcpy(&words[r], &it, 4);
+    inv_temp[r] = inv_temperature(temperature[r]);
   }
-  words[rows + 0] = (uint32_t)seed;
-  words[rows + 1] = (uint32_t)(seed >> 32);
-  words[rows + 2] = (uint32_t)offset;
-  words[rows + 3] = (uint32_t)(offset >> 32);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // pageable source: the call returns once the words are staged, so the stack buffer may go away
-  cudaError_t r = cudaMemcpyAsync(scratch, words, (size_t)(rows + 4) * 4, cudaMemcpyHostToDevice, st);
-  if (r == cudaSuccess)
-    r = launch_sample(logits_dev, rows, vocab, reinterpret_cast<const float*>(scratch), scratch + rows, nullptr,
-                      out_ids_dev, nullptr, st);
+  const uint32_t rng[4] = {(uint32_t)seed, (uint32_t)(seed >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)};
+  const cudaError_t r = launch_sample_noalloc(logits_dev, rows, vocab, inv_temp.data(), rng, scratch, out_ids_dev,
+                                              static_cast<cudaStream_t>(stream));
   if (r != cudaSuccess) return fail(nullptr, ENG_ECUDA, std::string("eng_sample_noalloc: ") + cudaGetErrorString(r));
   return ENG_OK;
 }

@@ -765,14 +765,14 @@ __global__ void __launch_bounds__(256, 1) k_gemm_tc(GemmParams p, const __grid_c
 
 static constexpr int kMaxCluster = 8;
 
-void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split) {
+void gemm_plan(int N, int K, int rg_fixed, int sms, int* RG, int* S, int* kt_per_split) {
   // Every round trip after the kernel's wait costs about a microsecond, and so does a cluster reduction,
   // so the plan first looks for the fewest K splits whose per-CTA weight slice still fits the shared-memory
   // budget of the bulk copy (the slice is then fetched before the wait), with at most one wave of CTAs at
   // one CTA per SM (the other half of the SM stays free for the next kernel's early CTAs); among those it
   // takes the most CTAs.  When no slice fits, it takes the most CTAs in one wave (ties: fewer splits).
   const int tiles = N / 16, KT = K / 32;
-  const int wave = 152;
+  const int wave = sms;
   int best_rg = 0, best_s = 0, best_ctas = 0;
   for (int sp = 1; sp <= kMaxCluster && sp <= KT && best_ctas == 0; ++sp) {
     if (KT % sp) continue;
@@ -812,14 +812,14 @@ void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split) {
   *kt_per_split = KT / best_s;
 }
 
-void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split) {
+void gemm_plan_large(int N, int K, int rg_fixed, int sms, int* RG, int* S, int* kt_per_split) {
   // Steps of more than 8 tokens: every CTA also reads its K-range of the activation planes for each token
   // (T x K-range x 4 bytes from L2), which at 32 tokens outweighs a thin weight slice.  The plan minimises
   // the bytes one SM moves, waves x (2 W + X) with W the CTA's weight slice (from HBM, counted twice) and X
   // its activation slice for 32 tokens, over row groups of 1..8 tiles and 1..8 K splits in at most two
   // waves (ties: fewer CTAs, then fewer splits).  Falls back to the small-step plan when nothing fits.
   const int tiles = N / 16, KT = K / 32;
-  const int wave = 152;
+  const int wave = sms;
   double best = 0.0;
   int best_rg = 0, best_s = 0, best_ctas = 0;
   for (int rg = 1; rg <= 8; rg <<= 1) {
@@ -839,7 +839,7 @@ void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_sp
     }
   }
   if (best_ctas == 0) {
-    gemm_plan(N, K, rg_fixed, RG, S, kt_per_split);
+    gemm_plan(N, K, rg_fixed, sms, RG, S, kt_per_split);
     return;
   }
   *RG = best_rg;
@@ -850,14 +850,12 @@ void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_sp
 template <int NT, int EPI, bool NORM_IN, bool TC>
 static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, dim3 grid, const TcMaps* tm) {
   const size_t smem_bytes = TC ? tc_smem(p.S) : gemm_smem(NT, p.RG, p.kt_per_split, p.S).total;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if constexpr (TC)
-      cudaFuncSetAttribute(k_gemm_tc<EPI, NORM_IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
-    else
-      cudaFuncSetAttribute(k_gemm<NT, EPI, NORM_IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
-    attr_set = true;
-  }
+  cudaError_t ae;
+  if constexpr (TC)
+    ae = ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<EPI, NORM_IN>), (int)kSmemBudget);
+  else
+    ae = ensure_smem_limit(reinterpret_cast<const void*>(k_gemm<NT, EPI, NORM_IN>), (int)kSmemBudget);
+  if (ae != cudaSuccess) return ae;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(256);

@@ -12,6 +12,12 @@ namespace grd {
 
 typedef __nv_bfloat16 bf16;
 
+// SM count of the current device (looked up once per device; 0 when it cannot be read).
+int device_sm_count();
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per (device, kernel):
+// the attribute belongs to the device's context, so each GPU a process uses gets its own call.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
 // Launch options shared by all launchers: programmatic dependent launch on/off.
 struct LaunchOpts {
   bool pdl = false;
@@ -125,10 +131,11 @@ static constexpr int kTcTokens = 9;
 static constexpr int kTcPrefillTokens = 65;
 
 // Picks RG / S / kt_per_split for an [N][K] weight (independent of T, so every token count computes
-// each output with the same summation order).  rg_fixed > 0 forces the rows per CTA (whole heads).
-void gemm_plan(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split);
+// each output with the same summation order).  rg_fixed > 0 forces the rows per CTA (whole heads); sms is
+// the device's SM count (one wave of CTAs).
+void gemm_plan(int N, int K, int rg_fixed, int sms, int* RG, int* S, int* kt_per_split);
 // The plan for steps of more than 8 tokens (activation bytes per CTA weigh in; see gemm.cu).
-void gemm_plan_large(int N, int K, int rg_fixed, int* RG, int* S, int* kt_per_split);
+void gemm_plan_large(int N, int K, int rg_fixed, int sms, int* RG, int* S, int* kt_per_split);
 // Token count from which a step uses the large plans.
 static constexpr int kLargePlanTokens = 9;
 // tc: the tensor maps of the tcgen05 path (then RG must be 8, S 1, no x_rows; N % 128 == 0, K % 64 == 0),
@@ -222,8 +229,16 @@ cudaError_t launch_sample_filtered(const FilterParams& p, int rows, cudaStream_t
 // producer of the logits); rows past it (and top-p without top-k) draw over a pass of the whole row.
 constexpr int kFilterGatherCap = 8192;
 cudaError_t launch_exp_rn(const float* d, float* out, int64_t n, cudaStream_t s);
-// Fixed device array for eng_sample_noalloc: [inverse temperatures of up to noalloc_max_rows() rows][4 words].
-int noalloc_max_rows();
+// eng_sample_noalloc: the sampler with its per-call words (the rows' inverse temperatures, then seed_lo,
+// seed_hi, offset_lo, offset_hi) in a fixed device array of this library (sample.cu) instead of an
+// allocation.  The words reach the array as the parameters of a staging kernel, so the call reads no host
+// memory after it returns.  At most kNoAllocMaxRows rows: 16 KiB of inverse temperatures.
+constexpr int kNoAllocMaxRows = 4096;
+static_assert(kNoAllocMaxRows * sizeof(float) == 16 * 1024, "the array holds 16 KiB of inverse temperatures");
+// Device address of the array on the current device (looked up once per device, with that device current).
 cudaError_t noalloc_scratch(uint32_t** out);
+// Stages inv_temp[rows] and rng[4] into the array at `scratch`, then runs the sampler over the logits.
+cudaError_t launch_sample_noalloc(const float* logits, int rows, int vocab, const float* inv_temp_host,
+                                  const uint32_t rng_host[4], uint32_t* scratch, int* out_ids, cudaStream_t s);
 
 }  // namespace grd

@@ -2,6 +2,7 @@
 // Gumbel transform and the greedy / Gumbel-max argmax over caller-provided logits.  The fused LM-head
 // epilogue (gemm.cu) uses the same device functions, so these launches let tests compare the GPU's
 // noise and log bit for bit with a CPU restatement.
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -89,17 +90,27 @@ cudaError_t launch_sample(const float* logits, int rows, int vocab, const float*
 // allocates.  The variant below keeps that block in a fixed array linked into this library instead, for
 // callers that are not allowed to allocate device memory.  Every GPU that loads the library holds the
 // array (kNoAllocMaxRows + 4 words) until the process exits, and every call on that GPU shares it.
+// The words reach the array as the parameters of a one-CTA staging kernel (launch parameters are copied
+// when the launch is enqueued), so the call never reads host memory after it returns.
 
 namespace grd {
 
-static constexpr int kNoAllocMaxRows = 4096;
 static constexpr int kMaxDevices = 64;
 static __device__ __align__(256) uint32_t g_sample_scratch[kNoAllocMaxRows + 4];
 
-int noalloc_max_rows() { return kNoAllocMaxRows; }
+struct NoAllocWords {
+  uint32_t n;                          // words in use: rows + 4
+  uint32_t w[kNoAllocMaxRows + 4];     // inverse temperatures (float bits), then seed_lo, seed_hi, offset_lo, offset_hi
+};
+static_assert(sizeof(NoAllocWords) < 32000, "kernel parameters are limited to 32 KB");
+
+__global__ void __launch_bounds__(256) k_noalloc_stage(const __grid_constant__ NoAllocWords p, uint32_t* dst) {
+  for (uint32_t i = threadIdx.x; i < p.n; i += blockDim.x) dst[i] = p.w[i];
+}
 
 // Device address of g_sample_scratch for the current device, looked up once per device.  In host code the
-// array's name is only a host-side handle, so the address must come from cudaGetSymbolAddress.
+// array's name is only a host-side handle, so the address must come from cudaGetSymbolAddress.  The cached
+// address belongs to the device's current context: after cudaDeviceReset it is no longer valid.
 cudaError_t noalloc_scratch(uint32_t** out) {
   static std::mutex mu;
   static uint32_t* addr[kMaxDevices] = {};
@@ -116,6 +127,21 @@ cudaError_t noalloc_scratch(uint32_t** out) {
   }
   *out = addr[dev];
   return cudaSuccess;
+}
+
+cudaError_t launch_sample_noalloc(const float* logits, int rows, int vocab, const float* inv_temp_host,
+                                  const uint32_t rng_host[4], uint32_t* scratch, int* out_ids, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (rows > kNoAllocMaxRows || !scratch) return cudaErrorInvalidValue;
+  NoAllocWords w;
+  w.n = (uint32_t)rows + 4;
+  memcpy(w.w, inv_temp_host, (size_t)rows * 4);
+  for (int i = 0; i < 4; ++i) w.w[rows + i] = rng_host[i];
+  k_noalloc_stage<<<1, 256, 0, s>>>(w, scratch);
+  cudaError_t r = cudaGetLastError();
+  if (r != cudaSuccess) return r;
+  return launch_sample(logits, rows, vocab, reinterpret_cast<const float*>(scratch), scratch + rows, nullptr, out_ids,
+                       nullptr, s);
 }
 
 }  // namespace grd

@@ -765,22 +765,18 @@ __global__ void __launch_bounds__(kFThreads, 1) k_sample_filtered(FilterParams p
 
 constexpr size_t kFilterSmem = (size_t)kBuckets * 24 + (size_t)kGatherCap * 8;
 
-// Cluster size for `rows` rows: enough CTAs per row to cover the SMs, at most kMaxCluster.
+// Cluster size for `rows` rows: enough CTAs per row to cover the device's SMs, at most kMaxCluster.
 static int filter_cluster(int rows) {
+  const int sms = device_sm_count();
   int C = 1;
-  while (C < kMaxCluster && rows * C * 2 <= 152) C <<= 1;
+  while (C < kMaxCluster && rows * C * 2 <= sms) C <<= 1;
   return C;
 }
 
 cudaError_t launch_sample_filtered(const FilterParams& p, int rows, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  static bool attr_set = false;  // the attribute is per function, set once per process
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(k_sample_filtered, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFilterSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k_sample_filtered), (int)kFilterSmem);
+  if (e != cudaSuccess) return e;
   const int C = filter_cluster(rows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, rows, 1);

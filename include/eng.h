@@ -338,13 +338,15 @@ int eng_sample(const float* logits_dev, int32_t rows, int32_t vocab, const float
  * latency-critical loop that cannot take an allocation's implicit synchronisation.
  * Arguments, results and errors are those of eng_sample, with rows <= 4096 (ENG_EINVAL beyond that,
  * with a message).  The per-call scratch (the rows' inverse temperatures and the four Philox words) lives
- * in one fixed 16 KiB array inside this library; every GPU that loads the library holds it until the
- * process exits.  The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.  All calls on a device share
- * the array, and each call rewrites every word it reads, so nothing carries over between calls -- but
- * calls whose work overlaps on the GPU (for example on two unordered streams) race on it.  The call copies
- * from pageable memory, so it returns after the copy into the array has been staged; synchronise the
- * stream before reading out_ids_dev.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ * in one fixed array of 16 KiB + 16 bytes inside this library; every GPU that loads the library holds it
+ * until the process exits.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and keeps it; make that first call before any stream
+ * capture.  The kept address is not valid after cudaDeviceReset.  All calls on a device share the array,
+ * and each call rewrites every word it reads, so nothing carries over between calls -- but calls whose
+ * work overlaps on the GPU (for example on two unordered streams) race on it.  The words reach the array
+ * as the launch parameters of a small staging kernel on `stream`, so the call neither synchronises nor
+ * reads host memory after it returns; synchronise the stream before reading out_ids_dev.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
  */
 int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature,
                        uint64_t seed, uint64_t offset, int32_t* out_ids_dev, void* stream);

@@ -12,7 +12,10 @@ Recipe (the pages run real checkpoints; these stand in for them):
     fp16-rounded quantiles (the fp16 variant of a shape: the same draws,
     rounded to the other 16-bit format);
   * RMSNorm and QK-norm weights = 1.0 (N(0, 0.02) norm weights would drive
-    every activation towards zero);
+    every activation towards zero); with ``norm_scale`` > 0 they are instead
+    bf16 draws of 1 + N(0, norm_scale^2) from the tensor's own stream (the same
+    quantile-table method), so that every norm weight differs from its
+    neighbours and from the other norms' weights;
   * prompt ids uniform over the vocabulary;
   * pre-filled context K/V ~ N(0, 1), bf16, by the same table method.
 """
@@ -54,6 +57,20 @@ def _quantile_table(scale: float) -> np.ndarray:
     k = np.arange(65536, dtype=np.float64)
     q = ndtri((k + 0.5) / 65536.0) * scale
     return bf16_bits_from_f32(q.astype(np.float32))
+
+
+@functools.lru_cache(maxsize=8)
+def _quantile_table_shifted(scale: float, shift: float) -> np.ndarray:
+    k = np.arange(65536, dtype=np.float64)
+    q = shift + ndtri((k + 0.5) / 65536.0) * scale
+    return bf16_bits_from_f32(q.astype(np.float32))
+
+
+@functools.lru_cache(maxsize=8)
+def _quantile_table_f16_shifted(scale: float, shift: float) -> np.ndarray:
+    k = np.arange(65536, dtype=np.float64)
+    q = shift + ndtri((k + 0.5) / 65536.0) * scale
+    return q.astype(np.float16).view(np.uint16)
 
 
 @functools.lru_cache(maxsize=8)
@@ -122,12 +139,17 @@ class Weights:
 
     Tensor ``i`` of ``weight_names`` is drawn from stream ``[seed, WEIGHTS, i]``,
     so any tensor can be produced alone and in any order with the same bits.
+    Norm weights are 1.0, or with ``norm_scale`` > 0 draws of 1 + N(0, norm_scale^2).
     """
 
-    def __init__(self, s: ModelShape, seed: int = 0, cache: bool = True, dtype: str = "bf16"):
+    def __init__(self, s: ModelShape, seed: int = 0, cache: bool = True, dtype: str = "bf16",
+                 norm_scale: float = 0.0):
+        if not norm_scale >= 0.0:
+            raise ValueError("norm_scale must be >= 0")
         self.shape = s
         self.seed = seed
         self.dtype = dtype
+        self.norm_scale = float(norm_scale)
         self._draw = _normal(dtype)
         self._one = BF16_ONE if dtype == "bf16" else F16_ONE
         self._spec = weight_names(s)
@@ -150,7 +172,13 @@ class Weights:
         dims = self._spec[i][1]
         n = int(np.prod(dims))
         if name.endswith("norm.weight") or name.endswith("layernorm.weight"):
-            arr = np.full(dims, self._one, dtype=np.uint16)
+            if self.norm_scale == 0.0:
+                arr = np.full(dims, self._one, dtype=np.uint16)
+            else:
+                rng = np.random.default_rng([self.seed, Streams.WEIGHTS, i])
+                table = (_quantile_table_shifted if self.dtype == "bf16" else _quantile_table_f16_shifted)(
+                    self.norm_scale, 1.0)
+                arr = table[_table_indices(rng, n)].reshape(dims)
         else:
             rng = np.random.default_rng([self.seed, Streams.WEIGHTS, i])
             arr = self._draw(rng, n, 0.02).reshape(dims)
@@ -167,8 +195,9 @@ class Weights:
             self._cache.pop(name, None)
 
 
-def make_weights(s: ModelShape, seed: int = 0, cache: bool = True, dtype: str = "bf16") -> Weights:
-    return Weights(s, seed, cache, dtype)
+def make_weights(s: ModelShape, seed: int = 0, cache: bool = True, dtype: str = "bf16",
+                 norm_scale: float = 0.0) -> Weights:
+    return Weights(s, seed, cache, dtype, norm_scale)
 
 
 def prompt_ids(n: int, vocab: int, key: int, seed: int = 0) -> np.ndarray:

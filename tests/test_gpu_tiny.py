@@ -3,6 +3,11 @@
 Workload: 4 requests with 16-token uniform-random prompts, block size 16, one packed prefill step followed
 by 15 pure-decode steps (16 sampled tokens per request), greedy; and the same with Gumbel-max sampling.
 Both sides consume the GPU's sampled ids (teacher forcing).
+
+The weights' RMSNorm and QK-norm vectors are bf16 draws of 1 + N(0, 0.1^2), different for every norm and
+layer, so that each norm-weight multiply fused into a projection's prologue or epilogue is checked (and the
+order of QK-norm and RoPE, which unit weights cannot tell apart); one case keeps the unit weights of the
+benchmark's recipe.
 """
 import numpy as np
 import pytest
@@ -22,6 +27,11 @@ NB, MBS = 64, 8
 def weights():
     import torch
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return synth.make_weights(S, seed=0, norm_scale=0.1)
+
+
+@pytest.fixture(scope="module")
+def unit_norm_weights():
     return synth.make_weights(S, seed=0)
 
 
@@ -80,6 +90,11 @@ def run_tiny(weights, temps, capture=True, steps=16, seed=5):
 
 def test_tiny_greedy_prefill_then_graph_decode(weights):
     errs = run_tiny(weights, [0.0] * 4)
+    assert max(errs) <= 3e-2
+
+
+def test_tiny_greedy_unit_norm_weights(unit_norm_weights):
+    errs = run_tiny(unit_norm_weights, [0.0] * 4, steps=6)
     assert max(errs) <= 3e-2
 
 
@@ -354,7 +369,8 @@ def test_async_step_gathers_the_previous_steps_ids(weights):
     step sampled.  Two engines run the same steps, one with the ids read back on the host (eng_step), one
     with placeholders and a row map (eng_step_async): ids and logits agree bit for bit, in a replayed decode
     step, in a mixed step (a new prompt chunk plus gathered decode rows), and in a device-resident step
-    after an async one."""
+    after an async one.  The oracle's gather rule ("33. Removing overhead", §Async scheduling) gives the
+    ids each async step reads, and its forward on those ids matches the async engine's logits and ids."""
     import torch
     from graph_replayed_decode_gb300 import eng
     from graph_replayed_decode_gb300.eng import StepArrays
@@ -370,10 +386,15 @@ def test_async_step_gathers_the_previous_steps_ids(weights):
         ids = np.concatenate([synth.prompt_ids(n, S.vocab, 60 + r) for r, n in enumerate(lens)])
         pos = np.concatenate([np.arange(n) for n in lens])
         cu = np.concatenate([[0], np.cumsum(lens)])
+        model = oracle.OracleModel(S, weights)
+        cache = oracle.PagedCache(S, NB)
+        for r, blk in enumerate(blocks):
+            cache.set_block_table(r, blk)
         st1 = StepArrays(ids, pos, cu, bt[:3], np.array(lens), temps, seed=4, offset=0)
         ia, _ = a.step(st1)
-        ib, _ = b.step(st1)
+        ib, lb = b.step(st1)
         np.testing.assert_array_equal(ia, ib)
+        check_logits_and_ids(lb, ib, oracle.forward_step(model, cache, ids, pos, cu), temps, 4, 0)
         # decode step: explicit ids on engine a, placeholders (invalid ids, ignored) gathered on engine b
         p2 = np.array(lens)
         ia2, la2 = a.step(StepArrays(ia, p2, np.arange(4), bt[:3], p2 + 1, temps, seed=4, offset=1))
@@ -382,6 +403,9 @@ def test_async_step_gathers_the_previous_steps_ids(weights):
         assert b.info().replayed == 1
         np.testing.assert_array_equal(ia2, ib2)
         np.testing.assert_array_equal(la2.view(np.uint32), lb2.view(np.uint32))
+        g2 = oracle.gather_input_ids(np.full(3, -5), [0, 1, 2], ib)
+        np.testing.assert_array_equal(g2, ia)
+        check_logits_and_ids(lb2, ib2, oracle.forward_step(model, cache, g2, p2, np.arange(4)), temps, 4, 1)
         # mixed step: a new 5-token prompt chunk (explicit ids) first, then the three decode rows; row 1's id
         # given explicitly, rows 0 and 2 gathered from the previous step's rows 0 and 2
         newp = synth.prompt_ids(5, S.vocab, 70)
@@ -398,6 +422,10 @@ def test_async_step_gathers_the_previous_steps_ids(weights):
         ib3, lb3 = b.step_async(StepArrays(ids_b, pos3, cu3, bt3, seq3, t3, seed=4, offset=2), prev)
         np.testing.assert_array_equal(ia3, ib3)
         np.testing.assert_array_equal(la3.view(np.uint32), lb3.view(np.uint32))
+        g3 = oracle.gather_input_ids(ids_b, prev, ib2)
+        np.testing.assert_array_equal(g3, ids_a)
+        check_logits_and_ids(lb3, ib3, oracle.forward_step(model, cache, g3, pos3, cu3, request_keys=[3, 0, 1, 2]),
+                             t3, 4, 2)
         # an async decode step, then the device-resident loop continues the batch on both engines
         p4 = p3 + 1
         a.step(StepArrays(ia3[1:], p4, np.arange(4), bt[:3], p4 + 1, temps, seed=4, offset=3))
@@ -492,9 +520,10 @@ def test_filters_need_an_engine_created_for_them(weights):
 
 
 def test_generate_checks_stop_ids_once_per_group(weights):
-    """eng_generate ("19. Fast decode": stop tokens checked every check_every steps, one sync per check,
-    tokens after a stop trimmed) against eng_decode on an identical engine: the same tokens, each length at
-    the request's first stop id, and the steps run end at the first group boundary where all have stopped."""
+    """eng_generate ("19. Fast decode", §Host synchronizations: stop tokens checked every check_every steps,
+    one sync per check, tokens after a stop trimmed) against the oracle's stop rule applied to the tokens
+    eng_decode samples on an identical engine: the same tokens, each length at the request's first stop id,
+    and the steps run end at the first group boundary where all have stopped."""
     import torch
     from graph_replayed_decode_gb300 import eng
     from graph_replayed_decode_gb300.eng import StepArrays
@@ -520,6 +549,10 @@ def test_generate_checks_stop_ids_once_per_group(weights):
         stops = sorted({int(full[0, 5]), int(full[1, 13])})
         first = [next((k + 1 for k in range(steps) if full[r, k] in stops), None) for r in range(R)]
         toks, lens, n = eng.eng_generate(a.h, R, steps, group, stops)
+        want_toks, want_lens, want_n = oracle.stop_trim(full, stops, group, steps)
+        assert n == want_n
+        np.testing.assert_array_equal(lens, want_lens)
+        np.testing.assert_array_equal(toks, want_toks)
         assert n == (steps if None in first else min(steps, -(-max(first) // group) * group))
         for r in range(R):
             L = first[r] if first[r] is not None else n

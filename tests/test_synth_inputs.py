@@ -1,7 +1,7 @@
-"""The synthetic input recipe: seeded, deterministic, and distributed as the design notes state.
+"""The synthetic input recipe: seeded, deterministic, and distributed as follows.
 
 Weights ~ N(0, 0.02) in bf16 (a normal truncated at 4.32 sigma by the 16-bit quantile table), norm
-weights 1.0, ids uniform over the vocabulary, context lengths drawn from the stated set, prompt chunks
+weights 1.0 (or bf16 draws of 1 + N(0, sigma^2) when asked for), ids uniform over the vocabulary, context lengths drawn from the stated set, prompt chunks
 filled first-come-first-served up to the budget with only the last prompt cut, context K/V ~ N(0, 1).
 """
 import numpy as np
@@ -71,3 +71,26 @@ def test_context_kv_is_standard_normal_bf16():
     assert abs(x.mean()) < 0.01 and abs(x.std() - 1.0) < 0.01
     np.testing.assert_array_equal(kv, synth.kv_context(s, layer=3, request_key=7, ctx=300))
     assert not np.array_equal(kv, synth.kv_context(s, layer=4, request_key=7, ctx=300))
+
+
+def test_random_norm_weights_are_one_plus_normal_draws():
+    s = synth.shape("tiny")
+    w = synth.make_weights(s, seed=0, norm_scale=0.1)
+    names = ["model.norm.weight", "model.layers.0.input_layernorm.weight",
+             "model.layers.0.post_attention_layernorm.weight", "model.layers.1.input_layernorm.weight",
+             "model.layers.0.self_attn.q_norm.weight", "model.layers.0.self_attn.k_norm.weight"]
+    vals = [_bf16(w[n]) for n in names]
+    for n, x in zip(names, vals):
+        np.testing.assert_array_equal(synth.bf16_bits_from_f32(x.astype(np.float32)), w[n])   # bf16-exact
+        assert len(np.unique(x)) > x.size // 4                      # the entries differ from one another
+    for i in range(len(vals)):
+        for j in range(i + 1, len(vals)):
+            if vals[i].shape == vals[j].shape:
+                assert not np.array_equal(vals[i], vals[j])          # and from the other norms' weights
+    big = np.concatenate([_bf16(synth.make_weights(synth.shape("qwen3_0p6b"), norm_scale=0.1)[
+        f"model.layers.{l}.input_layernorm.weight"]) for l in range(8)])
+    assert abs(big.mean() - 1.0) < 0.01 and abs(big.std() - 0.1) < 0.01
+    assert stats.kstest((big[::3] - 1.0) / 0.1, "norm").pvalue > 1e-3
+    # the matrices are the same draws as with unit norms
+    np.testing.assert_array_equal(w["model.layers.0.mlp.down_proj.weight"],
+                                  synth.make_weights(s, seed=0)["model.layers.0.mlp.down_proj.weight"])

@@ -4,15 +4,23 @@ Some callers cannot allocate device memory while they run -- a serving runtime t
 device memory to its own pool, or a latency-critical loop that cannot afford an allocation's implicit
 synchronisation.  eng_sample_noalloc keeps its per-call scratch in a fixed array inside the library.  This
 file checks, through the C ABI, that it returns exactly the ids of eng_sample (which allocates its scratch
-per call) on two calls in a row, so the shared array's leftovers from one call cannot leak into the next,
+per call) on two calls in a row, so the shared array's leftovers from one call cannot leak into the next;
+that one call's ids equal the CPU oracle's sampler on the same Philox uniforms; that the calls change
+neither the device's default memory pool, nor torch's caching allocator, nor the device's free memory;
 and that it rejects more rows than its array holds.  It sits last in collection order on purpose.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
+import oracle
 from harness import ensure_built
 
 pytestmark = pytest.mark.gpu
+
+_RESERVED_MEM_CURRENT = 5   # CUmemPool_attribute values (cuda.h)
+_USED_MEM_CURRENT = 7
 
 
 @pytest.fixture(scope="module")
@@ -23,23 +31,69 @@ def torch_cuda():
     return torch
 
 
-def test_noalloc_sampler_matches_eng_sample_on_two_calls(torch_cuda):
-    from graph_replayed_decode_gb300 import eng
-    torch = torch_cuda
+class _DeviceMemory:
+    """The device's default memory pool counters and free memory, through the driver API."""
+
+    def __init__(self, device: int):
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        dev = ctypes.c_int()
+        assert self.cu.cuDeviceGet(ctypes.byref(dev), device) == 0
+        self.pool = ctypes.c_void_p()
+        assert self.cu.cuDeviceGetDefaultMemPool(ctypes.byref(self.pool), dev) == 0
+
+    def snapshot(self) -> dict:
+        out = {}
+        for name, attr in (("pool_reserved", _RESERVED_MEM_CURRENT), ("pool_used", _USED_MEM_CURRENT)):
+            v = ctypes.c_uint64()
+            assert self.cu.cuMemPoolGetAttribute(self.pool, attr, ctypes.byref(v)) == 0
+            out[name] = v.value
+        free, total = ctypes.c_size_t(), ctypes.c_size_t()
+        assert self.cu.cuMemGetInfo_v2(ctypes.byref(free), ctypes.byref(total)) == 0
+        out["device_free"] = free.value
+        return out
+
+
+def _calls(torch):
     rng = np.random.default_rng(11)
-    calls = [
+    out = []
+    for rows, vocab, temps, seed, offset in [
         (9, 151936, np.array([0.7, 1.0, 0.0, 0.8, 1e-3, 2.0, 0.0, 1.3, 0.5], dtype=np.float32), 0, 0),
         (5, 4096, np.array([0.0, 1.0, 0.0, 0.9, 3.0], dtype=np.float32), 77, 123456789),
-    ]
-    for rows, vocab, temps, seed, offset in calls:          # two calls in a row share the fixed array
-        z = torch.from_numpy((rng.standard_normal((rows, vocab)) * 3).astype(np.float32)).cuda()
+    ]:
+        z = (rng.standard_normal((rows, vocab)) * 3).astype(np.float32)
+        out.append((rows, vocab, temps, seed, offset, z, torch.from_numpy(z).cuda()))
+    return out
+
+
+def test_noalloc_sampler_matches_eng_sample_and_the_oracle_on_two_calls(torch_cuda):
+    from graph_replayed_decode_gb300 import eng
+    torch = torch_cuda
+    calls = _calls(torch)
+    # the first call on this device looks up the array's address and loads the kernels; the measured calls
+    # below are the ones that must leave every allocator untouched
+    warm = torch.zeros(16, dtype=torch.int32, device="cuda")
+    eng.eng_sample_noalloc(calls[1][6].data_ptr(), 1, calls[1][1], calls[1][2][:1], 0, 0, warm.data_ptr())
+    outs = [torch.full((c[0],), -7, dtype=torch.int32, device="cuda") for c in calls]
+    torch.cuda.synchronize()
+    mem = _DeviceMemory(torch.cuda.current_device())
+    before = mem.snapshot()
+    torch_reserved = torch.cuda.memory_reserved()
+    for (rows, vocab, temps, seed, offset, _, zd), got in zip(calls, outs):   # two calls share the array
+        eng.eng_sample_noalloc(zd.data_ptr(), rows, vocab, temps, seed, offset, got.data_ptr())
+    torch.cuda.synchronize()
+    assert mem.snapshot() == before
+    assert torch.cuda.memory_reserved() == torch_reserved
+    for (rows, vocab, temps, seed, offset, z, zd), got in zip(calls, outs):
         want = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
-        got = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
-        eng.eng_sample(z.data_ptr(), rows, vocab, temps, seed, offset, want.data_ptr())
-        eng.eng_sample_noalloc(z.data_ptr(), rows, vocab, temps, seed, offset, got.data_ptr())
+        eng.eng_sample(zd.data_ptr(), rows, vocab, temps, seed, offset, want.data_ptr())
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(got.cpu().numpy(), want.cpu().numpy())
-        assert (got.cpu().numpy() >= 0).all()
+        ids = got.cpu().numpy()
+        np.testing.assert_array_equal(ids, want.cpu().numpy())
+        assert (ids >= 0).all()
+    rows, vocab, temps, seed, offset, z, _ = calls[0]
+    ids = outs[0].cpu().numpy()
+    for r in range(rows):                        # the CPU sampler on the same Philox uniforms
+        assert ids[r] == oracle.sample_row(z[r], float(temps[r]), seed, offset, r), r
 
 
 def test_noalloc_sampler_rejects_rows_beyond_its_array(torch_cuda):
