@@ -141,6 +141,18 @@ struct eng {
   int* ring = nullptr;  // [ring_cap][bucket] ids recorded by the advance kernel
   int ring_cap = 1024;
 
+  // persistent decode step (decode_step.cu): decode-only steps of at most ds_rows tokens
+  bool ds_on = false;
+  int ds_rows = 0, ds_slots = 0, ds_kx = 0, ds_ablk = 0, ds_splits = 0;
+  size_t ds_smem = 0;
+  DsLayer* ds_layers = nullptr;  // device [layers]
+  unsigned long long *ds_h = nullptr, *ds_qkv = nullptr, *ds_act = nullptr;
+  CUtensorMap ds_kv_map{};  // the KV pool as [rows][head_dim] bf16 for the kernel's swizzled block copies
+  unsigned long long* ds_ws = nullptr;
+  unsigned int* ds_epoch = nullptr;
+  int* ds_diag = nullptr;  // [4] the first wait of the persistent kernel that gave up (site, block, thread, layer)
+  std::map<int, std::pair<int*, int*>> ds_sched;  // token count -> device (ranges, items)
+
   // the decode batch that eng_decode continues (host mirror of its lengths)
   int dec_R = 0, dec_rows = 0, dec_bt_stride = 0;
   int prev_rows = 0;  // requests of the last step (rows an async step may gather sampled ids from)
@@ -512,6 +524,72 @@ static int setup_buffers(eng_t* e) {
   return ENG_OK;
 }
 
+// ------------------------------------------------------------------ persistent decode step set-up
+
+// Decides whether decode-only steps of a few tokens run on the persistent kernel (decode_step.cu) and
+// allocates its buffers.  The kernel stages its input rows in shared memory, so the token count it takes
+// is the largest power of two (at most 8) whose rows of the widest projection input fit 50 KB; it needs
+// one CTA per SM, all resident together (a cooperative launch).  It is taken only with ENG_DECODE_KERNEL=1
+// in the environment when the engine is created: until it beats the per-layer kernels, decode steps run on
+// those by default.
+static int setup_decode_step(eng_t* e) {
+  const eng_config_t& c = e->c;
+  const char* v = getenv("ENG_DECODE_KERNEL");
+  if (!v || v[0] != '1') return ENG_OK;
+  const int d = c.head_dim, G = c.q_heads / c.kv_heads;
+  if (c.layers > 50 || G > 8 || (d != 64 && d != 128)) return ENG_OK;
+  const int kx = std::max({c.hidden, c.q_heads * d, c.intermediate}) + 8;
+  const size_t stage_cap = 50 * 1024;
+  int rows = 8;
+  while (rows > 1 && ((size_t)4 * rows * kx > stage_cap || rows > c.max_reqs)) rows >>= 1;
+  if ((size_t)4 * rows * kx > stage_cap) return ENG_OK;
+  int slots = 5;
+  size_t smem = decode_step_smem(slots, rows, kx, d, c.layers);
+  while (slots > 2 && smem > 227 * 1024) smem = decode_step_smem(--slots, rows, kx, d, c.layers);
+  if (smem > 227 * 1024) return ENG_OK;
+  int coop = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, e->device) != cudaSuccess || !coop) return ENG_OK;
+  if (decode_step_prepare(smem, &per_sm) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    return ENG_OK;
+  }
+  // attention: splits of whole ring chunks, at most kDsMaxSplits per (row, KV head)
+  const int bpc = kDsSlotBytes / (2 * 16 * d * 2);
+  const int cpi = (c.max_blocks_per_seq + bpc * kDsMaxSplits - 1) / (bpc * kDsMaxSplits);
+  e->ds_ablk = bpc * cpi;
+  e->ds_splits = (c.max_blocks_per_seq + e->ds_ablk - 1) / e->ds_ablk;
+  const uint64_t kv_rows = (uint64_t)c.layers * 2 * (c.num_blocks + 1) * c.kv_heads * 16;
+  if (kv_rows >= (1ull << 31) || !make_tc_map(&e->ds_kv_map, e->kv, kv_rows, d, 16)) return ENG_OK;
+  e->ds_rows = rows;
+  e->ds_kx = kx;
+  e->ds_slots = slots;
+  e->ds_smem = smem;
+  const int QKV = (c.q_heads + 2 * c.kv_heads) * d;
+  TRY(dev_alloc(e, &e->ds_h, (size_t)rows * c.hidden));
+  TRY(dev_alloc(e, &e->ds_qkv, (size_t)rows * QKV));
+  TRY(dev_alloc(e, &e->ds_act, (size_t)rows * c.intermediate));
+  TRY(dev_alloc(e, &e->ds_ws, (size_t)rows * c.kv_heads * e->ds_splits * G * (d + 2)));
+  TRY(dev_alloc(e, &e->ds_epoch, 2));
+  TRY(dev_alloc(e, &e->ds_diag, 4 + 4 * (size_t)e->sms));
+  const unsigned int ep[2] = {1u, 0u};  // tags start above the zero-filled buffers' tag 0
+  CUDA_OR_FAIL(e, cudaMemcpy(e->ds_epoch, ep, sizeof(ep), cudaMemcpyHostToDevice));
+  TRY(dev_alloc(e, &e->ds_layers, (size_t)c.layers));
+  e->ds_on = true;
+  return ENG_OK;
+}
+
+// The persistent kernel's table of per-layer weight pointers (after the weights are loaded).
+static int fill_decode_layers(eng_t* e) {
+  if (!e->ds_on) return ENG_OK;
+  std::vector<DsLayer> v(e->layers.size());
+  for (size_t l = 0; l < v.size(); ++l) {
+    const Layer& L = e->layers[l];
+    v[l] = DsLayer{L.qkv, L.o, L.gu, L.down, L.qkv_bias, L.q_norm, L.k_norm, L.in_norm, L.post_norm};
+  }
+  CUDA_OR_FAIL(e, cudaMemcpy(e->ds_layers, v.data(), v.size() * sizeof(DsLayer), cudaMemcpyHostToDevice));
+  return ENG_OK;
+}
+
 // ------------------------------------------------------------------ the step's kernel sequence
 
 // Event pair around one launch when eng_profile is collecting (no-op otherwise).
@@ -604,6 +682,69 @@ static cudaError_t gemm_launch(eng_t* e, const GemmParams& p, const GemmSite& s,
   return r;
 }
 
+static cudaError_t enqueue_tail(eng_t* e, int T, int R, int sq_parts, bool advance, cudaStream_t st);
+
+// True when a step runs on the persistent decode kernel: decode-only (every request one token) with at
+// most ds_rows tokens.  Only the token count decides, so an eager step and its padded bucket take the same
+// path whenever ds_rows is a capture size.
+static bool ds_applies(const eng_t* e, int T, int R, int P) { return e->ds_on && P == 0 && T == R && T <= e->ds_rows; }
+
+// The persistent kernel's schedule for T tokens, built on first use: every CTA's items of each phase,
+// handed out largest first to the CTA with the fewest bytes so far (weights of a tile, or the K/V of a
+// full attention split), so that every SM streams about the same share of the layer.
+static int ds_schedule(eng_t* e, int T, int** d_off, int** d_items) {
+  auto it = e->ds_sched.find(T);
+  if (it != e->ds_sched.end()) {
+    *d_off = it->second.first;
+    *d_items = it->second.second;
+    return ENG_OK;
+  }
+  const eng_config_t& c = e->c;
+  const int grid = e->sms, d = c.head_dim;
+  std::vector<std::vector<int>> lists((size_t)grid * DS_PHASES);
+  std::vector<int64_t> load(grid, 0);
+  auto assign = [&](int phase, int count, int64_t bytes) {
+    for (int i = 0; i < count; ++i) {
+      int best = 0;
+      for (int k = 1; k < grid; ++k)
+        if (load[k] < load[best]) best = k;
+      load[best] += bytes;
+      lists[(size_t)best * DS_PHASES + phase].push_back(i);
+    }
+  };
+  const int64_t kv_item = (int64_t)e->ds_ablk * 16 * d * 2 * 2;
+  assign(DS_DOWN, c.hidden / 16, (int64_t)c.intermediate / 32 * 1024);
+  assign(DS_O, c.hidden / 16, (int64_t)c.q_heads * d / 32 * 1024);
+  assign(DS_GU, 2 * c.intermediate / 16, (int64_t)c.hidden / 32 * 1024);
+  assign(DS_QKV, (c.q_heads + 2 * c.kv_heads) * d / 16, (int64_t)c.hidden / 32 * 1024);
+  assign(DS_ATTN, T * c.kv_heads * e->ds_splits, kv_item);
+  std::vector<int> off((size_t)grid * (DS_PHASES + 1)), items;
+  const int S = e->ds_splits;
+  for (int b = 0; b < grid; ++b) {
+    const size_t first = items.size();
+    for (int ph = 0; ph < DS_PHASES; ++ph) {
+      off[(size_t)b * (DS_PHASES + 1) + ph] = (int)items.size();
+      auto& l = lists[(size_t)b * DS_PHASES + ph];
+      if (ph == DS_ATTN)  // split 0 merges a row's splits: a CTA runs its splits in descending order
+        std::sort(l.begin(), l.end(), [S](int x, int y) { return x % S != y % S ? x % S > y % S : x < y; });
+      else
+        std::sort(l.begin(), l.end());
+      items.insert(items.end(), l.begin(), l.end());
+      off[(size_t)b * (DS_PHASES + 1) + ph + 1] = (int)items.size();
+    }
+    if (items.size() - first > (size_t)kDsMaxItems) return fail(e, ENG_EINVAL, "decode step schedule too long");
+  }
+  int *o = nullptr, *itm = nullptr;
+  TRY(dev_alloc(e, &o, off.size()));
+  TRY(dev_alloc(e, &itm, items.size()));
+  CUDA_OR_FAIL(e, cudaMemcpy(o, off.data(), off.size() * 4, cudaMemcpyHostToDevice));
+  CUDA_OR_FAIL(e, cudaMemcpy(itm, items.data(), items.size() * 4, cudaMemcpyHostToDevice));
+  e->ds_sched[T] = {o, itm};
+  *d_off = o;
+  *d_items = itm;
+  return ENG_OK;
+}
+
 // Enqueues one forward over T packed tokens of R requests; requests [0, P) go to the packed prefill
 // kernel (n_items work items), [P, R) to the decode kernel with `splits` splits per row.  With
 // `advance`, a decode-only step ends by feeding its sampled ids back as the next inputs (advance.cu).
@@ -620,6 +761,67 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
   LaunchOpts o;
   o.pdl = e->pdl;
   cudaError_t r;
+
+  if (ds_applies(e, T, R, P)) {
+    int* d_off = nullptr;
+    int* d_items = nullptr;
+    if (ds_schedule(e, T, &d_off, &d_items) != ENG_OK) return cudaErrorInvalidValue;
+    DecodeStepParams dp{};
+    dp.kv_map = e->ds_kv_map;
+    dp.L = c.layers;
+    dp.H = H;
+    dp.Hq = Hq;
+    dp.Hkv = Hkv;
+    dp.d = d;
+    dp.I = c.intermediate;
+    dp.V = c.vocab;
+    dp.NB = c.num_blocks;
+    dp.mbs = c.max_blocks_per_seq;
+    dp.max_pos = e->max_pos;
+    dp.eps = c.rms_eps;
+    dp.scale_log2 = 1.4426950408889634f / sqrtf((float)d);
+    dp.layers = e->ds_layers;
+    dp.embed = e->embed;
+    dp.final_norm = e->final_norm;
+    dp.rope = e->rope;
+    dp.kv = e->kv;
+    dp.T = T;
+    dp.ids = in + e->in.ids;
+    dp.prev_row = in + e->in.prev;
+    dp.prev_ids = e->ids;
+    dp.prev_rows = c.max_reqs;
+    dp.pos = in + e->in.pos;
+    dp.seq = in + e->in.seq;
+    dp.bt = in + e->in.bt;
+    dp.sched_off = d_off;
+    dp.sched_items = d_items;
+    dp.ablk = e->ds_ablk;
+    dp.asplits = e->ds_splits;
+    dp.trows = e->ds_rows;
+    dp.kx = e->ds_kx;
+    dp.slots_n = e->ds_slots;
+    dp.h_ll = e->ds_h;
+    dp.qkv_ll = e->ds_qkv;
+    dp.act_ll = e->ds_act;
+    dp.attn_ws = e->ds_ws;
+    dp.epoch = e->ds_epoch;
+    dp.xn_h = e->xn_h;
+    dp.xn_l = e->xn_l;
+    dp.sq = e->sq;
+    dp.sq_stride = e->sq_stride;
+    dp.h_out = e->h;
+    dp.slots = e->slots;
+    dp.status = e->status;
+    dp.diag = e->ds_diag;
+    int64_t wbytes = 0;
+    for (const GemmSite* g : {&e->g_qkv, &e->g_o, &e->g_gu, &e->g_down}) wbytes += (int64_t)g->N * g->K * 2;
+    e->launches++;
+    prof_begin(e, st, ENG_K_DECODE_LAYERS, wbytes * c.layers + kv_read * c.layers + (int64_t)T * kv_tok * c.layers);
+    r = launch_decode_step(dp, e->sms, e->ds_smem, st);
+    prof_end(e, st);
+    if (r != cudaSuccess) return r;
+    return enqueue_tail(e, T, R, 1, advance, st);
+  }
 
   EmbedParams ep{};
   ep.embed = e->embed;
@@ -778,6 +980,18 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     sq_parts = e->g_down.groups(T);
   }
 
+  return enqueue_tail(e, T, R, sq_parts, advance, st);
+}
+
+// The end of a step: final RMSNorm at each request's last token, LM head and sampling, the optional
+// top-k / top-p redraw, and for a device-resident decode loop the in-place advance of the inputs.
+static cudaError_t enqueue_tail(eng_t* e, int T, int R, int sq_parts, bool advance, cudaStream_t st) {
+  (void)T;
+  const eng_config_t& c = e->c;
+  int* in = e->d_in;
+  LaunchOpts o;
+  o.pdl = e->pdl;
+  cudaError_t r;
   // ---- final RMSNorm at each request's last token + LM head + sampling
   GemmParams pl = gemm_params(e, e->g_lm, e->lm, R);
   pl.Xh = e->xn_h;
@@ -920,7 +1134,9 @@ int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_w
   }
   if (rc == ENG_OK && cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking) != cudaSuccess) rc = ENG_ECUDA;
   if (rc == ENG_OK) rc = setup_buffers(e);
+  if (rc == ENG_OK) rc = setup_decode_step(e);
   if (rc == ENG_OK) rc = load_weights(e, weights, n_weights);
+  if (rc == ENG_OK) rc = fill_decode_layers(e);
   if (rc == ENG_OK && cudaDeviceSynchronize() != cudaSuccess) rc = fail(e, ENG_ECUDA, "device error after load");
   if (rc != ENG_OK) {
     g_create_error = e->err.empty() ? g_create_error : e->err;
@@ -976,6 +1192,10 @@ int eng_debug_buffer(eng_t* e, const char* name, void** dev_ptr, int64_t* bytes)
   } else if (n == "logits") {
     *dev_ptr = e->logits;
     *bytes = (int64_t)c.max_reqs * c.vocab * 4;
+  } else if (n == "decode_diag") {
+    if (!e->ds_diag) return fail(e, ENG_EINVAL, "the engine has no persistent decode kernel");
+    *dev_ptr = e->ds_diag;
+    *bytes = 16 + 16 * (int64_t)e->sms;
   } else if (n == "ids") {
     *dev_ptr = e->ids;
     *bytes = (int64_t)c.max_reqs * 4;

@@ -241,4 +241,74 @@ cudaError_t noalloc_scratch(uint32_t** out);
 cudaError_t launch_sample_noalloc(const float* logits, int rows, int vocab, const float* inv_temp_host,
                                   const uint32_t rng_host[4], uint32_t* scratch, int* out_ids, cudaStream_t s);
 
+
+// ------------------------------------------------------------------ persistent decode step (decode_step.cu)
+// Every layer of a decode-only step of at most a few tokens in one cooperative launch: one CTA per SM, a
+// static per-CTA list of work items per layer and phase (QKV tiles, attention splits, o_proj tiles,
+// gate|up tiles, down tiles), weights and K/V streamed into a shared-memory ring ahead of need, and
+// activations handed between phases as tagged 64-bit words (value bits | tag << 32).
+struct DsLayer {
+  const bf16* qkv;  // packed [(Hq + 2 Hkv) d][H]
+  const bf16* o;    // packed [H][Hq d]
+  const bf16* gu;   // packed [2I][H], gate/up rows interleaved per 16-row tile
+  const bf16* down; // packed [H][I]
+  const float* qkv_bias;  // or null
+  const float* q_norm;    // or null
+  const float* k_norm;
+  const float* in_norm;
+  const float* post_norm;
+};
+enum DsPhase { DS_QKV = 0, DS_ATTN = 1, DS_O = 2, DS_GU = 3, DS_DOWN = 4, DS_PHASES = 5 };
+struct DecodeStepParams {
+  CUtensorMap kv_map;     // the KV pool as rows of head_dim bf16 ([L][2][NB + 1][Hkv][16] rows), 64 x 16 boxes,
+                          // 128-byte swizzle: K/V blocks land in shared memory in a bank-conflict-free order
+  int L, H, Hq, Hkv, d, I, V, NB, mbs, max_pos;
+  float eps, scale_log2;
+  const DsLayer* layers;  // device [L]
+  const bf16* embed;      // packed [V][H]
+  const float* final_norm;
+  const float* rope;      // [max_pos][d/2][2]
+  bf16* kv;               // [L][2][NB + 1][Hkv][16][d]
+  int T;                  // rows of the step (one token each)
+  const int* ids;
+  const int* prev_row;
+  const int* prev_ids;
+  int prev_rows;
+  const int* pos;
+  const int* seq;
+  const int* bt;          // [rows][mbs]
+  const int* sched_off;   // [gridDim.x][DS_PHASES + 1]: item ranges of each CTA's phases
+  const int* sched_items;
+  int ablk;               // attention: KV blocks per split
+  int asplits;            // splits per (row, KV head), at most kDsMaxSplits
+  int trows;              // rows of the activation staging planes (>= T)
+  int kx;                 // row stride of the staging planes (elements)
+  int slots_n;            // ring slots of 32 KB
+  unsigned long long* h_ll;    // [trows][H]
+  unsigned long long* qkv_ll;  // [trows][(Hq + 2 Hkv) d]
+  unsigned long long* act_ll;  // [trows][I]
+  unsigned long long* attn_ws;  // [trows][Hkv][asplits][G][d + 2]: each split's (O, max, sum), merged by the
+                                //   output projection's staging
+  unsigned int* epoch;    // [0]: this step's epoch (tags), [1]: epoch of a step given up after a timeout
+  bf16* xn_h;             // outputs for the LM head: planes of h * final_norm [T][H]
+  bf16* xn_l;
+  float* sq;              //   per-token sum of squares of h (one part)
+  int sq_stride;
+  float* h_out;           //   the final residual [T][H]
+  int* slots;             //   [T] KV slot of each token (-1 padding)
+  int* status;
+  int* diag;              // [4]: the first wait that gave up -- site (DsWaitSite), block, thread, layer
+};
+// Where a wait of the persistent decode kernel gave up (recorded in DecodeStepParams::diag).
+enum DsWaitSite { WAIT_RING_FULL = 1, WAIT_RING_EMPTY = 2, WAIT_STAGE = 3, WAIT_HEAD = 4, WAIT_ATTN_STATS = 5,
+                  WAIT_ATTN_OUT = 6, WAIT_RESIDUAL = 7 };
+// Ring slot size, and the shared memory a launch needs for `trows` staged rows of width kmax.
+constexpr int kDsSlotBytes = 32 * 1024;
+constexpr int kDsMaxItems = 256;  // work items of one CTA per layer (all phases)
+constexpr int kDsMaxSplits = 4;   // attention key splits per (row, KV head)
+size_t decode_step_smem(int slots_n, int trows, int kx, int d, int layers);
+// The kernel's shared-memory limit is raised on first use; false if the device cannot host the grid.
+cudaError_t decode_step_prepare(size_t smem, int* max_ctas_per_sm);
+cudaError_t launch_decode_step(const DecodeStepParams& p, int grid, size_t smem, cudaStream_t s);
+
 }  // namespace grd

@@ -244,7 +244,7 @@ def eng_decode(e, n_steps: int, out_ids_dev: int) -> None:
 
 
 KERNEL_KINDS = ["embed_norm", "norm", "gemm_qkv", "rope_kv", "attn_decode", "attn_prefill", "gemm_o",
-                "gemm_gate_up", "gemm_down", "lm_head", "advance", "sample_filter"]
+                "gemm_gate_up", "gemm_down", "lm_head", "advance", "sample_filter", "decode_layers"]
 
 
 def eng_profile(e, capacity: int = 4096):

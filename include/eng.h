@@ -241,6 +241,7 @@ int eng_generate(eng_t* e, int32_t max_steps, int32_t check_every, const int32_t
 #define ENG_K_LM_HEAD 9
 #define ENG_K_ADVANCE 10
 #define ENG_K_SAMPLE_FILTER 11
+#define ENG_K_DECODE_LAYERS 12 /* every layer of a small decode-only step in one persistent kernel */
 
 /*
  * eng_profile -- time every kernel of one further decode step of the current batch (as eng_decode with

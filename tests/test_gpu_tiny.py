@@ -35,8 +35,21 @@ def unit_norm_weights():
     return synth.make_weights(S, seed=0)
 
 
-def _engine(weights, stream=None):
-    return GpuEngine(S, weights, num_blocks=NB, max_reqs=8, max_tokens=128, max_blocks_per_seq=MBS, stream=stream)
+def _engine(weights, stream=None, decode_kernel=True, num_blocks=NB, mbs=MBS):
+    """An engine over the tiny shape.  decode_kernel=True runs small decode-only steps on the persistent decode
+    kernel (ENG_DECODE_KERNEL=1 when the engine is created; the engine's default is the per-layer kernels),
+    so that most tests here cover it; decode_kernel=False keeps them on the per-layer kernels."""
+    import os
+    old = os.environ.get("ENG_DECODE_KERNEL")
+    os.environ["ENG_DECODE_KERNEL"] = "1" if decode_kernel else "0"
+    try:
+        return GpuEngine(S, weights, num_blocks=num_blocks, max_reqs=8, max_tokens=128, max_blocks_per_seq=mbs,
+                         stream=stream)
+    finally:
+        if old is None:
+            del os.environ["ENG_DECODE_KERNEL"]
+        else:
+            os.environ["ENG_DECODE_KERNEL"] = old
 
 
 def run_tiny(weights, temps, capture=True, steps=16, seed=5):
@@ -297,7 +310,7 @@ def test_device_decode_loop_equals_host_driven_steps(weights):
         np.testing.assert_array_equal(dev, np.stack(host))
         prof = eng.eng_profile(g.h)
         kinds = [k for k, _, _ in prof]
-        assert kinds.count("attn_decode") == S.layers and kinds[-1] == "advance" and kinds[-2] == "lm_head"
+        assert kinds == ["decode_layers", "lm_head", "advance"]   # the persistent kernel runs every layer
         assert all(ms > 0 for _, ms, _ in prof)
         with pytest.raises(eng.EngError) as ei:          # past the block tables' capacity
             eng.eng_decode(g.h, 200, ring.data_ptr())
@@ -310,9 +323,10 @@ def test_device_decode_loop_equals_host_driven_steps(weights):
 def test_attention_merge_modes_agree_bit_for_bit(weights):
     """Decode rows whose attention splits merge on chip (a batch of 4 rows) and through the global
     workspace (the same rows plus two more) give bit-identical logits: a row's result does not depend on
-    the merge path nor on the other rows of the batch."""
+    the merge path nor on the other rows of the batch.  (Per-layer kernels: small decode steps otherwise
+    run on the persistent decode kernel.)"""
     from graph_replayed_decode_gb300.eng import StepArrays
-    g = _engine(weights)
+    g = _engine(weights, decode_kernel=False)
     try:
         ctxs = [100, 37, 64, 17, 90, 50]                      # 2..7 blocks: several splits per row
         blocks = [list(g.alloc(oracle.blocks_needed(c + 1))) for c in ctxs]
@@ -330,6 +344,73 @@ def test_attention_merge_modes_agree_bit_for_bit(weights):
         assert g.status() == 0
     finally:
         g.close()
+
+
+def test_persistent_decode_kernel_matches_oracle_and_per_layer_kernels(weights):
+    """The persistent decode kernel (every layer of a decode step of up to 8 tokens in one launch) against
+    the oracle, on rows whose contexts span up to five attention splits (so the split merge runs) and a
+    row of one block; the per-layer kernels on the same inputs land within the same bar.  Eager (3 rows)
+    and replayed (bucket 4, one padding row) steps agree bit for bit, and the device loop continues them."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    from graph_replayed_decode_gb300.eng import StepArrays
+    mbs, nb = 48, 160
+    ctxs = [600, 37, 250]
+    engines = [_engine(weights, decode_kernel=k, num_blocks=nb, mbs=mbs) for k in (True, False)]
+    try:
+        blocks = None
+        for g in engines:
+            b = [list(g.alloc(oracle.blocks_needed(c + 4))) for c in ctxs]
+            assert blocks is None or b == blocks
+            blocks = b
+            for l in range(S.layers):
+                for r, c in enumerate(ctxs):
+                    g.fill_context(l, blocks[r], synth.kv_context(S, l, 300 + r, c))
+        bt = block_table(blocks, mbs)
+        model = oracle.OracleModel(S, weights)
+        cache = oracle.ContiguousCache(S, {r: c + 4 for r, c in enumerate(ctxs)})
+        for l in range(S.layers):
+            for r, c in enumerate(ctxs):
+                kv = synth.kv_context(S, l, 300 + r, c)
+                cache.keys[(l, r)][:, :c, :] = oracle.widen_bf16(kv[0])
+                cache.values[(l, r)][:, :c, :] = oracle.widen_bf16(kv[1])
+        ids = synth.decode_ids(3, S.vocab, 5)
+        pos = np.array(ctxs)
+        temps = np.array([0.0, 0.9, 1.3], dtype=np.float32)
+        st = StepArrays(ids, pos, np.arange(4), bt, pos + 1, temps, seed=2, offset=0)
+        fast, slow = engines
+        f_ids, f_log = fast.step(st)                               # eager, persistent kernel
+        assert fast.info().launches == 3                           # the kernel, the LM head, the advance
+        s_ids, s_log = slow.step(st)                               # eager, per-layer kernels
+        assert slow.info().launches > 2 * S.layers
+        olog = oracle.forward_step(model, cache, ids, pos, np.arange(4))
+        check_logits_and_ids(f_log, f_ids, olog, temps, 2, 0)
+        check_logits_and_ids(s_log, s_ids, olog, temps, 2, 0)
+        # the same step replayed in bucket 4 (one padding row) is bit-identical to the eager one
+        for g in engines:
+            g.capture([4, 8])
+        r_ids, r_log = fast.step(st)
+        assert fast.info().replayed == 1 and fast.info().bucket == 4
+        np.testing.assert_array_equal(r_ids, f_ids)
+        np.testing.assert_array_equal(r_log.view(np.uint32), f_log.view(np.uint32))
+        # two more steps on the device, checked against the oracle
+        ring = torch.zeros((2, 3), dtype=torch.int32, device="cuda")
+        eng.eng_decode(fast.h, 2, ring.data_ptr())
+        torch.cuda.synchronize()
+        cur, p = f_ids.copy(), pos + 1
+        for k in range(2):
+            z = oracle.forward_step(model, cache, cur, p, np.arange(4))
+            want = oracle.sample(z.astype(np.float32), temps, 2, k + 1)
+            got = ring[k].cpu().numpy()
+            for r in range(3):
+                srt = np.sort(z[r])
+                if temps[r] == 0.0 and srt[-1] - srt[-2] > 0.1:
+                    assert got[r] == want[r]
+            cur, p = got.copy(), p + 1
+        assert fast.status() == 0 and slow.status() == 0
+    finally:
+        for g in engines:
+            g.close()
 
 
 def test_tensor_core_prefill_chunks(weights):
