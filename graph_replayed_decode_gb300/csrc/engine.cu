@@ -143,12 +143,12 @@ struct eng {
 
   // persistent decode step (decode_step.cu): decode-only steps of at most ds_rows tokens
   bool ds_on = false;
-  int ds_rows = 0, ds_slots = 0, ds_kx = 0, ds_ablk = 0, ds_splits = 0;
+  int ds_rows = 0, ds_slots = 0, ds_kx = 0;
   size_t ds_smem = 0;
   DsLayer* ds_layers = nullptr;  // device [layers]
   unsigned long long *ds_h = nullptr, *ds_qkv = nullptr, *ds_act = nullptr;
   CUtensorMap ds_kv_map{};  // the KV pool as [rows][head_dim] bf16 for the kernel's swizzled block copies
-  unsigned long long* ds_ws = nullptr;
+  unsigned long long *ds_ws = nullptr, *ds_out = nullptr;
   unsigned int* ds_epoch = nullptr;
   int* ds_diag = nullptr;  // [4] the first wait of the persistent kernel that gave up (site, block, thread, layer)
   std::map<int, std::pair<int*, int*>> ds_sched;  // token count -> device (ranges, items)
@@ -537,15 +537,15 @@ static int setup_decode_step(eng_t* e) {
   const char* v = getenv("ENG_DECODE_KERNEL");
   if (!v || v[0] != '1') return ENG_OK;
   const int d = c.head_dim, G = c.q_heads / c.kv_heads;
-  if (c.layers > 50 || G > 8 || (d != 64 && d != 128)) return ENG_OK;
+  if (c.layers > 50 || G > 8 || c.kv_heads > 255 || (d != 64 && d != 128)) return ENG_OK;
   const int kx = std::max({c.hidden, c.q_heads * d, c.intermediate}) + 8;
   const size_t stage_cap = 50 * 1024;
   int rows = 8;
   while (rows > 1 && ((size_t)4 * rows * kx > stage_cap || rows > c.max_reqs)) rows >>= 1;
   if ((size_t)4 * rows * kx > stage_cap) return ENG_OK;
   int slots = 5;
-  size_t smem = decode_step_smem(slots, rows, kx, d, c.layers);
-  while (slots > 2 && smem > 227 * 1024) smem = decode_step_smem(--slots, rows, kx, d, c.layers);
+  size_t smem = decode_step_smem(slots, rows, kx, d, G, c.hidden, c.layers);
+  while (slots > 2 && smem > 227 * 1024) smem = decode_step_smem(--slots, rows, kx, d, G, c.hidden, c.layers);
   if (smem > 227 * 1024) return ENG_OK;
   int coop = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, e->device) != cudaSuccess || !coop) return ENG_OK;
@@ -553,11 +553,6 @@ static int setup_decode_step(eng_t* e) {
     cudaGetLastError();
     return ENG_OK;
   }
-  // attention: splits of whole ring chunks, at most kDsMaxSplits per (row, KV head)
-  const int bpc = kDsSlotBytes / (2 * 16 * d * 2);
-  const int cpi = (c.max_blocks_per_seq + bpc * kDsMaxSplits - 1) / (bpc * kDsMaxSplits);
-  e->ds_ablk = bpc * cpi;
-  e->ds_splits = (c.max_blocks_per_seq + e->ds_ablk - 1) / e->ds_ablk;
   const uint64_t kv_rows = (uint64_t)c.layers * 2 * (c.num_blocks + 1) * c.kv_heads * 16;
   if (kv_rows >= (1ull << 31) || !make_tc_map(&e->ds_kv_map, e->kv, kv_rows, d, 16)) return ENG_OK;
   e->ds_rows = rows;
@@ -568,7 +563,8 @@ static int setup_decode_step(eng_t* e) {
   TRY(dev_alloc(e, &e->ds_h, (size_t)rows * c.hidden));
   TRY(dev_alloc(e, &e->ds_qkv, (size_t)rows * QKV));
   TRY(dev_alloc(e, &e->ds_act, (size_t)rows * c.intermediate));
-  TRY(dev_alloc(e, &e->ds_ws, (size_t)rows * c.kv_heads * e->ds_splits * G * (d + 2)));
+  TRY(dev_alloc(e, &e->ds_ws, (size_t)rows * c.kv_heads * kDsMaxSplits * G * (d + 2)));
+  TRY(dev_alloc(e, &e->ds_out, (size_t)rows * c.q_heads * d));
   TRY(dev_alloc(e, &e->ds_epoch, 2));
   TRY(dev_alloc(e, &e->ds_diag, 4 + 4 * (size_t)e->sms));
   const unsigned int ep[2] = {1u, 0u};  // tags start above the zero-filled buffers' tag 0
@@ -582,10 +578,15 @@ static int setup_decode_step(eng_t* e) {
 static int fill_decode_layers(eng_t* e) {
   if (!e->ds_on) return ENG_OK;
   std::vector<DsLayer> v(e->layers.size());
+  // the kernel copies norm weights to shared memory in 16-byte pieces (each tensor is its own allocation)
+  auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
   for (size_t l = 0; l < v.size(); ++l) {
     const Layer& L = e->layers[l];
     v[l] = DsLayer{L.qkv, L.o, L.gu, L.down, L.qkv_bias, L.q_norm, L.k_norm, L.in_norm, L.post_norm};
+    if (!a16(L.q_norm) || !a16(L.k_norm) || !a16(L.in_norm) || !a16(L.post_norm))
+      return fail(e, ENG_EINVAL, "decode step: norm weights must be 16-byte aligned");
   }
+  if (!a16(e->final_norm) || !a16(e->rope)) return fail(e, ENG_EINVAL, "decode step: misaligned table");
   CUDA_OR_FAIL(e, cudaMemcpy(e->ds_layers, v.data(), v.size() * sizeof(DsLayer), cudaMemcpyHostToDevice));
   return ENG_OK;
 }
@@ -692,6 +693,13 @@ static bool ds_applies(const eng_t* e, int T, int R, int P) { return e->ds_on &&
 // The persistent kernel's schedule for T tokens, built on first use: every CTA's items of each phase,
 // handed out largest first to the CTA with the fewest bytes so far (weights of a tile, or the K/V of a
 // full attention split), so that every SM streams about the same share of the layer.
+// Attention splits per (row, KV head) of a T-row step: enough items for one per SM, at most kDsMaxSplits.
+// A row's last split merges the others, which it waits for; a CTA running several attention items takes
+// them in item order, where a row's last split comes after the row's other splits.
+static int ds_splits(const eng_t* e, int T) {
+  return std::max(1, std::min(kDsMaxSplits, e->sms / (T * e->c.kv_heads)));
+}
+
 static int ds_schedule(eng_t* e, int T, int** d_off, int** d_items) {
   auto it = e->ds_sched.find(T);
   if (it != e->ds_sched.end()) {
@@ -712,23 +720,26 @@ static int ds_schedule(eng_t* e, int T, int** d_off, int** d_items) {
       lists[(size_t)best * DS_PHASES + phase].push_back(i);
     }
   };
-  const int64_t kv_item = (int64_t)e->ds_ablk * 16 * d * 2 * 2;
+  const int64_t kv_item = kDsSlotBytes;  // about one ring chunk of keys per attention split
   assign(DS_DOWN, c.hidden / 16, (int64_t)c.intermediate / 32 * 1024);
   assign(DS_O, c.hidden / 16, (int64_t)c.q_heads * d / 32 * 1024);
   assign(DS_GU, 2 * c.intermediate / 16, (int64_t)c.hidden / 32 * 1024);
   assign(DS_QKV, (c.q_heads + 2 * c.kv_heads) * d / 16, (int64_t)c.hidden / 32 * 1024);
-  assign(DS_ATTN, T * c.kv_heads * e->ds_splits, kv_item);
+  assign(DS_ATTN, T * c.kv_heads * ds_splits(e, T), kv_item);
+  // attention items as (row << 16) | (KV head << 8) | split (the kernel decodes them with shifts)
+  const int ns = ds_splits(e, T);
+  for (int b = 0; b < grid; ++b)
+    for (int& it : lists[(size_t)b * DS_PHASES + DS_ATTN]) {
+      const int sp = it % ns, rg = it / ns;
+      it = ((rg / c.kv_heads) << 16) | ((rg % c.kv_heads) << 8) | sp;
+    }
   std::vector<int> off((size_t)grid * (DS_PHASES + 1)), items;
-  const int S = e->ds_splits;
   for (int b = 0; b < grid; ++b) {
     const size_t first = items.size();
     for (int ph = 0; ph < DS_PHASES; ++ph) {
       off[(size_t)b * (DS_PHASES + 1) + ph] = (int)items.size();
       auto& l = lists[(size_t)b * DS_PHASES + ph];
-      if (ph == DS_ATTN)  // split 0 merges a row's splits: a CTA runs its splits in descending order
-        std::sort(l.begin(), l.end(), [S](int x, int y) { return x % S != y % S ? x % S > y % S : x < y; });
-      else
-        std::sort(l.begin(), l.end());
+      std::sort(l.begin(), l.end());
       items.insert(items.end(), l.begin(), l.end());
       off[(size_t)b * (DS_PHASES + 1) + ph + 1] = (int)items.size();
     }
@@ -795,8 +806,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     dp.bt = in + e->in.bt;
     dp.sched_off = d_off;
     dp.sched_items = d_items;
-    dp.ablk = e->ds_ablk;
-    dp.asplits = e->ds_splits;
+    dp.asplits = ds_splits(e, T);
     dp.trows = e->ds_rows;
     dp.kx = e->ds_kx;
     dp.slots_n = e->ds_slots;
@@ -804,6 +814,7 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     dp.qkv_ll = e->ds_qkv;
     dp.act_ll = e->ds_act;
     dp.attn_ws = e->ds_ws;
+    dp.attn_out = e->ds_out;
     dp.epoch = e->ds_epoch;
     dp.xn_h = e->xn_h;
     dp.xn_l = e->xn_l;

@@ -279,16 +279,15 @@ struct DecodeStepParams {
   const int* bt;          // [rows][mbs]
   const int* sched_off;   // [gridDim.x][DS_PHASES + 1]: item ranges of each CTA's phases
   const int* sched_items;
-  int ablk;               // attention: KV blocks per split
-  int asplits;            // splits per (row, KV head), at most kDsMaxSplits
+  int asplits;            // attention splits per (row, KV head) of this step, at most kDsMaxSplits
   int trows;              // rows of the activation staging planes (>= T)
   int kx;                 // row stride of the staging planes (elements)
   int slots_n;            // ring slots of 32 KB
   unsigned long long* h_ll;    // [trows][H]
   unsigned long long* qkv_ll;  // [trows][(Hq + 2 Hkv) d]
   unsigned long long* act_ll;  // [trows][I]
-  unsigned long long* attn_ws;  // [trows][Hkv][asplits][G][d + 2]: each split's (O, max, sum), merged by the
-                                //   output projection's staging
+  unsigned long long* attn_ws;   // [trows][Hkv][kDsMaxSplits][G][d + 2]: each split's (O, max, sum)
+  unsigned long long* attn_out;  // [trows][Hq d]: the attention output, merged by each row's last split
   unsigned int* epoch;    // [0]: this step's epoch (tags), [1]: epoch of a step given up after a timeout
   bf16* xn_h;             // outputs for the LM head: planes of h * final_norm [T][H]
   bf16* xn_l;
@@ -300,13 +299,13 @@ struct DecodeStepParams {
   int* diag;              // [4]: the first wait that gave up -- site (DsWaitSite), block, thread, layer
 };
 // Where a wait of the persistent decode kernel gave up (recorded in DecodeStepParams::diag).
-enum DsWaitSite { WAIT_RING_FULL = 1, WAIT_RING_EMPTY = 2, WAIT_STAGE = 3, WAIT_HEAD = 4, WAIT_ATTN_STATS = 5,
-                  WAIT_ATTN_OUT = 6, WAIT_RESIDUAL = 7 };
+enum DsWaitSite { WAIT_RING_FULL = 1, WAIT_RING_EMPTY = 2, WAIT_STAGE = 3, WAIT_HEAD = 4, WAIT_ATTN_MERGE = 6,
+                  WAIT_RESIDUAL = 7 };
 // Ring slot size, and the shared memory a launch needs for `trows` staged rows of width kmax.
 constexpr int kDsSlotBytes = 32 * 1024;
 constexpr int kDsMaxItems = 256;  // work items of one CTA per layer (all phases)
-constexpr int kDsMaxSplits = 4;   // attention key splits per (row, KV head)
-size_t decode_step_smem(int slots_n, int trows, int kx, int d, int layers);
+constexpr int kDsMaxSplits = 16;  // attention key splits per (row, KV head)
+size_t decode_step_smem(int slots_n, int trows, int kx, int d, int G, int H, int layers);
 // The kernel's shared-memory limit is raised on first use; false if the device cannot host the grid.
 cudaError_t decode_step_prepare(size_t smem, int* max_ctas_per_sm);
 cudaError_t launch_decode_step(const DecodeStepParams& p, int grid, size_t smem, cudaStream_t s);
