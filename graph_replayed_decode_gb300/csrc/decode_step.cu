@@ -87,6 +87,16 @@ ENG_DEVICE int csync_and(int v) {
       : "memory");
   return r;
 }
+// Non-blocking test of a phase (the common case: the ring chunk landed long ago).
+ENG_DEVICE bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 ENG_DEVICE bool mbar_try(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -163,7 +173,7 @@ __device__ __noinline__ bool ds_mbar_spin(const DecodeStepParams& p, uint64_t* b
 }
 ENG_DEVICE bool ds_mbar_wait(const DecodeStepParams& p, uint64_t* bar, uint32_t parity, uint32_t epoch,
                              int site = WAIT_RING_FULL) {
-  return mbar_try(bar, parity) || ds_mbar_spin(p, bar, parity, epoch, site);
+  return mbar_test(bar, parity) || ds_mbar_spin(p, bar, parity, epoch, site);
 }
 
 // Re-polls a word pair (or a single word) until it carries `tag`; the rare, out-of-line part of a wait.
@@ -338,6 +348,9 @@ ENG_DEVICE void ds_producer(const DecodeStepParams& p, const DsSmem& S, uint32_t
 #pragma unroll 1
   for (int l = 0; l < p.L; ++l) {
     const DsLayer& Lw = S.layers[l];
+    // the LM head reads its weights right after this kernel: the first part of them into L2 while the last
+    // layer runs (it leaves most of the memory bandwidth unused)
+    if (l == p.L - 1 && p.pf_bytes) prefetch_share(p.pf_ptr, p.pf_bytes);
 #pragma unroll 1
     for (int ph = 0; ph < DS_PHASES; ++ph) {
 #pragma unroll 1
@@ -575,13 +588,15 @@ ENG_DEVICE bool ds_gather_head(const DecodeStepParams& p, const DsSmem& S, const
 }
 
 // The n (<= kDsGroup) 16-row tiles of a packed weight ([N][K]) that one pass of a projection phase takes,
-// against the staged planes.  The tiles' chunks come from the ring in order; in each chunk warp w takes the
-// k-tiles w, w + 7, ... into four independent accumulator chains of its tile (two k-steps x hi/lo planes),
-// and the warps' sums are added in warp order.  On return warp i (< n) holds tile i's values in v, in MMA
-// fragment order: (row r, token c), (r, c + 1), (r + 8, c), (r + 8, c + 1) with r = lane / 4, c = 2 (lane % 4).
-// A row past the step's tokens reads row 0, so lanes of one step's rows read the same words as a broadcast.
-ENG_DEVICE bool ds_gemv(const DecodeStepParams& p, const DsSmem& S, int K, int n, RingPos& rp, uint32_t epoch,
-                        float4& v) {
+// against the staged planes.  In each ring chunk warp w takes the k-tiles w, w + 7, ... into four independent
+// accumulator chains of its tile (two k-steps x hi/lo planes); tiles of a single chunk each (K <= 1024) run
+// interleaved, the chunks of all n tiles being in the ring together.  The warps' sums are added in warp
+// order.  On return warp i (< n) holds tile i's values in v, in MMA fragment order: (row r, token c),
+// (r, c + 1), (r + 8, c), (r + 8, c + 1) with r = lane / 4, c = 2 (lane % 4); with `norm`, rs holds
+// 1 / rms of the staged rows c and c + 1 (ds_stage's parts).  A row past the step's tokens reads row 0, so
+// lanes of one step's rows read the same words as a broadcast.
+ENG_DEVICE bool ds_gemv(const DecodeStepParams& p, const DsSmem& S, int K, int n, bool norm, RingPos& rp,
+                        uint32_t epoch, float4& v, float (&rs)[2]) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KT = K >> 5, nch = (KT + 31) >> 5;
   const int g = lane >> 2;
@@ -589,50 +604,108 @@ ENG_DEVICE bool ds_gemv(const DecodeStepParams& p, const DsSmem& S, int K, int n
   const uint4* xs = reinterpret_cast<const uint4*>(S.xs + (size_t)xrow * p.kx) + (lane & 3);
   const uint4* xl = reinterpret_cast<const uint4*>(S.xl + (size_t)xrow * p.kx) + (lane & 3);
   bool ok = true;
-#pragma unroll 1
-  for (int i = 0; i < n && ok; ++i) {
-    float acc[4][4];
+  if (nch == 1 && n <= p.slots_n) {  // every tile's chunk fits in the ring at once
+    float acc[kDsGroup][4][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < nch; ++c, rp.next(p.slots_n)) {
-      if (!ds_mbar_wait(p, &S.full[rp.slot], rp.round & 1, epoch)) {
-        ok = false;
-        break;
+    for (int i = 0; i < kDsGroup; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
+    RingPos r2 = rp;
+    const uint4* w[kDsGroup];
+#pragma unroll
+    for (int i = 0; i < kDsGroup; ++i) {
+      w[i] = reinterpret_cast<const uint4*>(S.ring + (size_t)r2.slot * kDsSlotBytes) + lane;
+      if (i < n) {
+        if (ok && !ds_mbar_wait(p, &S.full[r2.slot], r2.round & 1, epoch)) ok = false;
+        r2.next(p.slots_n);
       }
-      const uint4* w = reinterpret_cast<const uint4*>(S.ring + (size_t)rp.slot * kDsSlotBytes) + lane;
-      const int nkt = min(32, KT - 32 * c);
-      const uint4* xsc = xs + 32 * c * 4;
-      const uint4* xlc = xl + 32 * c * 4;
+    }
+    if (ok) {
 #pragma unroll
       for (int j = 0; j < (32 + kDsWarps - 1) / kDsWarps; ++j) {
         const int kt = warp + kDsWarps * j;
-        if (kt >= nkt) break;
-        const uint4 a0 = w[kt * 64], a1 = w[kt * 64 + 32];
-        const uint4 bh = xsc[kt * 4], bl = xlc[kt * 4];
-        mma_bf16(acc[0], a0.x, a0.y, a0.z, a0.w, bh.x, bh.y);
-        mma_bf16(acc[1], a1.x, a1.y, a1.z, a1.w, bh.z, bh.w);
-        mma_bf16(acc[2], a0.x, a0.y, a0.z, a0.w, bl.x, bl.y);
-        mma_bf16(acc[3], a1.x, a1.y, a1.z, a1.w, bl.z, bl.w);
+        if (kt >= KT) break;
+        const uint4 bh = xs[kt * 4], bl = xl[kt * 4];
+#pragma unroll
+        for (int i = 0; i < kDsGroup; ++i) {
+          if (i >= n) break;
+          const uint4 a0 = w[i][kt * 64], a1 = w[i][kt * 64 + 32];
+          mma_bf16(acc[i][0], a0.x, a0.y, a0.z, a0.w, bh.x, bh.y);
+          mma_bf16(acc[i][1], a1.x, a1.y, a1.z, a1.w, bh.z, bh.w);
+          mma_bf16(acc[i][2], a0.x, a0.y, a0.z, a0.w, bl.x, bl.y);
+          mma_bf16(acc[i][3], a1.x, a1.y, a1.z, a1.w, bl.z, bl.w);
+        }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[rp.slot]);
+#pragma unroll
+      for (int i = 0; i < kDsGroup; ++i) {
+        if (i >= n) break;
+        if (lane == 0) mbar_arrive(&S.empty[rp.slot]);
+        rp.next(p.slots_n);
+        S.red[(i * kDsWarps + warp) * 32 + lane] =
+            make_float4((acc[i][0][0] + acc[i][1][0]) + (acc[i][2][0] + acc[i][3][0]),
+                        (acc[i][0][1] + acc[i][1][1]) + (acc[i][2][1] + acc[i][3][1]),
+                        (acc[i][0][2] + acc[i][1][2]) + (acc[i][2][2] + acc[i][3][2]),
+                        (acc[i][0][3] + acc[i][1][3]) + (acc[i][2][3] + acc[i][3][3]));
+      }
     }
-    S.red[(i * kDsWarps + warp) * 32 + lane] =
-        make_float4((acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]), (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]),
-                    (acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2]), (acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]));
+  } else {
+#pragma unroll 1
+    for (int i = 0; i < n && ok; ++i) {
+      float acc[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < nch; ++c, rp.next(p.slots_n)) {
+        if (!ds_mbar_wait(p, &S.full[rp.slot], rp.round & 1, epoch)) {
+          ok = false;
+          break;
+        }
+        const uint4* w = reinterpret_cast<const uint4*>(S.ring + (size_t)rp.slot * kDsSlotBytes) + lane;
+        const int nkt = min(32, KT - 32 * c);
+        const uint4* xsc = xs + 32 * c * 4;
+        const uint4* xlc = xl + 32 * c * 4;
+#pragma unroll
+        for (int j = 0; j < (32 + kDsWarps - 1) / kDsWarps; ++j) {
+          const int kt = warp + kDsWarps * j;
+          if (kt >= nkt) break;
+          const uint4 a0 = w[kt * 64], a1 = w[kt * 64 + 32];
+          const uint4 bh = xsc[kt * 4], bl = xlc[kt * 4];
+          mma_bf16(acc[0], a0.x, a0.y, a0.z, a0.w, bh.x, bh.y);
+          mma_bf16(acc[1], a1.x, a1.y, a1.z, a1.w, bh.z, bh.w);
+          mma_bf16(acc[2], a0.x, a0.y, a0.z, a0.w, bl.x, bl.y);
+          mma_bf16(acc[3], a1.x, a1.y, a1.z, a1.w, bl.z, bl.w);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[rp.slot]);
+      }
+      S.red[(i * kDsWarps + warp) * 32 + lane] =
+          make_float4((acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]), (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]),
+                      (acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2]), (acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]));
+    }
   }
   if (!csync_and(ok)) return false;
   if (warp < n) {
     const float4* r = S.red + (size_t)warp * kDsWarps * 32 + lane;
-    v = r[0];
+    float4 u[kDsWarps];
+#pragma unroll
+    for (int w2 = 0; w2 < kDsWarps; ++w2) u[w2] = r[w2 * 32];
+    rs[0] = rs[1] = 1.f;
+    if (norm) {
+#pragma unroll 1
+      for (int t = 0; t < p.T; ++t) {
+        const float r_t = rsqrtf(ds_sumsq(S, t) / (float)K + p.eps);
+        if (t == 2 * (lane & 3)) rs[0] = r_t;
+        if (t == 2 * (lane & 3) + 1) rs[1] = r_t;
+      }
+    }
+    v = u[0];
 #pragma unroll
     for (int w2 = 1; w2 < kDsWarps; ++w2) {
-      const float4 u = r[w2 * 32];
-      v.x += u.x;
-      v.y += u.y;
-      v.z += u.z;
-      v.w += u.w;
+      v.x += u[w2].x;
+      v.y += u[w2].y;
+      v.z += u[w2].z;
+      v.w += u[w2].w;
     }
   }
   return true;
@@ -1078,16 +1151,8 @@ ENG_DEVICE void ds_consumer(const DecodeStepParams& p, const DsSmem& S, uint32_t
         if (it != first) request(it);
         const uint32_t nch = (uint32_t)((K / 32 + 31) / 32);
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        ok = ds_gemv(p, S, K, n, rp, epoch, v);
         float rs[2] = {1.f, 1.f};  // 1 / rms of the lane's tokens c, c + 1 (norm phases)
-        if (ok && norm && warp < n) {
-#pragma unroll 1
-          for (int t = 0; t < p.T; ++t) {
-            const float r_t = rsqrtf(ds_sumsq(S, t) / (float)K + p.eps);
-            if (t == 2 * (lane & 3)) rs[0] = r_t;
-            if (t == 2 * (lane & 3) + 1) rs[1] = r_t;
-          }
-        }
+        ok = ds_gemv(p, S, K, n, norm, rp, epoch, v, rs);
         ok = ok && csync_and(warp >= n || ds_epilogue(p, ph, tile, pre, bias, rs, tres, ds_tag(epoch, l, ph), epoch, v));
         q += (uint32_t)n * nch;
       }

@@ -1,8 +1,8 @@
 // device.cu -- per-device facts the launchers need: the SM count (grid sizing) and the dynamic
-// shared-memory limit of each kernel, which belongs to the device's context and so is set once per
-// (device, kernel), under a lock, rather than once per process.
+// shared-memory limit of each kernel, which belongs to the device's context and so is kept per
+// (device, kernel), under a lock, rather than per process.
+#include <map>
 #include <mutex>
-#include <set>
 #include <utility>
 
 #include "kernels.h"
@@ -25,16 +25,20 @@ int device_sm_count() {
   return count[dev];
 }
 
+// The limit only ever grows: engines on one device may need different amounts for the same kernel, and a
+// limit above a launch's need is harmless.
 cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
   static std::mutex mu;
-  static std::set<std::pair<int, const void*>> done;
+  static std::map<std::pair<int, const void*>, int> limit;
   int dev = 0;
   cudaError_t r = cudaGetDevice(&dev);
   if (r != cudaSuccess) return r;
   std::lock_guard<std::mutex> lock(mu);
-  if (done.count({dev, kernel})) return cudaSuccess;
+  const auto key = std::make_pair(dev, kernel);
+  const auto it = limit.find(key);
+  if (it != limit.end() && it->second >= bytes) return cudaSuccess;
   r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (r == cudaSuccess) done.insert({dev, kernel});
+  if (r == cudaSuccess) limit[key] = bytes;
   return r;
 }
 

@@ -529,13 +529,12 @@ static int setup_buffers(eng_t* e) {
 // Decides whether decode-only steps of a few tokens run on the persistent kernel (decode_step.cu) and
 // allocates its buffers.  The kernel stages its input rows in shared memory, so the token count it takes
 // is the largest power of two (at most 8) whose rows of the widest projection input fit 50 KB; it needs
-// one CTA per SM, all resident together (a cooperative launch).  It is taken only with ENG_DECODE_KERNEL=1
-// in the environment when the engine is created: until it beats the per-layer kernels, decode steps run on
-// those by default.
+// one CTA per SM, all resident together (a cooperative launch).  ENG_DECODE_KERNEL=0 in the environment when
+// the engine is created keeps every step on the per-layer kernels (for comparison).
 static int setup_decode_step(eng_t* e) {
   const eng_config_t& c = e->c;
   const char* v = getenv("ENG_DECODE_KERNEL");
-  if (!v || v[0] != '1') return ENG_OK;
+  if (v && v[0] == '0') return ENG_OK;
   const int d = c.head_dim, G = c.q_heads / c.kv_heads;
   if (c.layers > 50 || G > 8 || c.kv_heads > 255 || (d != 64 && d != 128)) return ENG_OK;
   const int kx = std::max({c.hidden, c.q_heads * d, c.intermediate}) + 8;
@@ -824,6 +823,8 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     dp.slots = e->slots;
     dp.status = e->status;
     dp.diag = e->ds_diag;
+    dp.pf_ptr = e->lm;
+    dp.pf_bytes = std::min<unsigned long long>((unsigned long long)c.vocab * H * 2, 80ull << 20);
     int64_t wbytes = 0;
     for (const GemmSite* g : {&e->g_qkv, &e->g_o, &e->g_gu, &e->g_down}) wbytes += (int64_t)g->N * g->K * 2;
     e->launches++;

@@ -297,6 +297,8 @@ struct DecodeStepParams {
   int* slots;             //   [T] KV slot of each token (-1 padding)
   int* status;
   int* diag;              // [4]: the first wait that gave up -- site (DsWaitSite), block, thread, layer
+  const void* pf_ptr;     // the start of the LM head's weights, prefetched into L2 during the last layer
+  unsigned long long pf_bytes;
 };
 // Where a wait of the persistent decode kernel gave up (recorded in DecodeStepParams::diag).
 enum DsWaitSite { WAIT_RING_FULL = 1, WAIT_RING_EMPTY = 2, WAIT_STAGE = 3, WAIT_HEAD = 4, WAIT_ATTN_MERGE = 6,

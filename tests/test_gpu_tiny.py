@@ -36,9 +36,8 @@ def unit_norm_weights():
 
 
 def _engine(weights, stream=None, decode_kernel=True, num_blocks=NB, mbs=MBS):
-    """An engine over the tiny shape.  decode_kernel=True runs small decode-only steps on the persistent decode
-    kernel (ENG_DECODE_KERNEL=1 when the engine is created; the engine's default is the per-layer kernels),
-    so that most tests here cover it; decode_kernel=False keeps them on the per-layer kernels."""
+    """An engine over the tiny shape.  decode_kernel=False keeps small decode-only steps on the per-layer
+    kernels (ENG_DECODE_KERNEL=0 when the engine is created) instead of the persistent decode kernel."""
     import os
     old = os.environ.get("ENG_DECODE_KERNEL")
     os.environ["ENG_DECODE_KERNEL"] = "1" if decode_kernel else "0"
