@@ -54,6 +54,13 @@ WORKLOADS = {
                                        "(synthetic KV), Gumbel-max T=1.0, bucket 32"),
 }
 
+# the mixed packed step (reported under "extra" by the default run; not graph-replayed): a 512-position chunk
+# of fresh prompts, then 32 decode rows
+MIXED = dict(shape="qwen2p5_1p5b",
+             text="Qwen2.5-1.5B-shaped decoder, one packed step: a 512-position chunk of fresh prompts "
+                  "({16,64,256,1024,4096}, FCFS, the last one cut) followed by 32 decode rows at contexts from "
+                  "{64,256,1024,4096} (synthetic KV), greedy, eager")
+
 
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -406,6 +413,100 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     return result
 
 
+def run_mixed(steps: int, warmup: int, local_rank: int) -> dict:
+    """The mixed packed step of the Qwen2.5-1.5B workload, eager (mixed steps are not replayed): the same step
+    `steps` times with host inputs (device time with CUDA events, and end to end with the sampled ids read
+    back), against the step roofline max(bytes / HBM, flops / sustained bf16 tensor peak)."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    wl = MIXED
+    s = synth.shape(wl["shape"])
+    chunk = synth.mixed_chunk_prompts(512, key=0, seed=0)
+    P = len(chunk)
+    dctx = [int(c) for c in synth.context_lengths(32, (64, 256, 1024, 4096), key=1, seed=0)]
+    need = [-(-(plen + 1) // 16) for plen, _ in chunk] + [-(-(c + 1) // 16) for c in dctx]
+    mbs = max(need)
+    nb = sum(need) + 4
+    weights = synth.make_weights(s, seed=0, cache=False)
+    stream = torch.cuda.Stream()
+    h = eng.eng_create(eng.make_config(s, nb, 64, 600, mbs), eng.TensorList(weights.items()), stream.cuda_stream)
+    del weights
+    blocks = [eng.eng_pool_alloc(h, n) for n in need]
+    bt = np.zeros((P + 32, mbs), dtype=np.int32)
+    for r, b in enumerate(blocks):
+        bt[r, :len(b)] = b
+    fill_synthetic_kv(h, s, nb, blocks[P:], dctx)
+    prompts = [synth.prompt_ids(take, s.vocab, 50 + i) for i, (plen, take) in enumerate(chunk)]
+    ids = np.concatenate(prompts + [synth.decode_ids(32, s.vocab, 2)]).astype(np.int32)
+    pos = np.concatenate([np.arange(take) for _, take in chunk] + [np.array(dctx)]).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum([take for _, take in chunk] + [1] * 32)]).astype(np.int32)
+    seq = np.array([take for _, take in chunk] + [c + 1 for c in dctx], dtype=np.int32)
+    temps = np.zeros(P + 32, dtype=np.float32)
+    st = eng.StepArrays(ids, pos, cu, bt, seq, temps, seed=0, offset=0)
+    ids_dev = torch.zeros(64, dtype=torch.int32, device="cuda")
+    T = int(cu[-1])
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(warmup):
+        eng.eng_step(h, st, ids_dev.data_ptr(), None)
+    torch.cuda.synchronize()
+    launches = eng.eng_last_step_info(h).launches
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(steps):
+            eng.eng_step(h, st, ids_dev.data_ptr(), None)
+        e1.record()
+    torch.cuda.synchronize()
+    t_dev = e0.elapsed_time(e1) / 1e3 / steps
+    pinned = torch.zeros(P + 32, dtype=torch.int32).pin_memory()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        eng.eng_step(h, st, ids_dev.data_ptr(), None)
+        with torch.cuda.stream(stream):
+            pinned.copy_(ids_dev[:P + 32], non_blocking=True)
+        stream.synchronize()
+    t_e2e = (time.perf_counter() - t0) / steps
+    h2d = eng.eng_last_step_info(h).h2d_bytes
+    clk = clocks.stop()
+    status = eng.eng_status(h, True)
+    eng.eng_destroy(h)
+    peaks = load_peaks()
+    keys_seen = sum(take * (take + 1) // 2 for _, take in chunk) + sum(c + 1 for c in dctx)
+    flops = roofline.step_flops(s, T, P + 32, keys_seen)
+    nbytes = roofline.step_bytes(s, T, [int(x) for x in seq])
+    t_b = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_f = flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    return {"workload": wl["text"], "tokens_per_step": T, "requests": P + 32, "steps": steps, "warmup": warmup,
+            "ms_per_step": t_dev * 1e3, "value": T / t_dev, "unit": "tokens/s",
+            "step_roofline": {"bound": "tensor" if t_f >= t_b else "hbm", "bytes_per_step": int(nbytes),
+                              "flops_per_step": int(flops), "t_roof_ms": max(t_b, t_f) * 1e3,
+                              "frac": max(t_b, t_f) / t_dev, "achieved_tflops": flops / t_dev / 1e12,
+                              "peak_tflops": peaks["bf16_tflops_sustained"], "peak_gbs": peaks["hbm_gbs"],
+                              "of": peaks["source"] + " (sustained bf16 for the tensor bound)"},
+            "e2e": {"value": T / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": 4 * (P + 32)},
+            "gpu_launches": steps * launches, "clocks": clk, "device_status": status}
+
+
+def run_extras(args, local_rank: int) -> dict:
+    """The other configurations the metric is stated on, in the same run: batch-32 decode (graph-replayed)
+    and the mixed packed step, each with its own roofline, clocks and end-to-end figure."""
+    import copy
+    out = {}
+    a = copy.copy(args)
+    a.steps, a.warmup, a.workload, a.no_cpu_baseline = min(args.steps, 64), min(args.warmup, 8), "qwen3_0p6b_b32", True
+    r = run_ours(a, WORKLOADS["qwen3_0p6b_b32"], 0, 1, local_rank)
+    out["qwen3_0p6b_b32"] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "config",
+                                                "step_roofline", "roofline", "e2e", "gpu_launches", "clocks",
+                                                "device_status")}
+    out["qwen3_0p6b_b32"]["kernels"] = dict(list(r["kernels"].items())[:4])
+    out["qwen2p5_1p5b_mixed"] = run_mixed(min(args.steps, 16), min(args.warmup, 4), local_rank)
+    return out
+
+
 def load_traffic(wl_name: str, kind: str):
     """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel sources."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -441,6 +542,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--top-k", type=int, default=0, help="top-k filter on every row (0: off)")
     ap.add_argument("--top-p", type=float, default=1.0, help="top-p filter on every row (1: off)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the batch-32 and mixed-step figures that the default run adds under 'extra'")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     wl = WORKLOADS[args.workload]
@@ -472,6 +575,8 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     res = run_ours(args, wl, rank, world, local_rank)
+    if res is not None and world == 1 and args.workload == "qwen3_0p6b_b1" and not args.no_extra:
+        res["extra"] = run_extras(args, local_rank)
     if res is not None:
         print(json.dumps(res))
     if world > 1:
