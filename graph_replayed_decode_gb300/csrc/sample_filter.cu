@@ -1,4 +1,5 @@
-// sample_filter.cu -- top-k / top-p filtered Gumbel-max sampling over float32 logits, one CTA per row.
+// sample_filter.cu -- top-k / top-p filtered Gumbel-max sampling over float32 logits, one thread-block
+// cluster of 2-8 CTAs per row.
 //
 // "19. Fast decode", section "Sampling without the CPU": the filters drop logits (to -inf) before the
 // argmax, with shapes that do not depend on the data.  Definitions, with every integer decision exact:
@@ -11,11 +12,13 @@
 //     shortest prefix whose mass reaches p, taken in integers so that no summation order matters;
 //   * the draw is the unfiltered sampler's key s + g over the survivors, ties to the lowest index.
 //
-// The kernel finds each filter's boundary without sorting the vocabulary.  A histogram over 4096 buckets
-// of s_max - s (monotone in the rank order, so every bucket is a contiguous run of ranks) holds each
-// bucket's count and integer weight; prefix sums over the buckets name the bucket holding the boundary;
-// that bucket alone is sorted in shared memory (bitonic, up to 8192 entries) or, when larger, resolved by a
-// radix descent over the rank keys.  The Philox noise and the two logarithms run for survivors only.
+// The kernel finds each filter's boundary without sorting the vocabulary.  The row is spread over the
+// cluster's CTAs; a histogram over kBuckets (2048) buckets of s_max - s (monotone in the rank order, so
+// every bucket is a contiguous run of ranks) holds each bucket's count and integer weight, summed over the
+// cluster in distributed shared memory; prefix sums over the buckets name the bucket holding the boundary.
+// When every top-k candidate fits (kGatherCap entries) they are gathered and rank-sorted in shared memory;
+// otherwise the boundary bucket alone is sorted (bitonic) or, when larger, resolved by a radix descent over
+// the rank keys.  The Philox noise and the two logarithms run for survivors only.
 #include <cooperative_groups.h>
 
 #include <cmath>

@@ -150,6 +150,13 @@ typedef struct {
  * static step buffers.  cuda_stream: the cudaStream_t to run on, or NULL for a
  * stream the engine creates.  Errors: ENG_EINVAL (config, missing/mis-sized
  * weight), ENG_ENOMEM, ENG_ECUDA.  *out is NULL on failure.
+ * Decode-only steps of at most a few tokens (the largest power of two <= 8 whose
+ * staged activation rows fit the kernel's shared memory) run every layer in one
+ * persistent cooperative kernel, one CTA per SM ("19. Fast decode", section
+ * "Where the time goes": the step's many small kernels); the environment variable
+ * ENG_DECODE_KERNEL=0 at creation keeps them on the per-layer kernels.  Results
+ * match the oracle either way and are bit-identical between eager steps and graph
+ * replays of the same path.
  */
 int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_weights, void* cuda_stream,
                eng_t** out);
