@@ -138,16 +138,19 @@ ENG_DEVICE void stage8(bf16* xs, bf16* xl, int idx, const float4 a, const float4
 // kTcStages shared-memory stages (weight tile, hi tile, lo tile per stage, TMA tensor copies with 128-byte
 // swizzle); one thread issues two tcgen05 MMAs per 16 k (hi plane, lo plane) into a 128 x 64 fp32 TMEM
 // accumulator; the accumulator is read back into the same [rows][tokens] tile the epilogues use.
-static constexpr int kTcStages = 4;
+static constexpr int kTcStages = 3;
 static constexpr uint32_t kTcA = 128 * 128;           // 128 weight rows x 64 bf16
 static constexpr uint32_t kTcB = 64 * 128;            // 64 tokens x 64 bf16, one plane
 static constexpr uint32_t kTcStage = kTcA + 2 * kTcB;
 static constexpr size_t kTcCsBytes = (size_t)64 * 128 * 4;  // QKV: the RoPE rows of the chunk's 64 tokens
+// only the QKV epilogue keeps RoPE rows: the other launches stay small enough for two CTAs per SM, so one
+// CTA's epilogue overlaps the other's k-loop
+__host__ __device__ constexpr size_t tc_cs_bytes(int epi) { return epi == EPI_QKV_ROPE ? kTcCsBytes : 0; }
 // dynamic shared memory of a TC launch with S K-splits: [ring][RoPE rows][split-K receive buffer] + 1 KB to
 // align the ring (the receive buffer is separate: peers push into it while this CTA still runs its ring)
 __host__ __device__ inline size_t tc_recv_bytes(int S) { return S > 1 ? (size_t)S * 128 * gemm_kblk(8, S) * 4 : 0; }
-__host__ __device__ inline size_t tc_smem(int S) {
-  return (size_t)kTcStages * kTcStage + kTcCsBytes + tc_recv_bytes(S) + 1024;
+__host__ __device__ inline size_t tc_smem(int S, int epi = EPI_QKV_ROPE) {
+  return (size_t)kTcStages * kTcStage + tc_cs_bytes(epi) + tc_recv_bytes(S) + 1024;
 }
 
 ENG_DEVICE uint8_t* tc_ring(uint8_t* smem) {
@@ -560,7 +563,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
   if (S > 1) {
     // push this CTA's partial sums of the tokens CTA q finishes into q's receive buffer (4 tokens per
     // 16-byte store), then every CTA adds its block's partials in split order (its own at its position)
-    float* recv = TC ? reinterpret_cast<float*>(tc_ring(smem) + (size_t)kTcStages * kTcStage + kTcCsBytes)
+    float* recv = TC ? reinterpret_cast<float*>(tc_ring(smem) + (size_t)kTcStages * kTcStage + tc_cs_bytes(EPI))
                     : reinterpret_cast<float*>(area + sm.recv_off);  // [S][rows][kblk]
     const int groups = kblk / 4;
     for (int i = threadIdx.x; i < S * rows * groups; i += 256) {
@@ -849,7 +852,7 @@ void gemm_plan_large(int N, int K, int rg_fixed, int sms, int* RG, int* S, int* 
 
 template <int NT, int EPI, bool NORM_IN, bool TC>
 static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStream_t s, dim3 grid, const TcMaps* tm) {
-  const size_t smem_bytes = TC ? tc_smem(p.S) : gemm_smem(NT, p.RG, p.kt_per_split, p.S).total;
+  const size_t smem_bytes = TC ? tc_smem(p.S, EPI) : gemm_smem(NT, p.RG, p.kt_per_split, p.S).total;
   cudaError_t ae;
   if constexpr (TC)
     ae = ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<EPI, NORM_IN>), (int)kSmemBudget);
