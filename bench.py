@@ -491,9 +491,63 @@ def run_mixed(steps: int, warmup: int, local_rank: int) -> dict:
             "gpu_launches": steps * launches, "clocks": clk, "device_status": status}
 
 
+def run_moe(steps: int, warmup: int) -> dict:
+    """The Qwen3-30B-A3B-shaped mixture-of-experts layer (eng_moe_mlp: alignment, grouped gate|up and down
+    GEMMs, combine) at a decode batch (32 tokens) and a prefill chunk (512 tokens), routed by the oracle's
+    router on synthetic token rows.  Step roofline: the experts' weights that the routing touches plus the
+    token rows in and the outputs, over measured HBM bandwidth (flops / sustained bf16 peak is smaller)."""
+    import torch
+    from graph_replayed_decode_gb300 import eng
+    import oracle.moe as omoe
+    from oracle.model import widen_bf16
+    m = synth.moe_shape("qwen3_30b_a3b_moe")
+    w = synth.moe_weights(m, seed=0)
+    peaks = load_peaks()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    gu, dn = dev(w["gate_up"]), dev(w["down"])
+    out = {"workload": "Qwen3-30B-A3B-shaped MoE MLP: hidden 2048, 128 experts, 8 per token, expert width 768, "
+                       "bf16 weights, routed by the oracle's router on synthetic token rows"}
+    for N in (32, 512):
+        x = synth.moe_tokens(N, m.hidden, key=7)
+        rw, ids = omoe.route(widen_bf16(x), widen_bf16(w["router"]), m.top_k)
+        dx = dev(x)
+        drw = torch.from_numpy(rw.astype(np.float32)).cuda()
+        dids = torch.from_numpy(ids.astype(np.int32)).cuda()
+        y = torch.empty((N, m.hidden), dtype=torch.float32, device="cuda")
+        nbytes = eng.eng_moe_workspace_bytes(N, m.top_k, m.experts, m.hidden, m.intermediate)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # larger than L2, between calls
+        call = lambda: eng.eng_moe_mlp(dx.data_ptr(), gu.data_ptr(), dn.data_ptr(), drw.data_ptr(), dids.data_ptr(), N,
+                                       m.hidden, m.intermediate, m.experts, m.top_k, y.data_ptr(), ws.data_ptr(),
+                                       nbytes, torch.cuda.current_stream().cuda_stream)
+        for _ in range(warmup):
+            call()
+        times = []
+        for _ in range(steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / 1e3)
+        t = statistics.median(times)
+        used = len(np.unique(ids))
+        nbytes_alg = used * (2 * m.intermediate * m.hidden + m.hidden * m.intermediate) * 2 + N * m.hidden * (2 + 4)
+        flops = 2 * N * m.top_k * 3 * m.intermediate * m.hidden
+        t_roof = max(nbytes_alg / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops_sustained"] * 1e12))
+        out[f"tokens_{N}"] = {"ms": t * 1e3, "experts_touched": used, "bytes": int(nbytes_alg), "flops": int(flops),
+                              "achieved_gbs": nbytes_alg / t / 1e9, "t_roof_ms": t_roof * 1e3, "frac": t_roof / t,
+                              "bound": "hbm", "peak_gbs": peaks["hbm_gbs"], "of": peaks["source"],
+                              "timing": f"median of {steps} calls, L2 flushed (256 MB written) before each"}
+    return out
+
+
 def run_extras(args, local_rank: int) -> dict:
     """The other configurations the metric is stated on, in the same run: batch-32 decode (graph-replayed)
-    and the mixed packed step, each with its own roofline, clocks and end-to-end figure."""
+    and the mixed packed step, each with its own roofline, clocks and end-to-end figure; and the
+    mixture-of-experts layer of the MoE calls."""
     import copy
     out = {}
     a = copy.copy(args)
@@ -504,6 +558,7 @@ def run_extras(args, local_rank: int) -> dict:
                                                 "device_status")}
     out["qwen3_0p6b_b32"]["kernels"] = dict(list(r["kernels"].items())[:4])
     out["qwen2p5_1p5b_mixed"] = run_mixed(min(args.steps, 16), min(args.warmup, 4), local_rank)
+    out["qwen3_30b_a3b_moe_layer"] = run_moe(min(args.steps, 20), 3)
     return out
 
 

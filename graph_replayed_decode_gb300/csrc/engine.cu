@@ -1657,6 +1657,53 @@ int eng_sample(const float* logits_dev, int32_t rows, int32_t vocab, const float
   return rc;
 }
 
+int eng_moe_route(const void* x, const void* w_router, int32_t num_tokens, int32_t hidden, int32_t num_experts,
+                  int32_t top_k, float* weights, int32_t* expert_ids, void* stream) {
+  if (num_tokens < 0 || hidden < 8 || hidden % 8 || num_experts < 1 || num_experts > 4096 || top_k < 1 || top_k > 32 ||
+      top_k > num_experts || (num_tokens > 0 && (!x || !w_router || !weights || !expert_ids)))
+    return fail(nullptr, ENG_EINVAL, "bad eng_moe_route arguments");
+  const cudaError_t r = launch_moe_route(static_cast<const bf16*>(x), static_cast<const bf16*>(w_router), num_tokens,
+                                         hidden, num_experts, top_k, weights, expert_ids, static_cast<cudaStream_t>(stream));
+  return r == cudaSuccess ? ENG_OK : fail(nullptr, ENG_ECUDA, std::string("eng_moe_route: ") + cudaGetErrorString(r));
+}
+
+int64_t eng_moe_padded_rows(int32_t num_tokens, int32_t top_k, int32_t num_experts, int32_t block_m) {
+  if (num_tokens < 0 || top_k < 1 || num_experts < 1 || block_m < 1) return -1;
+  return moe_padded_rows(num_tokens * top_k, num_experts, block_m);
+}
+
+int eng_moe_align(const int32_t* expert_ids, int32_t num_tokens, int32_t top_k, int32_t num_experts, int32_t block_m,
+                  int32_t* sorted_ids, int32_t* block_expert, int32_t* info, void* stream) {
+  if (num_tokens < 0 || top_k < 1 || num_experts < 1 || num_experts > 1024 || block_m < 1 || !sorted_ids ||
+      !block_expert || !info || (num_tokens > 0 && !expert_ids))
+    return fail(nullptr, ENG_EINVAL, "bad eng_moe_align arguments");
+  const cudaError_t r = launch_moe_align(expert_ids, num_tokens * top_k, num_experts, block_m, sorted_ids, block_expert,
+                                         info, static_cast<cudaStream_t>(stream));
+  return r == cudaSuccess ? ENG_OK : fail(nullptr, ENG_ECUDA, std::string("eng_moe_align: ") + cudaGetErrorString(r));
+}
+
+int64_t eng_moe_workspace_bytes(int32_t num_tokens, int32_t top_k, int32_t num_experts, int32_t hidden,
+                                int32_t inter) {
+  if (num_tokens < 0 || top_k < 1 || num_experts < 1 || hidden < 1 || inter < 1) return -1;
+  return (int64_t)moe_workspace_bytes(num_tokens, top_k, num_experts, hidden, inter);
+}
+
+int eng_moe_mlp(const void* x, const void* gate_up, const void* down, const float* weights, const int32_t* expert_ids,
+                int32_t num_tokens, int32_t hidden, int32_t inter, int32_t num_experts, int32_t top_k, float* out,
+                void* workspace, int64_t workspace_bytes, void* stream) {
+  if (num_tokens < 0 || hidden < 64 || hidden % 64 || inter < 64 || inter % 64 || num_experts < 1 ||
+      num_experts > 1024 || top_k < 1 ||
+      (num_tokens > 0 && (!x || !gate_up || !down || !weights || !expert_ids || !out || !workspace)))
+    return fail(nullptr, ENG_EINVAL, "bad eng_moe_mlp arguments");
+  if (num_tokens > 0 && workspace_bytes < (int64_t)moe_workspace_bytes(num_tokens, top_k, num_experts, hidden, inter))
+    return fail(nullptr, ENG_EINVAL, "eng_moe_mlp: workspace too small");
+  const cudaError_t r = launch_moe_mlp(static_cast<const bf16*>(x), static_cast<const bf16*>(gate_up),
+                                       static_cast<const bf16*>(down), weights, expert_ids, num_tokens, hidden, inter,
+                                       num_experts, top_k, out, workspace, (size_t)workspace_bytes,
+                                       static_cast<cudaStream_t>(stream));
+  return r == cudaSuccess ? ENG_OK : fail(nullptr, ENG_ECUDA, std::string("eng_moe_mlp: ") + cudaGetErrorString(r));
+}
+
 int eng_sample_noalloc(const float* logits_dev, int32_t rows, int32_t vocab, const float* temperature,
                        uint64_t seed, uint64_t offset, int32_t* out_ids_dev, void* stream) {
   if (rows < 0 || vocab < 1 || (rows > 0 && (!logits_dev || !temperature || !out_ids_dev)))

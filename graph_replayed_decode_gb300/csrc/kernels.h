@@ -242,6 +242,17 @@ cudaError_t launch_sample_noalloc(const float* logits, int rows, int vocab, cons
                                   const uint32_t rng_host[4], uint32_t* scratch, int* out_ids, cudaStream_t s);
 
 
+// moe.cu: a mixture-of-experts MLP with shapes that do not depend on the routing (router, alignment of the
+// assignments by expert into blocks of 16 rows, grouped gate|up and down GEMMs, combine).
+int moe_padded_rows(int total, int E, int bm);
+size_t moe_workspace_bytes(int N, int k, int E, int D, int I);
+cudaError_t launch_moe_route(const bf16* x, const bf16* wr, int N, int D, int E, int k, float* w, int* ids,
+                             cudaStream_t s);
+cudaError_t launch_moe_align(const int* ids, int total, int E, int bm, int* sorted_ids, int* block_expert, int* out,
+                             cudaStream_t s);
+cudaError_t launch_moe_mlp(const bf16* x, const bf16* gate_up, const bf16* down, const float* rw, const int* ids,
+                           int N, int D, int I, int E, int k, float* out, void* ws, size_t ws_bytes, cudaStream_t s);
+
 // ------------------------------------------------------------------ persistent decode step (decode_step.cu)
 // Every layer of a decode-only step of at most a few tokens in one cooperative launch: one CTA per SM, a
 // static per-CTA list of work items per layer and phase (QKV tiles, attention splits, o_proj tiles,

@@ -111,6 +111,16 @@ SIGNATURES = [
     ("eng_exp_f32", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     ("eng_generate", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, _I32P, ctypes.c_int32, _I32P,
                                     _I32P]),
+    ("eng_moe_route", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    ("eng_moe_padded_rows", ctypes.c_int64, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    ("eng_moe_align", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    ("eng_moe_workspace_bytes", ctypes.c_int64, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32]),
+    ("eng_moe_mlp", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
 ]
 
 
@@ -357,3 +367,33 @@ def eng_generate(e, num_reqs: int, max_steps: int, check_every: int, stop_ids=()
     n = _check(e, lib().eng_generate(e, max_steps, check_every, _ptr_i32(stops) if len(stops) else None, len(stops),
                                      _ptr_i32(toks), _ptr_i32(lens)))
     return toks, lens, n
+
+
+# ------------------------------------------------------------------ mixture of experts (device pointers)
+
+
+def eng_moe_route(x_dev: int, w_router_dev: int, num_tokens: int, hidden: int, num_experts: int, top_k: int,
+                  weights_dev: int, ids_dev: int, stream: int | None = None):
+    _check(None, lib().eng_moe_route(x_dev, w_router_dev, num_tokens, hidden, num_experts, top_k, weights_dev,
+                                     ids_dev, stream))
+
+
+def eng_moe_padded_rows(num_tokens: int, top_k: int, num_experts: int, block_m: int) -> int:
+    return int(lib().eng_moe_padded_rows(num_tokens, top_k, num_experts, block_m))
+
+
+def eng_moe_align(ids_dev: int, num_tokens: int, top_k: int, num_experts: int, block_m: int, sorted_ids_dev: int,
+                  block_expert_dev: int, info_dev: int, stream: int | None = None):
+    _check(None, lib().eng_moe_align(ids_dev, num_tokens, top_k, num_experts, block_m, sorted_ids_dev,
+                                     block_expert_dev, info_dev, stream))
+
+
+def eng_moe_workspace_bytes(num_tokens: int, top_k: int, num_experts: int, hidden: int, inter: int) -> int:
+    return int(lib().eng_moe_workspace_bytes(num_tokens, top_k, num_experts, hidden, inter))
+
+
+def eng_moe_mlp(x_dev: int, gate_up_dev: int, down_dev: int, weights_dev: int, ids_dev: int, num_tokens: int,
+                hidden: int, inter: int, num_experts: int, top_k: int, out_dev: int, workspace_dev: int,
+                workspace_bytes: int, stream: int | None = None):
+    _check(None, lib().eng_moe_mlp(x_dev, gate_up_dev, down_dev, weights_dev, ids_dev, num_tokens, hidden, inter,
+                                   num_experts, top_k, out_dev, workspace_dev, workspace_bytes, stream))

@@ -390,6 +390,58 @@ int eng_sample_filtered(const float* logits_dev, int32_t rows, int32_t vocab, co
  */
 int eng_exp_f32(const float* d_dev, float* out_dev, int64_t n, void* stream);
 
+/* ---------------------------------------------------------------- a mixture-of-experts layer
+ * "33. Removing overhead", section "A MoE layer that never asks the host": the assignments (token, slot)
+ * are grouped by expert on the device, each group padded to whole blocks, and one grouped GEMM multiplies
+ * every block by its expert's weights.  These are standalone calls (no engine configuration has experts):
+ * every pointer is device memory, nothing is allocated or synchronised, and every launch's shape depends only
+ * on the token count N, the experts per token k, the expert count E and the block size, so the calls can be
+ * captured in a CUDA graph.  Expert weights are bf16 (16-bit patterns); gate_up[e] holds the expert's gate
+ * rows first, then its up rows; the activation is silu(gate) * up.
+ */
+
+/*
+ * eng_moe_route -- for each token row t: logits x[t] . w_router[e] (bf16 operands, float32 accumulation),
+ * softmax over the E experts, the top_k most probable experts (ties to the lower id, most probable first)
+ * and their probabilities renormalised to sum to 1 (Qwen3-MoE's router; the pages call it from a chapter
+ * not included).  x: bf16 [N][hidden]; w_router: bf16 [E][hidden]; weights: float [N][top_k]; expert_ids:
+ * int32 [N][top_k].  hidden % 8 == 0, 1 <= top_k <= min(32, E), E <= 4096.  Errors: ENG_EINVAL, ENG_ECUDA.
+ */
+int eng_moe_route(const void* x, const void* w_router, int32_t num_tokens, int32_t hidden, int32_t num_experts,
+                  int32_t top_k, float* weights, int32_t* expert_ids, void* stream);
+
+/* Rows of the grouped layout: N k assignments plus block_m - 1 padding rows per expert, in whole blocks. */
+int64_t eng_moe_padded_rows(int32_t num_tokens, int32_t top_k, int32_t num_experts, int32_t block_m);
+
+/*
+ * eng_moe_align -- group the flat assignments a = t * top_k + j by expert.  expert_ids: int32 [N][top_k].
+ * sorted_ids: int32 [M], M = eng_moe_padded_rows(...): the assignment each row of the grouped GEMM handles,
+ * expert 0's group first, ascending inside a group, N * top_k on a padding row.  block_expert: int32
+ * [M / block_m]: the expert owning each block (E - 1 for blocks past the groups).  info: int32 [2]:
+ * [0] the rows the groups occupy (a multiple of block_m), [1] the assignments whose expert id is outside
+ * [0, E) (placed in no group).  E <= 1024.  Errors: ENG_EINVAL, ENG_ECUDA.
+ */
+int eng_moe_align(const int32_t* expert_ids, int32_t num_tokens, int32_t top_k, int32_t num_experts, int32_t block_m,
+                  int32_t* sorted_ids, int32_t* block_expert, int32_t* info, void* stream);
+
+/* Bytes of device workspace eng_moe_mlp needs for these sizes. */
+int64_t eng_moe_workspace_bytes(int32_t num_tokens, int32_t top_k, int32_t num_experts, int32_t hidden,
+                                int32_t inter);
+
+/*
+ * eng_moe_mlp -- out[t] = sum over j < top_k (in order) of weights[t][j] * down[e] (silu(gate[e] x[t]) *
+ * up[e] x[t]), e = expert_ids[t][j]: eng_moe_align with blocks of 16 rows, then one grouped tensor-core GEMM
+ * for gate|up with SiLU * up fused (the products in float32, kept as bf16 hi/lo pairs), one for down scaled
+ * by the router weight, and the sum of each token's assignment rows.  x: bf16 [N][hidden]; gate_up: bf16
+ * [E][2 inter][hidden]; down: bf16 [E][hidden][inter]; weights: float [N][top_k]; expert_ids: int32
+ * [N][top_k] in [0, E) (an id outside adds nothing); out: float [N][hidden].  hidden % 64 == 0,
+ * inter % 64 == 0, E <= 1024.  workspace: device memory of at least eng_moe_workspace_bytes(...) bytes,
+ * owned by the caller and not shared by overlapping calls.  Errors: ENG_EINVAL, ENG_ECUDA.
+ */
+int eng_moe_mlp(const void* x, const void* gate_up, const void* down, const float* weights, const int32_t* expert_ids,
+                int32_t num_tokens, int32_t hidden, int32_t inter, int32_t num_experts, int32_t top_k, float* out,
+                void* workspace, int64_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
