@@ -470,6 +470,20 @@ def run_mixed(steps: int, warmup: int, local_rank: int) -> dict:
         stream.synchronize()
     t_e2e = (time.perf_counter() - t0) / steps
     h2d = eng.eng_last_step_info(h).h2d_bytes
+    # the same step on piecewise graphs: the projections of a bucket of the step's token count replayed,
+    # attention between
+    eng.eng_capture_mixed(h, [T])
+    for _ in range(warmup):
+        eng.eng_step(h, st, ids_dev.data_ptr(), None)
+    torch.cuda.synchronize()
+    assert eng.eng_last_step_info(h).replayed == 2
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(steps):
+            eng.eng_step(h, st, ids_dev.data_ptr(), None)
+        e1.record()
+    torch.cuda.synchronize()
+    t_pw = e0.elapsed_time(e1) / 1e3 / steps
     clk = clocks.stop()
     status = eng.eng_status(h, True)
     eng.eng_destroy(h)
@@ -488,6 +502,9 @@ def run_mixed(steps: int, warmup: int, local_rank: int) -> dict:
                               "of": peaks["source"] + " (sustained bf16 for the tensor bound)"},
             "e2e": {"value": T / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": 4 * (P + 32)},
+            "piecewise": {"ms_per_step": t_pw * 1e3, "value": T / t_pw, "unit": "tokens/s",
+                          "frac": max(t_b, t_f) / t_pw, "bucket_tokens": T,
+                          "note": "projection pieces replayed as graphs, attention and LM head launched between"},
             "gpu_launches": steps * launches, "clocks": clk, "device_status": status}
 
 

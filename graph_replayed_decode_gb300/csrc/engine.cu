@@ -171,6 +171,9 @@ struct eng {
   // graphs
   std::map<int, cudaGraphExec_t> graphs;
   std::map<int, int> graph_launches;
+  // piecewise graphs of mixed steps: token bucket -> the L + 1 projection pieces (enqueue_piece)
+  std::map<int, std::vector<cudaGraphExec_t>> pieces;
+  std::map<int, int> piece_launches;
   bool eager_only = false;
   bool pdl = false;
   bool l2_prefetch = true;
@@ -758,6 +761,195 @@ static int ds_schedule(eng_t* e, int T, int** d_off, int** d_items) {
 // Enqueues one forward over T packed tokens of R requests; requests [0, P) go to the packed prefill
 // kernel (n_items work items), [P, R) to the decode kernel with `splits` splits per row.  With
 // `advance`, a decode-only step ends by feeding its sampled ids back as the next inputs (advance.cu).
+// Piece `piece` of a step's forward over T tokens: the projections between two attention launches.
+// Piece 0 is the embedding and layer 0's input norm + QKV projection (QK-norm, RoPE, paged KV write);
+// piece l (1 <= l < L) is layer l - 1's output projection, gate|up and down and layer l's QKV; piece L is
+// the last layer's output projection, gate|up and down.  An eager step runs the pieces with the attention
+// launches between them; piecewise graphs ("(7) Graph Mode", section PIECEWISE) record the same calls.
+static cudaError_t enqueue_piece(eng_t* e, int T, int piece, cudaStream_t st) {
+  const eng_config_t& c = e->c;
+  const int H = c.hidden, d = c.head_dim, Hq = c.q_heads, Hkv = c.kv_heads;
+  int* in = e->d_in;
+  const size_t plane = (size_t)(c.num_blocks + 1) * Hkv * 16 * d;
+  LaunchOpts o;
+  o.pdl = e->pdl;
+  cudaError_t r;
+  int sq_parts = 1;  // producers of the residual's partial sums: embed (1), then o_proj / down row groups
+  if (piece == 0) {
+    EmbedParams ep{};
+    ep.embed = e->embed;
+    ep.ids = in + e->in.ids;
+    ep.h_out = e->h;
+    ep.sq_out = e->sq;
+    ep.sq_stride = e->sq_stride;
+    ep.norm_w = e->layers[0].in_norm;
+    ep.prev_row = in + e->in.prev;
+    ep.prev_ids = e->ids;
+    ep.prev_rows = c.max_reqs;
+    ep.xh_out = e->xn_h;
+    ep.xl_out = e->xn_l;
+    ep.rows = T;
+    ep.H = H;
+    ep.V = c.vocab;
+    ep.status = e->status;
+    e->launches++;
+    prof_begin(e, st, ENG_K_EMBED_NORM, (int64_t)T * H * (2 + 4 + 4));
+    r = launch_embed(ep, o, st);
+    prof_end(e, st);
+    if (r != cudaSuccess) return r;
+  } else {
+    const int l = piece - 1;
+    const Layer& L = e->layers[l];
+    // ---- output projection + residual (+ sums of squares for the next norm)
+    GemmParams po = gemm_params(e, e->g_o, L.o, T);
+    po.Xh = e->attn_h;
+    po.Xl = e->attn_l;
+    po.resid = e->h;
+    po.sq_out = e->sq;
+    po.next_norm_w = L.post_norm;
+    po.xh_out = e->xn_h;
+    po.xl_out = e->xn_l;
+    set_prefetch(e, po.pf_ptr, po.pf_bytes, L.down, e->g_down);
+    if ((r = gemm_launch(e, po, e->g_o, EPI_RESID, false, ENG_K_GEMM_O, st, &L.m_o, &e->m_attn_h, &e->m_attn_l)) !=
+        cudaSuccess)
+      return r;
+
+    // ---- post-attention RMSNorm + fused gate|up projection + SiLU * up
+    GemmParams pg = gemm_params(e, e->g_gu, L.gu, T);
+    pg.Xh = e->xn_h;
+    pg.Xl = e->xn_l;
+    pg.sq_in = e->sq;
+    pg.sq_parts = e->g_o.groups(T);
+    pg.xh_out = e->act_h;
+    pg.xl_out = e->act_l;
+    if (l + 1 < c.layers) set_prefetch(e, pg.pf_ptr, pg.pf_bytes, e->layers[l + 1].qkv, e->g_qkv);
+    if ((r = gemm_launch(e, pg, e->g_gu, EPI_SILU, true, ENG_K_GEMM_GATE_UP, st, &L.m_gu, &e->m_xn_h, &e->m_xn_l)) !=
+        cudaSuccess)
+      return r;
+
+    // ---- down projection + residual
+    GemmParams pd = gemm_params(e, e->g_down, L.down, T);
+    pd.Xh = e->act_h;
+    pd.Xl = e->act_l;
+    pd.resid = e->h;
+    pd.sq_out = e->sq;
+    pd.next_norm_w = l + 1 < c.layers ? e->layers[l + 1].in_norm : e->final_norm;
+    pd.xh_out = e->xn_h;
+    pd.xl_out = e->xn_l;
+    if ((r = gemm_launch(e, pd, e->g_down, EPI_RESID, false, ENG_K_GEMM_DOWN, st, &L.m_down, &e->m_act_h,
+                         &e->m_act_l)) != cudaSuccess)
+      return r;
+    sq_parts = e->g_down.groups(T);
+  }
+  if (piece == c.layers) return cudaSuccess;
+
+  const int l = piece;
+  const Layer& L = e->layers[l];
+  bf16* kplane = e->kv + (size_t)l * 2 * plane;
+  bf16* vplane = kplane + plane;
+  // ---- input RMSNorm + fused QKV projection + QK-norm + RoPE + paged KV write
+  GemmParams q = gemm_params(e, e->g_qkv, L.qkv, T);
+  q.Xh = e->xn_h;
+  q.Xl = e->xn_l;
+  q.sq_in = e->sq;
+  q.sq_parts = sq_parts;
+  q.bias = L.qkv_bias;
+  q.positions = in + e->in.pos;
+  q.tok2req = in + e->in.tok2req;
+  q.seq_lens = in + e->in.seq;
+  q.bt = in + e->in.bt;
+  q.mbs = c.max_blocks_per_seq;
+  q.q_norm = L.q_norm;
+  q.k_norm = L.k_norm;
+  q.cos_sin = e->rope;
+  q.max_pos = e->max_pos;
+  q.q_out = e->q;
+  q.k_pool = kplane;
+  q.v_pool = vplane;
+  q.slots = e->slots;
+  q.Hq = Hq;
+  q.Hkv = Hkv;
+  q.d = d;
+  q.NB = c.num_blocks;
+  set_prefetch(e, q.pf_ptr, q.pf_bytes, L.o, e->g_o);
+  return gemm_launch(e, q, e->g_qkv, EPI_QKV_ROPE, true, ENG_K_GEMM_QKV, st, &L.m_qkv, &e->m_xn_h, &e->m_xn_l);
+}
+
+// Layer l's attention over the staged step: the packed prefill kernel for the first P requests (n_items work
+// items) and the split decode kernel for requests P .. R - 1.
+static cudaError_t enqueue_attention(eng_t* e, int l, int R, int P, int n_items, int splits, cudaStream_t st) {
+  const eng_config_t& c = e->c;
+  const int d = c.head_dim, Hq = c.q_heads, Hkv = c.kv_heads;
+  int* in = e->d_in;
+  const size_t plane = (size_t)(c.num_blocks + 1) * Hkv * 16 * d;
+  const int64_t kv_tok = (int64_t)2 * Hkv * d * 2;  // K and V bytes of one position in one layer
+  int64_t kv_read = 0;                              // decode rows' K/V bytes per layer (profiling only)
+  if (e->prof_on)
+    for (int v : e->dec_seq) kv_read += (int64_t)v * kv_tok;
+  LaunchOpts o;
+  o.pdl = e->pdl;
+  cudaError_t r;
+  const Layer& L = e->layers[l];
+  bf16* kplane = e->kv + (size_t)l * 2 * plane;
+  bf16* vplane = kplane + plane;
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)d);
+  if (P > 0) {
+    AttnPrefillParams ap{};
+    ap.q = e->q;
+    ap.k_pool = kplane;
+    ap.v_pool = vplane;
+    ap.bt = in + e->in.bt;
+    ap.mbs = c.max_blocks_per_seq;
+    ap.positions = in + e->in.pos;
+    ap.items = reinterpret_cast<const int4*>(in + e->in.items);
+    ap.n_items = n_items;
+    ap.out_h = e->attn_h;
+    ap.out_l = e->attn_l;
+    ap.Hq = Hq;
+    ap.Hkv = Hkv;
+    ap.d = d;
+    ap.NB = c.num_blocks;
+    ap.scale_log2 = scale_log2;
+    ap.status = e->status;
+    e->launches++;
+    prof_begin(e, st, ENG_K_ATTN_PREFILL, 0);
+    r = launch_attn_prefill(ap, o, st);
+    prof_end(e, st);
+    if (r != cudaSuccess) return r;
+  }
+  if (R > P) {
+    AttnDecodeParams dp{};
+    dp.q = e->q;
+    dp.k_pool = kplane;
+    dp.v_pool = vplane;
+    dp.bt = in + e->in.bt;
+    dp.mbs = c.max_blocks_per_seq;
+    dp.seq_lens = in + e->in.seq;
+    dp.cu = in + e->in.cu;
+    dp.r0 = P;
+    dp.rows = R - P;
+    dp.out_h = e->attn_h;
+    dp.out_l = e->attn_l;
+    dp.Hq = Hq;
+    dp.Hkv = Hkv;
+    dp.d = d;
+    dp.NB = c.num_blocks;
+    dp.split_blocks = e->split_blocks;
+    dp.max_splits = splits;
+    dp.ws = e->attn_ws;
+    dp.counters = e->attn_counters;
+    dp.scale_log2 = scale_log2;
+    dp.status = e->status;
+    set_prefetch(e, dp.pf_ptr, dp.pf_bytes, L.gu, e->g_gu);
+    e->launches++;
+    prof_begin(e, st, ENG_K_ATTN_DECODE, kv_read + (int64_t)(R - P) * Hq * d * 8);
+    r = launch_attn_decode(dp, o, st);
+    prof_end(e, st);
+    if (r != cudaSuccess) return r;
+  }
+  return cudaSuccess;
+}
+
 static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, int splits, bool advance,
                                    cudaStream_t st) {
   const eng_config_t& c = e->c;
@@ -835,164 +1027,11 @@ static cudaError_t enqueue_forward(eng_t* e, int T, int R, int P, int n_items, i
     return enqueue_tail(e, T, R, 1, advance, st);
   }
 
-  EmbedParams ep{};
-  ep.embed = e->embed;
-  ep.ids = in + e->in.ids;
-  ep.h_out = e->h;
-  ep.sq_out = e->sq;
-  ep.sq_stride = e->sq_stride;
-  ep.norm_w = e->layers[0].in_norm;
-  ep.prev_row = in + e->in.prev;
-  ep.prev_ids = e->ids;
-  ep.prev_rows = c.max_reqs;
-  ep.xh_out = e->xn_h;
-  ep.xl_out = e->xn_l;
-  ep.rows = T;
-  ep.H = H;
-  ep.V = c.vocab;
-  ep.status = e->status;
-  e->launches++;
-  prof_begin(e, st, ENG_K_EMBED_NORM, (int64_t)T * H * (2 + 4 + 4));
-  r = launch_embed(ep, o, st);
-  prof_end(e, st);
-  if (r != cudaSuccess) return r;
-  int sq_parts = 1;  // producers of the residual's partial sums: embed (1), then o_proj / down row groups
-
-  for (int l = 0; l < c.layers; ++l) {
-    const Layer& L = e->layers[l];
-    bf16* kplane = e->kv + (size_t)l * 2 * plane;
-    bf16* vplane = kplane + plane;
-
-    // ---- input RMSNorm + fused QKV projection + QK-norm + RoPE + paged KV write
-    GemmParams q = gemm_params(e, e->g_qkv, L.qkv, T);
-    q.Xh = e->xn_h;
-    q.Xl = e->xn_l;
-    q.sq_in = e->sq;
-    q.sq_parts = sq_parts;
-    q.bias = L.qkv_bias;
-    q.positions = in + e->in.pos;
-    q.tok2req = in + e->in.tok2req;
-    q.seq_lens = in + e->in.seq;
-    q.bt = in + e->in.bt;
-    q.mbs = c.max_blocks_per_seq;
-    q.q_norm = L.q_norm;
-    q.k_norm = L.k_norm;
-    q.cos_sin = e->rope;
-    q.max_pos = e->max_pos;
-    q.q_out = e->q;
-    q.k_pool = kplane;
-    q.v_pool = vplane;
-    q.slots = e->slots;
-    q.Hq = Hq;
-    q.Hkv = Hkv;
-    q.d = d;
-    q.NB = c.num_blocks;
-    set_prefetch(e, q.pf_ptr, q.pf_bytes, L.o, e->g_o);
-    if ((r = gemm_launch(e, q, e->g_qkv, EPI_QKV_ROPE, true, ENG_K_GEMM_QKV, st, &L.m_qkv, &e->m_xn_h, &e->m_xn_l)) !=
-        cudaSuccess)
-      return r;
-
-    // ---- attention, split by kind inside the step
-    const float scale_log2 = 1.4426950408889634f / sqrtf((float)d);
-    if (P > 0) {
-      AttnPrefillParams ap{};
-      ap.q = e->q;
-      ap.k_pool = kplane;
-      ap.v_pool = vplane;
-      ap.bt = in + e->in.bt;
-      ap.mbs = c.max_blocks_per_seq;
-      ap.positions = in + e->in.pos;
-      ap.items = reinterpret_cast<const int4*>(in + e->in.items);
-      ap.n_items = n_items;
-      ap.out_h = e->attn_h;
-      ap.out_l = e->attn_l;
-      ap.Hq = Hq;
-      ap.Hkv = Hkv;
-      ap.d = d;
-      ap.NB = c.num_blocks;
-      ap.scale_log2 = scale_log2;
-      ap.status = e->status;
-      e->launches++;
-      prof_begin(e, st, ENG_K_ATTN_PREFILL, 0);
-      r = launch_attn_prefill(ap, o, st);
-      prof_end(e, st);
-      if (r != cudaSuccess) return r;
-    }
-    if (R > P) {
-      AttnDecodeParams dp{};
-      dp.q = e->q;
-      dp.k_pool = kplane;
-      dp.v_pool = vplane;
-      dp.bt = in + e->in.bt;
-      dp.mbs = c.max_blocks_per_seq;
-      dp.seq_lens = in + e->in.seq;
-      dp.cu = in + e->in.cu;
-      dp.r0 = P;
-      dp.rows = R - P;
-      dp.out_h = e->attn_h;
-      dp.out_l = e->attn_l;
-      dp.Hq = Hq;
-      dp.Hkv = Hkv;
-      dp.d = d;
-      dp.NB = c.num_blocks;
-      dp.split_blocks = e->split_blocks;
-      dp.max_splits = splits;
-      dp.ws = e->attn_ws;
-      dp.counters = e->attn_counters;
-      dp.scale_log2 = scale_log2;
-      dp.status = e->status;
-      set_prefetch(e, dp.pf_ptr, dp.pf_bytes, L.gu, e->g_gu);
-      e->launches++;
-      prof_begin(e, st, ENG_K_ATTN_DECODE, kv_read + (int64_t)(R - P) * Hq * d * 8);
-      r = launch_attn_decode(dp, o, st);
-      prof_end(e, st);
-      if (r != cudaSuccess) return r;
-    }
-
-    // ---- output projection + residual (+ sums of squares for the next norm)
-    GemmParams po = gemm_params(e, e->g_o, L.o, T);
-    po.Xh = e->attn_h;
-    po.Xl = e->attn_l;
-    po.resid = e->h;
-    po.sq_out = e->sq;
-    po.next_norm_w = L.post_norm;
-    po.xh_out = e->xn_h;
-    po.xl_out = e->xn_l;
-    set_prefetch(e, po.pf_ptr, po.pf_bytes, L.down, e->g_down);
-    if ((r = gemm_launch(e, po, e->g_o, EPI_RESID, false, ENG_K_GEMM_O, st, &L.m_o, &e->m_attn_h, &e->m_attn_l)) !=
-        cudaSuccess)
-      return r;
-    sq_parts = e->g_o.groups(T);
-
-    // ---- post-attention RMSNorm + fused gate|up projection + SiLU * up
-    GemmParams pg = gemm_params(e, e->g_gu, L.gu, T);
-    pg.Xh = e->xn_h;
-    pg.Xl = e->xn_l;
-    pg.sq_in = e->sq;
-    pg.sq_parts = sq_parts;
-    pg.xh_out = e->act_h;
-    pg.xl_out = e->act_l;
-    if (l + 1 < c.layers) set_prefetch(e, pg.pf_ptr, pg.pf_bytes, e->layers[l + 1].qkv, e->g_qkv);
-    if ((r = gemm_launch(e, pg, e->g_gu, EPI_SILU, true, ENG_K_GEMM_GATE_UP, st, &L.m_gu, &e->m_xn_h, &e->m_xn_l)) !=
-        cudaSuccess)
-      return r;
-
-    // ---- down projection + residual
-    GemmParams pd = gemm_params(e, e->g_down, L.down, T);
-    pd.Xh = e->act_h;
-    pd.Xl = e->act_l;
-    pd.resid = e->h;
-    pd.sq_out = e->sq;
-    pd.next_norm_w = l + 1 < c.layers ? e->layers[l + 1].in_norm : e->final_norm;
-    pd.xh_out = e->xn_h;
-    pd.xl_out = e->xn_l;
-    if ((r = gemm_launch(e, pd, e->g_down, EPI_RESID, false, ENG_K_GEMM_DOWN, st, &L.m_down, &e->m_act_h,
-                         &e->m_act_l)) != cudaSuccess)
-      return r;
-    sq_parts = e->g_down.groups(T);
+  for (int l = 0; l <= c.layers; ++l) {
+    if ((r = enqueue_piece(e, T, l, st)) != cudaSuccess) return r;
+    if (l < c.layers && (r = enqueue_attention(e, l, R, P, n_items, splits, st)) != cudaSuccess) return r;
   }
-
-  return enqueue_tail(e, T, R, sq_parts, advance, st);
+  return enqueue_tail(e, T, R, e->g_down.groups(T), advance, st);
 }
 
 // The end of a step: final RMSNorm at each request's last token, LM head and sampling, the optional
@@ -1163,6 +1202,8 @@ void eng_destroy(eng_t* e) {
   if (!e) return;
   if (e->stream) cudaStreamSynchronize(e->stream);
   for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : e->pieces)
+    for (cudaGraphExec_t g : kv.second) cudaGraphExecDestroy(g);
   for (cudaEvent_t ev : e->prof_ev) cudaEventDestroy(ev);
   for (int i = 0; i < kSlots; ++i) {
     if (e->ev[i]) cudaEventDestroy(e->ev[i]);
@@ -1310,6 +1351,63 @@ int eng_capture(eng_t* e, const int32_t* sizes, int32_t n) {
   return ENG_OK;
 }
 
+int eng_capture_mixed(eng_t* e, const int32_t* token_buckets, int32_t n) {
+  if (!e || !token_buckets || n < 1) return e ? fail(e, ENG_EINVAL, "bad mixed capture sizes") : ENG_EINVAL;
+  std::vector<int> v(token_buckets, token_buckets + n);
+  std::sort(v.begin(), v.end());
+  for (size_t i = 0; i < v.size(); ++i) {
+    if (v[i] < kTcPrefillTokens || v[i] > e->c.max_tokens)
+      return fail(e, ENG_EINVAL, "mixed capture size outside [" + std::to_string(kTcPrefillTokens) + ", max_tokens]");
+    if (i && v[i] == v[i - 1]) return fail(e, ENG_EINVAL, "duplicate mixed capture size");
+  }
+  CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+  const int L = e->c.layers;
+  for (int size : v) {
+    auto old = e->pieces.find(size);
+    if (old != e->pieces.end()) {
+      for (cudaGraphExec_t g : old->second) cudaGraphExecDestroy(g);
+      e->pieces.erase(old);
+    }
+    // every token a padding token of request 0 (length 0: its K/V go to the scratch block)
+    int k;
+    int* h = take_slot(e, &k);
+    stage_padding(e, h, 1);
+    for (int t = 0; t < size; ++t) {
+      h[e->in.ids + t] = 0;
+      h[e->in.pos + t] = 0;
+      h[e->in.prev + t] = -1;
+      h[e->in.tok2req + t] = 0;
+    }
+    TRY(push_slot(e, k, e->in.words));
+    for (int w = 0; w < 2; ++w)  // warm-up (lazy attribute setup, first touch)
+      for (int p = 0; p <= L; ++p) CUDA_OR_FAIL(e, enqueue_piece(e, size, p, e->stream));
+    CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+    std::vector<cudaGraphExec_t> execs;
+    int launches = 0;
+    for (int p = 0; p <= L; ++p) {
+      cudaGraph_t graph = nullptr;
+      CUDA_OR_FAIL(e, cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal));
+      e->launches = 0;
+      const cudaError_t le = enqueue_piece(e, size, p, e->cap_stream);
+      const cudaError_t ce = cudaStreamEndCapture(e->cap_stream, &graph);
+      cudaGraphExec_t exec = nullptr;
+      const cudaError_t ie = le == cudaSuccess && ce == cudaSuccess ? cudaGraphInstantiate(&exec, graph, 0) : le;
+      if (graph) cudaGraphDestroy(graph);
+      if (le != cudaSuccess || ce != cudaSuccess || ie != cudaSuccess) {
+        for (cudaGraphExec_t g : execs) cudaGraphExecDestroy(g);
+        return fail(e, ENG_ECUDA, std::string("piecewise capture failed: ") +
+                                      cudaGetErrorString(le != cudaSuccess ? le : ce != cudaSuccess ? ce : ie));
+      }
+      execs.push_back(exec);
+      launches += e->launches;
+    }
+    e->pieces[size] = execs;
+    e->piece_launches[size] = launches;
+  }
+  CUDA_OR_FAIL(e, cudaStreamSynchronize(e->stream));
+  return ENG_OK;
+}
+
 static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int32_t* out_ids_dev,
                      float* out_logits_dev) {
   if (!e) return ENG_EINVAL;
@@ -1377,6 +1475,17 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
   }
   const bool replay = bucket > 0;
   const int rows = replay ? bucket : R;  // rows staged (padding included)
+  // a mixed (or prefill) step of at least kTcPrefillTokens tokens replays the projection pieces of the smallest
+  // captured token bucket that holds it (same token class, so the same kernels and summation orders as the
+  // eager step); its padding tokens belong to request R, of length 0, so a free request row is needed
+  int tbucket = 0;
+  if (!decode_only && !e->eager_only && T >= kTcPrefillTokens && R < c.max_reqs) {
+    for (auto& kv : e->pieces)
+      if (kv.first >= T) {
+        tbucket = kv.first;
+        break;
+      }
+  }
 
   int k;
   int* h = take_slot(e, &k);
@@ -1401,6 +1510,15 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
     if (bs < c.max_blocks_per_seq) memset(row + bs, 0, (size_t)(c.max_blocks_per_seq - bs) * 4);
   }
   h[L.cu + R] = T;
+  if (tbucket) {  // token-bucket padding: token 0 at position 0 of request R, of length 0
+    for (int t = T; t < tbucket; ++t) {
+      h[L.ids + t] = 0;
+      h[L.pos + t] = 0;
+      h[L.prev + t] = -1;
+      h[L.tok2req + t] = R;
+    }
+    h[L.seq + R] = 0;
+  }
   for (int r = R; r < rows; ++r) {  // bucket padding: token 0, position 0, length 0
     h[L.ids + r] = 0;
     h[L.pos + r] = 0;
@@ -1440,6 +1558,17 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
   if (replay) {
     CUDA_OR_FAIL(e, cudaGraphLaunch(e->graphs[bucket], e->stream));
     e->launches = e->graph_launches[bucket];
+  } else if (tbucket) {
+    int max_blocks = 1;
+    for (int r = P; r < R; ++r) max_blocks = std::max(max_blocks, (s->seq_lens[r] + 15) / 16);
+    const int splits = (max_blocks + e->split_blocks - 1) / e->split_blocks;
+    const std::vector<cudaGraphExec_t>& pc = e->pieces[tbucket];
+    for (int l = 0; l <= c.layers; ++l) {
+      CUDA_OR_FAIL(e, cudaGraphLaunch(pc[l], e->stream));
+      if (l < c.layers) CUDA_OR_FAIL(e, enqueue_attention(e, l, R, P, n_items, splits, e->stream));
+    }
+    CUDA_OR_FAIL(e, enqueue_tail(e, tbucket, R, e->g_down.groups(tbucket), false, e->stream));
+    e->launches += e->piece_launches[tbucket];
   } else {
     int max_blocks = 1;
     for (int r = P; r < R; ++r) max_blocks = std::max(max_blocks, (s->seq_lens[r] + 15) / 16);
@@ -1450,8 +1579,8 @@ static int step_impl(eng_t* e, const eng_step_t* s, const int32_t* prev_row, int
   if (out_logits_dev)
     CUDA_OR_FAIL(e, cudaMemcpyAsync(out_logits_dev, e->logits, (size_t)R * c.vocab * 4, cudaMemcpyDeviceToDevice,
                                     e->stream));
-  e->last.replayed = replay ? 1 : 0;
-  e->last.bucket = rows;
+  e->last.replayed = replay ? 1 : tbucket ? 2 : 0;
+  e->last.bucket = tbucket ? tbucket : rows;
   e->last.launches = e->launches;
   e->last.num_prefill = P;
   e->last.h2d_bytes = (int64_t)words * 4;

@@ -80,6 +80,7 @@ SIGNATURES = [
     ("eng_create", ctypes.c_int, [ctypes.POINTER(eng_config_t), ctypes.POINTER(eng_tensor_t), ctypes.c_int32,
                                   ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
     ("eng_capture", ctypes.c_int, [ctypes.c_void_p, _I32P, ctypes.c_int32]),
+    ("eng_capture_mixed", ctypes.c_int, [ctypes.c_void_p, _I32P, ctypes.c_int32]),
     ("eng_step", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_t), ctypes.c_void_p, ctypes.c_void_p]),
     ("eng_step_async", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(eng_step_t), ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p]),
@@ -229,6 +230,12 @@ def eng_create(cfg: eng_config_t, weights: TensorList, cuda_stream: int | None =
 def eng_capture(e, sizes: Sequence[int]) -> None:
     s = _i32(sizes)
     _check(e, lib().eng_capture(e, _ptr_i32(s), len(s)))
+
+
+def eng_capture_mixed(e, token_buckets: Sequence[int]) -> None:
+    """Piecewise graphs of the projections of mixed steps, one set per token bucket."""
+    s = _i32(token_buckets)
+    _check(e, lib().eng_capture_mixed(e, _ptr_i32(s), len(s)))
 
 
 def eng_step(e, step: StepArrays, out_ids_dev: int, out_logits_dev: int | None = None) -> None:

@@ -133,8 +133,9 @@ typedef struct {
 
 /* What the last eng_step did (for tests and benchmarks). */
 typedef struct {
-  int32_t replayed;     /* 1: a captured graph was replayed; 0: kernels were launched eagerly */
-  int32_t bucket;       /* capture size replayed (or num_reqs when eager) */
+  int32_t replayed;     /* 1: a captured graph was replayed; 2: the projection pieces of a mixed step were
+                           replayed with attention launched between them (eng_capture_mixed); 0: eager */
+  int32_t bucket;       /* capture size replayed: requests, or tokens when piecewise (num_reqs when eager) */
   int32_t launches;     /* kernels launched (the graph's kernel count when replayed) */
   int32_t num_prefill;  /* requests routed to the packed prefill attention kernel */
   int64_t h2d_bytes;    /* bytes copied host -> device by the step */
@@ -170,6 +171,21 @@ int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_w
  * values in [1, max_reqs].  Synchronises the stream.  Errors: ENG_EINVAL, ENG_ECUDA.
  */
 int eng_capture(eng_t* e, const int32_t* sizes, int32_t n);
+
+/*
+ * eng_capture_mixed -- piecewise graphs for mixed (and prefill) steps ("(7) Graph Mode", section
+ * PIECEWISE: split at attention; "33. Removing overhead", section "CUDA graphs for a changing batch",
+ * the mixed-batch case).  For each token bucket, the step's projections are recorded as L + 1 graphs:
+ * the embedding and layer 0's QKV projection, then per layer the output projection, gate|up, down and the
+ * next layer's QKV projection.  A later eng_step that is not decode-only, with num_tokens in
+ * [65, bucket] and num_reqs < max_reqs, pads its tokens to the smallest such bucket (padding tokens belong
+ * to request num_reqs, of length 0, whose K/V go to the scratch block), replays the pieces and launches
+ * attention (packed prefill and split decode kernels, sized by the step's own composition) and the LM head
+ * eagerly between and after them.  Results are identical to the eager step's bit for bit: both token
+ * counts take the same kernels.  token_buckets: host int32[n], each in [65, max_tokens], distinct.
+ * Synchronises the engine's stream.  Errors: ENG_EINVAL, ENG_ECUDA.
+ */
+int eng_capture_mixed(eng_t* e, const int32_t* token_buckets, int32_t n);
 
 /*
  * eng_step -- run one packed step and write one sampled token id per request.

@@ -60,6 +60,9 @@ class GpuEngine:
     def capture(self, sizes):
         self.eng.eng_capture(self.h, sizes)
 
+    def capture_mixed(self, token_buckets):
+        self.eng.eng_capture_mixed(self.h, token_buckets)
+
     def alloc(self, n):
         return self.eng.eng_pool_alloc(self.h, n)
 

@@ -140,7 +140,8 @@ def test_dense_8b_batch64_context2048():
 
 def test_qwen2p5_1p5b_mixed_prefill_chunk_and_decode_rows():
     """Qwen2.5-1.5B shape: a 512-position chunk of fresh prompts (the last one cut) followed by 32 decode
-    rows at contexts from {64, 256, 1024, 4096}, greedy, in one packed step."""
+    rows at contexts from {64, 256, 1024, 4096}, greedy, in one packed step; eager, then on piecewise graphs
+    (bit-identical)."""
     from graph_replayed_decode_gb300.eng import StepArrays
     s = synth.shape("qwen2p5_1p5b")
     w = synth.make_weights(s, seed=0, norm_scale=0.1)
@@ -165,6 +166,13 @@ def test_qwen2p5_1p5b_mixed_prefill_chunk_and_decode_rows():
         temps = np.zeros(P + 32, dtype=np.float32)
         gid, glog = g.step(StepArrays(ids, pos, cu, bt, seq, temps))
         assert g.info().num_prefill == P and g.info().replayed == 0
+        # the same step on piecewise graphs (projection pieces of a 600-token bucket, attention between them)
+        # rewrites the same K/V and gives the same ids and logits bit for bit
+        g.capture_mixed([600])
+        pid, plog = g.step(StepArrays(ids, pos, cu, bt, seq, temps))
+        assert g.info().replayed == 2 and g.info().bucket == 600
+        np.testing.assert_array_equal(pid, gid)
+        np.testing.assert_array_equal(plog.view(np.uint32), glog.view(np.uint32))
         model = oracle.OracleModel(s, w, cache_layers=False)
         # the prompt chunks (fresh prompts: all their keys are in this step)
         pc = oracle.PagedCache(s, sum(need) + 4)

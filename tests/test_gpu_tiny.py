@@ -236,6 +236,70 @@ def test_mixed_step_prefill_chunks_and_decode_rows(weights):
         g.close()
 
 
+def test_piecewise_graphs_for_a_mixed_step(weights):
+    """eng_capture_mixed ("(7) Graph Mode", §PIECEWISE): a mixed step of 78 tokens (prompt chunks of 40 and
+    35 and three decode rows) replays the 128-token projection pieces with attention launched between them.
+    Ids, logits and KV slots equal the eager step's bit for bit, the next decode step agrees too (the pieces
+    wrote the same K/V, the padding tokens only the scratch block), and the logits match the oracle."""
+    import torch
+    from graph_replayed_decode_gb300.eng import StepArrays
+    from harness import device_view
+    pw, eg = _engine(weights), _engine(weights)
+    try:
+        pw.capture_mixed([128])
+        model = oracle.OracleModel(S, weights)
+        cache = oracle.PagedCache(S, NB)
+        ctxs = [17, 5, 31]
+        blocks = None
+        for g in (pw, eg):
+            b = [list(g.alloc(n)) for n in (3, 3, 2, 2, 3)]
+            assert blocks is None or b == blocks
+            blocks = b
+            for j, ctx in enumerate(ctxs):
+                for l in range(S.layers):
+                    g.fill_context(l, blocks[2 + j], synth.kv_context(S, l, 100 + j, ctx))
+        for r, b in enumerate(blocks):
+            cache.set_block_table(r, b)
+        for j, ctx in enumerate(ctxs):
+            for l in range(S.layers):
+                kv = synth.kv_context(S, l, 100 + j, ctx)
+                K = np.swapaxes(oracle.widen_bf16(kv[0]), 0, 1)
+                V = np.swapaxes(oracle.widen_bf16(kv[1]), 0, 1)
+                cache.write(l, 2 + j, np.arange(ctx), K, V)
+        bt = block_table(blocks, MBS)
+        ids = np.concatenate([synth.prompt_ids(40, S.vocab, 70), synth.prompt_ids(35, S.vocab, 71),
+                              synth.decode_ids(3, S.vocab, 6)])
+        pos = np.concatenate([np.arange(40), np.arange(35), np.array(ctxs)])
+        cu = np.array([0, 40, 75, 76, 77, 78])
+        seq = np.array([40, 35, 18, 6, 32])
+        temps = np.array([0.0, 0.8, 0.0, 1.1, 0.0], dtype=np.float32)
+        st = StepArrays(ids, pos, cu, bt, seq, temps, seed=4, offset=1)
+        pid, plog = pw.step(st)
+        info = pw.info()
+        assert info.replayed == 2 and info.bucket == 128 and info.num_prefill == 2
+        eid, elog = eg.step(st)
+        assert eg.info().replayed == 0 and info.launches == eg.info().launches   # the same kernels
+        np.testing.assert_array_equal(pid, eid)
+        np.testing.assert_array_equal(plog.view(np.uint32), elog.view(np.uint32))
+        slots = []
+        for g in (pw, eg):
+            sp, _ = g.eng.eng_debug_buffer(g.h, "slots")
+            slots.append(device_view(sp, 4 * len(ids), torch.int32).cpu().numpy())
+        np.testing.assert_array_equal(slots[0], slots[1])
+        olog = oracle.forward_step(model, cache, ids, pos, cu)
+        check_logits_and_ids(plog, pid, olog, temps, 4, 1)
+        # one decode step of every request, on the K/V each engine wrote
+        nxt = StepArrays(pid, seq, np.arange(6), bt, seq + 1, temps, seed=4, offset=2)
+        a_ids, a_log = pw.step(nxt)
+        b_ids, b_log = eg.step(nxt)
+        np.testing.assert_array_equal(a_ids, b_ids)
+        np.testing.assert_array_equal(a_log.view(np.uint32), b_log.view(np.uint32))
+        assert pw.status() == 0 and eg.status() == 0
+    finally:
+        pw.close()
+        eg.close()
+
+
 def test_step_does_not_wait_for_the_gpu(weights):
     """eng_step returns while earlier work on its stream is still running (no host sync in the step)."""
     import torch
