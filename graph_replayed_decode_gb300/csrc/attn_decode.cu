@@ -30,7 +30,7 @@ namespace cg = cooperative_groups;
 namespace grd {
 
 static constexpr int kStages = 2;    // K/V blocks in flight per warp
-static constexpr int kMaxSplits = 8;    // splits of one (row, KV head)
+static constexpr int kMaxSplits = kAttnMaxSplits;  // splits of one (row, KV head)
 static constexpr int kClusterSplits = 8;  // at most this many merge on chip (one thread-block cluster)
 
 // Per-warp K/V stages, reused for the warp merge afterwards ([4][16] M, [4][16] L, [4][16][D] O, [G][D+2]).

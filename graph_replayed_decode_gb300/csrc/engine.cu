@@ -516,7 +516,7 @@ static int setup_buffers(eng_t* e) {
 
   // decode attention splits: at most 8 per row (a small batch's splits then merge on chip); fixed per
   // engine, so eager and replayed steps agree bit for bit
-  e->split_blocks = (c.max_blocks_per_seq + 7) / 8;
+  e->split_blocks = (c.max_blocks_per_seq + kAttnMaxSplits - 1) / kAttnMaxSplits;
   e->max_splits = (c.max_blocks_per_seq + e->split_blocks - 1) / e->split_blocks;
   TRY(dev_alloc(e, &e->attn_ws, (size_t)Rm * c.kv_heads * e->max_splits * (c.q_heads / c.kv_heads) * (d + 2)));
   TRY(dev_alloc(e, &e->attn_counters, (size_t)Rm * c.kv_heads));

@@ -144,6 +144,8 @@ cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const Launch
                         const TcMaps* tc = nullptr);
 
 // ------------------------------------------------------------------ attention (attn_decode.cu, attn_prefill.cu)
+// Key splits of one (row, KV head) in decode attention (the block-table width divided into at most this many).
+constexpr int kAttnMaxSplits = 8;
 struct AttnDecodeParams {
   const float* q;         // [T][Hq][d]
   const bf16* k_pool;     // layer K plane
@@ -158,7 +160,7 @@ struct AttnDecodeParams {
   bf16* out_l;
   int Hq, Hkv, d, NB;
   int split_blocks;       // KV blocks per split
-  int max_splits;         // grid.z (<= 8)
+  int max_splits;         // splits of the grid (<= kAttnMaxSplits)
   float* ws;              // [rows][Hkv][max_splits][G][d + 2] partials of multi-split rows
   int* counters;          // [rows][Hkv] finished splits, zero between launches
   float scale_log2;       // log2(e) / sqrt(d)
