@@ -286,6 +286,7 @@ struct DsSmem {
   float* mrun;   // [8] online softmax state per head
   float* lrun;
   float* alpha;
+  float* rs;     // [8] 1 / rms of the staged rows (norm phases)
 };
 
 // ------------------------------------------------------------------ producer: weights and K/V into the ring
@@ -603,6 +604,15 @@ ENG_DEVICE bool ds_gemv(const DecodeStepParams& p, const DsSmem& S, int K, int n
   const int xrow = g < p.T ? g : 0;
   const uint4* xs = reinterpret_cast<const uint4*>(S.xs + (size_t)xrow * p.kx) + (lane & 3);
   const uint4* xl = reinterpret_cast<const uint4*>(S.xl + (size_t)xrow * p.kx) + (lane & 3);
+  // 1 / rms of the staged rows, by the last warp (it has the fewest k-tiles) before its MMA pass; the
+  // reduction's barrier below publishes it to the epilogue warps
+  if (norm && warp == kDsWarps - 1) {
+#pragma unroll 1
+    for (int t = 0; t < p.T; ++t) {
+      const float r_t = rsqrtf(ds_sumsq(S, t) / (float)K + p.eps);
+      if (lane == 0) S.rs[t] = r_t;
+    }
+  }
   bool ok = true;
   if (nch == 1 && n <= p.slots_n) {  // every tile's chunk fits in the ring at once
     float acc[kDsGroup][4][4];
@@ -690,15 +700,9 @@ ENG_DEVICE bool ds_gemv(const DecodeStepParams& p, const DsSmem& S, int K, int n
     float4 u[kDsWarps];
 #pragma unroll
     for (int w2 = 0; w2 < kDsWarps; ++w2) u[w2] = r[w2 * 32];
-    rs[0] = rs[1] = 1.f;
-    if (norm) {
-#pragma unroll 1
-      for (int t = 0; t < p.T; ++t) {
-        const float r_t = rsqrtf(ds_sumsq(S, t) / (float)K + p.eps);
-        if (t == 2 * (lane & 3)) rs[0] = r_t;
-        if (t == 2 * (lane & 3) + 1) rs[1] = r_t;
-      }
-    }
+    const int c = 2 * (lane & 3);
+    rs[0] = norm && c < p.T ? S.rs[c] : 1.f;
+    rs[1] = norm && c + 1 < p.T ? S.rs[c + 1] : 1.f;
     v = u[0];
 #pragma unroll
     for (int w2 = 1; w2 < kDsWarps; ++w2) {
@@ -1004,13 +1008,21 @@ ENG_DEVICE bool ds_attention(const DecodeStepParams& p, const DsSmem& S, int l, 
   }
   csync();
 #pragma unroll 1
-  for (int e = tid; e < G * d; e += kDsConsumers) {
-    const int h = e / d;
-    float acc = 0.f;
+  for (int e2 = tid; e2 < G * d / 2; e2 += kDsConsumers) {  // element pairs: one pass for G * d <= 448
+    const int e = 2 * e2, h = e / d;
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll 4
-    for (int sp = 0; sp < a.na - 1; ++sp) acc += f[sp * G + h] * S.mland[((size_t)sp * G + h) * wrow + (e - h * d)];
-    acc += f[(a.na - 1) * G + h] * own[e];
-    ll_store(out + e, acc, tag_out);
+    for (int sp = 0; sp < a.na - 1; ++sp) {
+      const float fs = f[sp * G + h];
+      const float2 m2 = *reinterpret_cast<const float2*>(S.mland + ((size_t)sp * G + h) * wrow + (e - h * d));
+      a0 += fs * m2.x;
+      a1 += fs * m2.y;
+    }
+    const float fo = f[(a.na - 1) * G + h];
+    a0 += fo * own[e];
+    a1 += fo * own[e + 1];
+    ll_store(out + e, a0, tag_out);
+    ll_store(out + e + 1, a1, tag_out);
   }
   return true;
 }
@@ -1165,7 +1177,7 @@ ENG_DEVICE void ds_consumer(const DecodeStepParams& p, const DsSmem& S, uint32_t
 __global__ void __launch_bounds__(kDsThreads, 1) k_decode_step(const __grid_constant__ DecodeStepParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) uint64_t s_full[kDsMaxSlots], s_empty[kDsMaxSlots];
-  __shared__ float s_m[8], s_l[8], s_alpha[8];
+  __shared__ float s_m[8], s_l[8], s_alpha[8], s_rs[8];
   __shared__ int s_ids[8], s_seq[8], s_pos[8];
   __shared__ uint32_t s_issued, s_consumed;
   const int G = p.Hq / p.Hkv;
@@ -1204,6 +1216,7 @@ __global__ void __launch_bounds__(kDsThreads, 1) k_decode_step(const __grid_cons
   S.mrun = s_m;
   S.lrun = s_l;
   S.alpha = s_alpha;
+  S.rs = s_rs;
   const uint32_t epoch = ld_relaxed_u32(p.epoch);
   if (threadIdx.x == 0 && blockIdx.x == 0) g_ds_blockdiag = p.diag ? p.diag + 4 : nullptr;
   if (threadIdx.x == 0) {
