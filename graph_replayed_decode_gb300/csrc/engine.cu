@@ -136,7 +136,8 @@ struct eng {
   GemmSite g_qkv, g_o, g_gu, g_down, g_lm;
   CUtensorMap m_xn_h{}, m_xn_l{}, m_attn_h{}, m_attn_l{}, m_act_h{}, m_act_l{};  // activation planes (TC path)
   int split_blocks = 4, max_splits = 1;
-  float* attn_ws = nullptr;    // decode attention partials of multi-split rows
+  int attn_flat = 0;           // CTAs of the flat-partition decode attention
+  float* attn_ws = nullptr;    // its partials of segments split between warps
   int* attn_counters = nullptr;
   int* ring = nullptr;  // [ring_cap][bucket] ids recorded by the advance kernel
   int ring_cap = 1024;
@@ -514,11 +515,16 @@ static int setup_buffers(eng_t* e) {
   e->sq_stride = std::max(e->g_o.max_groups(), e->g_down.max_groups());
   TRY(dev_alloc(e, &e->sq, (size_t)Tm * e->sq_stride));
 
-  // decode attention splits: at most 8 per row (a small batch's splits then merge on chip); fixed per
-  // engine, so eager and replayed steps agree bit for bit
+  // decode attention: a few rows split each row's blocks into at most 8 splits merged on chip; more rows
+  // take the flat partition over a grid of the CTAs resident at once.  Both are fixed per engine, so eager
+  // and replayed steps agree bit for bit.
   e->split_blocks = (c.max_blocks_per_seq + kAttnMaxSplits - 1) / kAttnMaxSplits;
   e->max_splits = (c.max_blocks_per_seq + e->split_blocks - 1) / e->split_blocks;
-  TRY(dev_alloc(e, &e->attn_ws, (size_t)Rm * c.kv_heads * e->max_splits * (c.q_heads / c.kv_heads) * (d + 2)));
+  e->attn_flat = attn_flat_ctas(d, Rm, e->sms);
+  if (e->attn_flat < 1) return fail(e, ENG_ECUDA, "occupancy query of the decode attention kernel failed");
+  if ((int64_t)c.kv_heads * Rm * (c.max_blocks_per_seq + 8) >= (1ll << 30))
+    return fail(e, ENG_EINVAL, "kv_heads * max_reqs * max_blocks_per_seq too large for decode attention");
+  TRY(dev_alloc(e, &e->attn_ws, ((size_t)Rm * c.kv_heads + 4 * (size_t)e->attn_flat) * (c.q_heads / c.kv_heads) * (d + 2)));
   TRY(dev_alloc(e, &e->attn_counters, (size_t)Rm * c.kv_heads));
 
   e->used.assign(c.num_blocks, 0);
@@ -938,6 +944,7 @@ static cudaError_t enqueue_attention(eng_t* e, int l, int R, int P, int n_items,
     dp.max_splits = splits;
     dp.ws = e->attn_ws;
     dp.counters = e->attn_counters;
+    dp.flat_ctas = e->attn_flat;
     dp.scale_log2 = scale_log2;
     dp.status = e->status;
     set_prefetch(e, dp.pf_ptr, dp.pf_bytes, L.gu, e->g_gu);

@@ -66,7 +66,8 @@ struct GemmSmem {
 };
 
 static constexpr size_t kTmaMaxBytes = 128 * 1024;
-static constexpr size_t kSmemBudget = 200 * 1024;  // dynamic shared memory a GEMM CTA may use
+static constexpr size_t kSmemBudget = 200 * 1024;     // dynamic shared memory a tensor-core GEMM CTA may use
+static constexpr size_t kSmemBudgetMma = 216 * 1024;  // and a warp-MMA one (its static arrays take under 8 KB)
 
 // Split-K: CTA `split` of a cluster finishes the block of kblk consecutive tokens starting at split * kblk
 // (a multiple of 4, so that partial sums move between CTAs as 16-byte vectors).
@@ -94,7 +95,7 @@ __host__ __device__ inline GemmSmem gemm_smem(int NT, int RG, int ktn, int S) {
   m.recv_off = m.x_bytes > tail ? m.x_bytes : tail;
   m.recv_off = (m.recv_off + 15) & ~(size_t)15;
   m.total = m.w_bytes + m.recv_off + m.recv_bytes;
-  if (m.tma && m.total > kSmemBudget) {  // too big with the weights staged: stream them through registers
+  if (m.tma && m.total > kSmemBudgetMma) {  // too big with the weights staged: stream them through registers
     m.tma = false;
     m.total -= m.w_bytes;
     m.w_bytes = 0;
@@ -577,8 +578,8 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
       *reinterpret_cast<float4*>(cluster.map_shared_rank(recv, q) + ((size_t)split * rows + r) * kblk + 4 * c) = v;
     }
     cluster.sync();
-    for (int i = threadIdx.x; i < rows * nown; i += 256) {
-      const int k = i / rows, r = i - k * rows;
+    for (int i = threadIdx.x; i < rows * nown; i += 256) {  // consecutive threads: consecutive tokens of a row
+      const int r = i / nown, k = i - r * nown;
       const int tok = tok_first + k;
       float v = 0.f;
       for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kblk + k];
@@ -857,7 +858,7 @@ static cudaError_t launch_nt(const GemmParams& p, const LaunchOpts& o, cudaStrea
   if constexpr (TC)
     ae = ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<EPI, NORM_IN>), (int)kSmemBudget);
   else
-    ae = ensure_smem_limit(reinterpret_cast<const void*>(k_gemm<NT, EPI, NORM_IN>), (int)kSmemBudget);
+    ae = ensure_smem_limit(reinterpret_cast<const void*>(k_gemm<NT, EPI, NORM_IN>), (int)kSmemBudgetMma);
   if (ae != cudaSuccess) return ae;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;

@@ -161,14 +161,18 @@ struct AttnDecodeParams {
   int Hq, Hkv, d, NB;
   int split_blocks;       // KV blocks per split
   int max_splits;         // splits of the grid (<= kAttnMaxSplits)
-  float* ws;              // [rows][Hkv][max_splits][G][d + 2] partials of multi-split rows
-  int* counters;          // [rows][Hkv] finished splits, zero between launches
+  float* ws;              // flat partition: [rows * Hkv + 4 * flat_ctas][G][d + 2] partials of split segments
+  int* counters;          // [rows][Hkv] finished pieces, zero between launches
+  int flat_ctas;          // grid of the flat partition (more than 4 rows): CTAs resident at once
   float scale_log2;       // log2(e) / sqrt(d)
   const void* pf_ptr;     // weights of a later kernel to prefetch into L2
   unsigned long long pf_bytes;
   int* status;
 };
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, cudaStream_t s);
+// CTAs of the flat-partition kernel that are resident at once on a device of `sms` SMs, for launches of up
+// to `rows` rows (0 if the occupancy query fails).
+int attn_flat_ctas(int d, int rows, int sms);
 
 struct AttnPrefillParams {
   const float* q;         // [T][Hq][d]
