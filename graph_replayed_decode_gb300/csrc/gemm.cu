@@ -312,11 +312,23 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
   auto issue_x = [&](int pc, int pn) {
     if (x_async) {
       const int cpr = pn * 4;  // 16-byte chunks of a row in one plane
-      for (int i = threadIdx.x; i < 2 * ntok * cpr; i += 256) {
-        const int plane = i >= ntok * cpr;
-        const int rem = i - plane * ntok * cpr, r = rem / cpr, c = rem - r * cpr;
-        const size_t off = (size_t)s_xrow[r] * p.ldx + (size_t)(kt0 + pc) * 32 + c * 8;
-        cp_async16((plane ? xl : xs) + (size_t)r * xstride + c * 8, (plane ? p.Xl : p.Xh) + off);
+      if (cpr >= 16) {         // a warp per token row, lanes over its chunks
+        for (int r = warp; r < ntok; r += 8) {
+          const size_t off = (size_t)s_xrow[r] * p.ldx + (size_t)(kt0 + pc) * 32;
+          bf16* dh = xs + (size_t)r * xstride;
+          bf16* dl = xl + (size_t)r * xstride;
+          for (int c = lane; c < cpr; c += 32) {
+            cp_async16(dh + c * 8, p.Xh + off + c * 8);
+            cp_async16(dl + c * 8, p.Xl + off + c * 8);
+          }
+        }
+      } else {
+        for (int i = threadIdx.x; i < 2 * ntok * cpr; i += 256) {
+          const int plane = i >= ntok * cpr;
+          const int rem = i - plane * ntok * cpr, r = rem / cpr, c = rem - r * cpr;
+          const size_t off = (size_t)s_xrow[r] * p.ldx + (size_t)(kt0 + pc) * 32 + c * 8;
+          cp_async16((plane ? xl : xs) + (size_t)r * xstride + c * 8, (plane ? p.Xl : p.Xh) + off);
+        }
       }
       cp_async_commit();
     } else if (warp == 0) {
@@ -632,7 +644,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     }
   } else if (EPI == EPI_QKV_ROPE) {
     const int D = p.d;
-    const int E = D / 32;
+    const int E = D / 32;  // 2 or 4 elements of a head per lane (loops below unrolled to 4)
     const int nheads_cta = rows / D;
     for (int item = warp; item < nown * nheads_cta; item += 8) {
       const int k = item / nheads_cta, hc = item - k * nheads_cta;
@@ -651,7 +663,7 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
         if (slot < -1) set_status(p.status, slot == -2 ? ST_BAD_POSITION : ST_BAD_BLOCK);
       }
       float x[4];
-      for (int e = 0; e < E; ++e) {
+      _Pragma("unroll") for (int e = 0; e < 4; ++e) if (e < E) {
         const int r = rbase + lane * E + e;
         x[e] = ts[r * TS + tok] + s_row[r];
       }
@@ -661,31 +673,31 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
         const float* nw = is_q ? s_qn : s_kn;
         if (is_q ? p.q_norm != nullptr : p.k_norm != nullptr) {
           float ss = 0.f;
-          for (int e = 0; e < E; ++e) ss += x[e] * x[e];
+          _Pragma("unroll") for (int e = 0; e < 4; ++e) if (e < E) ss += x[e] * x[e];
           ss = warp_sum(ss);
           const float rs = rsqrtf(ss / (float)D + p.eps);
-          for (int e = 0; e < E; ++e) x[e] = x[e] * rs * nw[lane * E + e];
+          _Pragma("unroll") for (int e = 0; e < 4; ++e) if (e < E) x[e] = x[e] * rs * nw[lane * E + e];
         }
         // rotate-half RoPE: element i < D/2 pairs with i + D/2, held by lane ^ 16
         const float* cs = TC ? reinterpret_cast<const float*>(tc_ring(smem) + (size_t)kTcStages * kTcStage) + (size_t)k * D
                              : (k < kCsTokens ? s_cs[k] : p.cos_sin + (size_t)s_pos[k] * D);  // [D/2][2]
         float y[4];
-        for (int e = 0; e < E; ++e) {
+        _Pragma("unroll") for (int e = 0; e < 4; ++e) if (e < E) {
           const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
           const int ii = (lane & 15) * E + e;
           const float c = cs[2 * ii], sn = cs[2 * ii + 1];
           y[e] = (lane < 16) ? (x[e] * c - other * sn) : (x[e] * c + other * sn);
         }
-        for (int e = 0; e < E; ++e) x[e] = y[e];
+        _Pragma("unroll") for (int e = 0; e < 4; ++e) if (e < E) x[e] = y[e];
       }
       if (is_q) {  // q stays fp32: the attention splits it into hi/lo operands
         float* dq = p.q_out + ((size_t)tkn * p.Hq + head) * D + lane * E;
-        for (int e = 0; e < E; ++e) dq[e] = x[e];
+        _Pragma("unroll") for (int e = 0; e < 4; ++e) if (e < E) dq[e] = x[e];
       } else {     // the cache holds bf16
         const int kvh = is_k ? head - p.Hq : head - p.Hq - p.Hkv;
         bf16* plane = is_k ? p.k_pool : p.v_pool;
         bf16* dst = plane + (((size_t)blk * p.Hkv + kvh) * 16 + off) * D;
-        for (int e = 0; e < E; e += 2)
+        _Pragma("unroll") for (int e = 0; e < 4; e += 2) if (e < E)
           *reinterpret_cast<uint32_t*>(dst + lane * E + e) = pack_bf16x2(x[e], x[e + 1]);
       }
     }
