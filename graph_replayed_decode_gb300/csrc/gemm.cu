@@ -590,28 +590,37 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
       *reinterpret_cast<float4*>(cluster.map_shared_rank(recv, q) + ((size_t)split * rows + r) * kblk + 4 * c) = v;
     }
     cluster.sync();
-    for (int i = threadIdx.x; i < rows * nown; i += 256) {  // consecutive threads: consecutive tokens of a row
-      const int r = i / nown, k = i - r * nown;
-      const int tok = tok_first + k;
-      float v = 0.f;
-      for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kblk + k];
-      ts[r * TS + tok] = v;
+    // lanes over a row's tokens (2^ksh >= nown lanes a row), 32 >> ksh rows a warp pass
+    const int ksh = nown <= 1 ? 0 : 32 - __clz(nown - 1);
+    if (ksh <= 5) {
+      for (int r = (warp << (5 - ksh)) + (lane >> ksh); r < rows; r += 8 << (5 - ksh)) {
+        const int k = lane & ((1 << ksh) - 1);
+        if (k >= nown) continue;
+        const int tok = tok_first + k;
+        float v = 0.f;
+        for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kblk + k];
+        ts[r * TS + tok] = v;
+      }
+    } else {
+      for (int i = threadIdx.x; i < rows * nown; i += 256) {
+        const int r = i / nown, k = i - r * nown;
+        const int tok = tok_first + k;
+        float v = 0.f;
+        for (int sp = 0; sp < S; ++sp) v += sp == split ? ts[r * TS + tok] : recv[((size_t)sp * rows + r) * kblk + k];
+        ts[r * TS + tok] = v;
+      }
     }
     __syncthreads();
   }
-  if (NORM_IN) {  // RMSNorm(h) W^T = (1 / rms(h)) ((h * w) W^T)
-    for (int i = threadIdx.x; i < rows * nown; i += 256) {
-      const int k = i / rows, r = i - k * rows;
-      const int tok = tok_first + k * tok_step;
-      ts[r * TS + tok] *= s_rstd[tok];
-    }
-    __syncthreads();
-  }
+  // RMSNorm(h) W^T = (1 / rms(h)) ((h * w) W^T): with NORM_IN every epilogue scales token tok's sums by
+  // rstd(tok) as it reads them.  rows (16 RG) is a power of two.
+  auto rstd = [&](int tok) { return NORM_IN ? s_rstd[tok] : 1.f; };
+  const int rows_sh = __ffs(rows) - 1;
   if (EPI == EPI_STORE_F32) {
     for (int i = threadIdx.x; i < rows * nown; i += 256) {
-      const int k = i / rows, r = i - k * rows;
+      const int k = i >> rows_sh, r = i & (rows - 1);
       const int tok = tok_first + k * tok_step;
-      p.out_f32[(size_t)(n0 + tok) * p.ldo + row0 + r] = ts[r * TS + tok] + s_row[r];
+      p.out_f32[(size_t)(n0 + tok) * p.ldo + row0 + r] = ts[r * TS + tok] * rstd(tok) + s_row[r];
     }
   } else if (EPI == EPI_RESID) {
     // h += Y, this CTA's share of each token's sum of squares (lanes over rows, warps over tokens) and
@@ -636,10 +645,11 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     const int I = p.N >> 1;
     const int half = rows >> 1;  // gate rows j: tile row r < 8 of each 16-row tile; up rows: r + 8
     for (int i = threadIdx.x; i < half * nown; i += 256) {
-      const int k = i / half, jj = i - k * half;
+      const int k = i >> (rows_sh - 1), jj = i & (half - 1);
       const int tok = tok_first + k * tok_step;
       const int r = (jj >> 3) * 16 + (jj & 7);
-      const float ga = ts[r * TS + tok], up = ts[(r + 8) * TS + tok];
+      const float rs = rstd(tok);
+      const float ga = ts[r * TS + tok] * rs, up = ts[(r + 8) * TS + tok] * rs;
       put_split(p.xh_out, p.xl_out, (size_t)(n0 + tok) * I + (row0 >> 1) + jj, ga / (1.f + expf(-ga)) * up);
     }
   } else if (EPI == EPI_QKV_ROPE) {
@@ -663,9 +673,10 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
         if (slot < -1) set_status(p.status, slot == -2 ? ST_BAD_POSITION : ST_BAD_BLOCK);
       }
       float x[4];
+      const float rs_in = rstd(tok);
       _Pragma("unroll") for (int e = 0; e < 4; ++e) if (e < E) {
         const int r = rbase + lane * E + e;
-        x[e] = ts[r * TS + tok] + s_row[r];
+        x[e] = ts[r * TS + tok] * rs_in + s_row[r];
       }
       const bool is_q = head < p.Hq;
       const bool is_k = !is_q && head < p.Hq + p.Hkv;
@@ -709,11 +720,12 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
       const int tok = tok_first + k * tok_step;
       const int tkn = n0 + tok;
       const float it = p.inv_temp[tkn];
+      const float rs_in = rstd(tok);
       unsigned long long best = 0ull;
       uint32_t omax = 0u, omin_inv = 0u;  // extremes of the finite logits, as order-preserving bits
       for (int r = lane; r < rows; r += 32) {
         const int v = row0 + r;
-        const float z = ts[r * TS + tok];
+        const float z = ts[r * TS + tok] * rs_in;
         if (wl) p.logits[(size_t)tkn * p.N + v] = z;
         const float key = sample_key(z, it, rng, (uint32_t)tkn, (uint32_t)v);
         if (wk) p.keys_out[(size_t)tkn * p.N + v] = key;
