@@ -480,11 +480,22 @@ ENG_DEVICE void gemm_body(const GemmParams& p, const TcMaps* tm) {
     __syncthreads();
     float4* red = reinterpret_cast<float4*>(area);
     ts = reinterpret_cast<float*>(area + sm.red_bytes);
+    if (KG == 1) {  // one warp per row tile: its fragments go straight into the tile
   #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-    __syncthreads();
-    for (int i = threadIdx.x; i < RG * NT * 32; i += 256) {
+      for (int nt = 0; nt < NT; ++nt) {
+        const int r0 = rt * 16 + (lane >> 2), c0 = nt * 8 + 2 * (lane & 3);
+        ts[r0 * TS + c0] = acc[nt][0];
+        ts[r0 * TS + c0 + 1] = acc[nt][1];
+        ts[(r0 + 8) * TS + c0] = acc[nt][2];
+        ts[(r0 + 8) * TS + c0 + 1] = acc[nt][3];
+      }
+    } else {
+  #pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+      __syncthreads();
+    }
+    for (int i = threadIdx.x; KG > 1 && i < RG * NT * 32; i += 256) {
       const int ln = i & 31, nt = (i >> 5) % NT, r_t = (i >> 5) / NT;
       float4 v = red[((0 * RG + r_t) * NT + nt) * 32 + ln];
       for (int j = 1; j < KG; ++j) {
