@@ -17,8 +17,10 @@
 // new token after.  Two launch shapes:
 //   * a few rows (<= 4): a CTA per (row, KV head, split), the splits of a row in one thread-block
 //     cluster, merged on chip in split order;
-//   * more rows: a fixed grid of CTAs over a flat partition of all the rows' blocks (k_attn_decode_flat
-//     below), so that rows of very different lengths still keep every SM streaming to the end.
+//   * more rows, a KV head serving at most two query heads: a fixed grid of CTAs over a flat partition of
+//     all the rows' blocks (k_attn_decode_flat below), so that rows of very different lengths still keep
+//     every SM streaming to the end;
+//   * more rows, larger query groups: a CTA per (row, KV head, split), merged through a global workspace.
 // Both merge partial results in a fixed order, so the result does not depend on which CTA or warp
 // finishes last, and every counter is back at zero when the launch ends (graph replay finds it so).
 #include <cooperative_groups.h>
@@ -206,16 +208,20 @@ ENG_DEVICE int attn_pool_block(const AttnDecodeParams& p, int r, int b) {
   return blk;
 }
 
-// ---- few rows: one CTA per (row, KV head, split), the splits of a (row, KV head) in one cluster
+// ---- one CTA per (row, KV head, split)
 
 // Work of one CTA: request row, KV head, and a range of `split_blocks` 16-key blocks.  Each of the 4
 // warps takes every 4th block of the range (cp.async double buffering; blocks already in the pool are
 // fetched before the kernel waits for the preceding kernel, only the block that holds this step's new
-// token after).  Warps merge through shared memory; the splits of a row merge on split 0 through
-// distributed shared memory, in split order.
-template <int D>
-__global__ void __launch_bounds__(128) k_attn_decode_cluster(AttnDecodeParams p) {
+// token after).  Warps merge through shared memory.  CLUSTER: the splits of a row form a thread-block
+// cluster and merge on split 0 through distributed shared memory (a few rows).  Otherwise each split
+// writes its unnormalised (O, max, sum) to a global workspace and counts itself in on an atomic counter;
+// the split that finishes last merges them, in split order, and resets the counter (rows whose KV heads
+// serve more than two query heads, where the flat partition's merges cost more than they save).
+template <int D, bool CLUSTER>
+__global__ void __launch_bounds__(128) k_attn_decode_split(AttnDecodeParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_last;
   constexpr int TILE = 16 * D;
   const int row = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -239,6 +245,14 @@ __global__ void __launch_bounds__(128) k_attn_decode_cluster(AttnDecodeParams p)
   const bool active = sl > 0 && split < nsplit;
   const int b_begin = split * p.split_blocks;
   const int b_end = min(nblk, b_begin + p.split_blocks);
+  if (!CLUSTER && !active) {  // nothing to read: a padding row (zeros from split 0) or a split past its length
+    pdl_trigger();
+    if (sl <= 0 && split == 0) {
+      pdl_wait();
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x) put_split(p.out_h, p.out_l, obase + i, 0.f);
+    }
+    return;
+  }
 
   bf16* wbuf = reinterpret_cast<bf16*>(smem) + warp * (kStages * 2 * TILE);  // kStages x (K, V) per warp
 
@@ -272,7 +286,7 @@ __global__ void __launch_bounds__(128) k_attn_decode_cluster(AttnDecodeParams p)
     if (bb == nblk - 1) break;
     issue(bb, issued);
   }
-  if (p.max_splits > 1) cluster.sync();  // every split has started before pushes into split 0
+  if (CLUSTER && p.max_splits > 1) cluster.sync();  // every split has started before pushes into split 0
   pdl_trigger();
   pdl_wait();
   for (; issued < ahead; ++issued) issue(b_begin + warp + 4 * issued, issued);
@@ -331,6 +345,37 @@ __global__ void __launch_bounds__(128) k_attn_decode_cluster(AttnDecodeParams p)
     }
   };
 
+  if (!CLUSTER) {
+    float* part = p.ws + (((size_t)row * p.Hkv + kvh) * p.max_splits + split) * G * (D + 2);
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+      const int hr = i / D, dd = i - hr * D;
+      float O, M, L;
+      partial(hr, dd, O, M, L);
+      if (nsplit == 1) {
+        put_split(p.out_h, p.out_l, obase + hr * D + dd, O / L);
+      } else {  // this split's unnormalised partial (O, M, L)
+        part[hr * (D + 2) + dd] = O;
+        if (dd == 0) {
+          part[hr * (D + 2) + D] = M;
+          part[hr * (D + 2) + D + 1] = L;
+        }
+      }
+    }
+    if (nsplit == 1) return;
+    // the last split to finish merges the partials in split order
+    __threadfence();
+    __syncthreads();
+    int* counter = p.counters + (size_t)row * p.Hkv + kvh;
+    if (threadIdx.x == 0) s_last = atomicAdd(counter, 1) == nsplit - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float* parts = p.ws + ((size_t)row * p.Hkv + kvh) * p.max_splits * G * (D + 2);
+    merge_splits<D>(p, nsplit, G, obase,
+                    [&](int sp, int hr, int j) { return __ldcg(parts + ((size_t)sp * G + hr) * (D + 2) + j); });
+    if (threadIdx.x == 0) *counter = 0;  // ready for the next launch
+    return;
+  }
   float* recv = reinterpret_cast<float*>(smem + attn_stage_bytes(D));  // split 0: [splits][G][D + 2]
   if (active) {
     float* dst = nsplit > 1 ? cluster.map_shared_rank(recv, 0) + (size_t)split * G * (D + 2) : nullptr;
@@ -615,12 +660,14 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, c
   if (p.rows <= 0) return cudaSuccess;
   if (p.max_splits < 1 || p.max_splits > kMaxSplits || p.Hq / p.Hkv > 8) return cudaErrorInvalidValue;
   if (p.d != 64 && p.d != 128) return cudaErrorInvalidValue;
-  // a few rows: merge on chip (a cluster per row and KV head); more rows: the flat partition.  Only the
-  // row count decides, and 4 is a default capture size, so an eager step and its padded bucket take the
-  // same shape.
-  const bool cluster = p.rows <= 4 && p.max_splits <= kClusterSplits;
-  if (!cluster && (!p.ws || !p.counters || p.flat_ctas < 1)) return cudaErrorInvalidValue;
+  // a few rows: merge on chip (a cluster per row and KV head); more rows: the flat partition when a KV head
+  // serves at most two query heads, else splits merged through the workspace.  Only the row count and the
+  // shape decide, and 4 is a default capture size, so an eager step and its padded bucket take the same
+  // kernel.
   const int G = p.Hq / p.Hkv;
+  const bool cluster = p.rows <= 4 && p.max_splits <= kClusterSplits;
+  const bool flat = !cluster && G <= 2;
+  if (!cluster && (!p.ws || !p.counters || (flat && p.flat_ctas < 1))) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(128);
   cfg.stream = s;
@@ -629,20 +676,25 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, c
   attr[0].val.programmaticStreamSerializationAllowed = o.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!cluster) {
+  if (flat) {
     cfg.gridDim = dim3(p.flat_ctas);
     cfg.dynamicSmemBytes = flat_smem_bytes(p.d, p.rows);
     return p.d == 128 ? launch_kernel(k_attn_decode_flat<128>, cfg, p) : launch_kernel(k_attn_decode_flat<64>, cfg, p);
   }
   cfg.gridDim = dim3(p.rows, p.Hkv, p.max_splits);
+  if (!cluster) {
+    cfg.dynamicSmemBytes = attn_stage_bytes(p.d);
+    return p.d == 128 ? launch_kernel(k_attn_decode_split<128, false>, cfg, p)
+                      : launch_kernel(k_attn_decode_split<64, false>, cfg, p);
+  }
   cfg.dynamicSmemBytes = attn_stage_bytes(p.d) + (size_t)kClusterSplits * G * (p.d + 2) * 4;
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = 1;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = p.max_splits;
   cfg.numAttrs = p.max_splits > 1 ? 2 : 1;
-  return p.d == 128 ? launch_kernel(k_attn_decode_cluster<128>, cfg, p)
-                    : launch_kernel(k_attn_decode_cluster<64>, cfg, p);
+  return p.d == 128 ? launch_kernel(k_attn_decode_split<128, true>, cfg, p)
+                    : launch_kernel(k_attn_decode_split<64, true>, cfg, p);
 }
 
 int attn_flat_ctas(int d, int rows, int sms) {

@@ -524,7 +524,9 @@ static int setup_buffers(eng_t* e) {
   if (e->attn_flat < 1) return fail(e, ENG_ECUDA, "occupancy query of the decode attention kernel failed");
   if ((int64_t)c.kv_heads * Rm * (c.max_blocks_per_seq + 8) >= (1ll << 30))
     return fail(e, ENG_EINVAL, "kv_heads * max_reqs * max_blocks_per_seq too large for decode attention");
-  TRY(dev_alloc(e, &e->attn_ws, ((size_t)Rm * c.kv_heads + 4 * (size_t)e->attn_flat) * (c.q_heads / c.kv_heads) * (d + 2)));
+  // partials: the flat partition's pieces, or the splits of each (row, KV head)
+  const size_t ws_slots = std::max((size_t)Rm * c.kv_heads + 4 * (size_t)e->attn_flat, (size_t)Rm * c.kv_heads * e->max_splits);
+  TRY(dev_alloc(e, &e->attn_ws, ws_slots * (c.q_heads / c.kv_heads) * (d + 2)));
   TRY(dev_alloc(e, &e->attn_counters, (size_t)Rm * c.kv_heads));
 
   e->used.assign(c.num_blocks, 0);

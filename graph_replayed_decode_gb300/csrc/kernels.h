@@ -161,7 +161,8 @@ struct AttnDecodeParams {
   int Hq, Hkv, d, NB;
   int split_blocks;       // KV blocks per split
   int max_splits;         // splits of the grid (<= kAttnMaxSplits)
-  float* ws;              // flat partition: [rows * Hkv + 4 * flat_ctas][G][d + 2] partials of split segments
+  float* ws;              // partials [slots][G][d + 2]: rows * Hkv + 4 * flat_ctas pieces of the flat
+                          //   partition, or rows * Hkv * max_splits splits
   int* counters;          // [rows][Hkv] finished pieces, zero between launches
   int flat_ctas;          // grid of the flat partition (more than 4 rows): CTAs resident at once
   float scale_log2;       // log2(e) / sqrt(d)
