@@ -205,8 +205,9 @@ class _CudaArray:
                                          "strides": None}
 
 
-def fill_synthetic_kv(h, s, nb: int, blocks, ctxs) -> None:
-    """Write each request's synthetic context K/V (synth.kv_context, bf16) into the engine's paged pool."""
+def fill_synthetic_kv(h, s, nb: int, blocks, ctxs, dtype: str = "bf16") -> None:
+    """Write each request's synthetic context K/V (synth.kv_context, 16-bit values of the engine's format)
+    into the engine's paged pool."""
     import torch
     from graph_replayed_decode_gb300 import eng
     ptr, nbytes = eng.eng_kv_pool(h)
@@ -216,7 +217,7 @@ def fill_synthetic_kv(h, s, nb: int, blocks, ctxs) -> None:
         pos = torch.arange(ctx, device="cuda")
         bt = torch.as_tensor(np.asarray(b, dtype=np.int64), device="cuda")
         for l in range(s.layers):
-            x = torch.from_numpy(synth.kv_context(s, l, r, ctx).view(np.int16)).to("cuda")
+            x = torch.from_numpy(synth.kv_context(s, l, r, ctx, dtype=dtype).view(np.int16)).to("cuda")
             pool[l, :, bt[pos // 16], :, pos % 16, :] = x.permute(2, 0, 1, 3)
     torch.cuda.synchronize()
 
@@ -413,10 +414,11 @@ def run_ours(args, wl: dict, rank: int, world: int, local_rank: int) -> dict | N
     return result
 
 
-def run_mixed(steps: int, warmup: int, local_rank: int) -> dict:
+def run_mixed(steps: int, warmup: int, local_rank: int, dtype: str = "bf16") -> dict:
     """The mixed packed step of the Qwen2.5-1.5B workload, eager (mixed steps are not replayed): the same step
     `steps` times with host inputs (device time with CUDA events, and end to end with the sampled ids read
-    back), against the step roofline max(bytes / HBM, flops / sustained bf16 tensor peak)."""
+    back), against the step roofline max(bytes / HBM, flops / sustained bf16 tensor peak; dense fp16 has the
+    same nominal rate).  dtype "f16" runs the fp16 variant of the model (fp16 weights, K/V and operands)."""
     import torch
     from graph_replayed_decode_gb300 import eng
     wl = MIXED
@@ -427,15 +429,16 @@ def run_mixed(steps: int, warmup: int, local_rank: int) -> dict:
     need = [-(-(plen + 1) // 16) for plen, _ in chunk] + [-(-(c + 1) // 16) for c in dctx]
     mbs = max(need)
     nb = sum(need) + 4
-    weights = synth.make_weights(s, seed=0, cache=False)
+    weights = synth.make_weights(s, seed=0, cache=False, dtype=dtype)
     stream = torch.cuda.Stream()
-    h = eng.eng_create(eng.make_config(s, nb, 64, 600, mbs), eng.TensorList(weights.items()), stream.cuda_stream)
+    h = eng.eng_create(eng.make_config(s, nb, 64, 600, mbs, dtype=dtype), eng.TensorList(weights.items(), dtype),
+                       stream.cuda_stream)
     del weights
     blocks = [eng.eng_pool_alloc(h, n) for n in need]
     bt = np.zeros((P + 32, mbs), dtype=np.int32)
     for r, b in enumerate(blocks):
         bt[r, :len(b)] = b
-    fill_synthetic_kv(h, s, nb, blocks[P:], dctx)
+    fill_synthetic_kv(h, s, nb, blocks[P:], dctx, dtype)
     prompts = [synth.prompt_ids(take, s.vocab, 50 + i) for i, (plen, take) in enumerate(chunk)]
     ids = np.concatenate(prompts + [synth.decode_ids(32, s.vocab, 2)]).astype(np.int32)
     pos = np.concatenate([np.arange(take) for _, take in chunk] + [np.array(dctx)]).astype(np.int32)
@@ -493,7 +496,8 @@ def run_mixed(steps: int, warmup: int, local_rank: int) -> dict:
     nbytes = roofline.step_bytes(s, T, [int(x) for x in seq])
     t_b = nbytes / (peaks["hbm_gbs"] * 1e9)
     t_f = flops / (peaks["bf16_tflops_sustained"] * 1e12)
-    return {"workload": wl["text"], "tokens_per_step": T, "requests": P + 32, "steps": steps, "warmup": warmup,
+    text = wl["text"] if dtype == "bf16" else wl["text"].replace("Qwen2.5-1.5B-shaped decoder", "Qwen2.5-1.5B-shaped decoder in fp16")
+    return {"workload": text, "dtype": dtype, "tokens_per_step": T, "requests": P + 32, "steps": steps, "warmup": warmup,
             "ms_per_step": t_dev * 1e3, "value": T / t_dev, "unit": "tokens/s",
             "step_roofline": {"bound": "tensor" if t_f >= t_b else "hbm", "bytes_per_step": int(nbytes),
                               "flops_per_step": int(flops), "t_roof_ms": max(t_b, t_f) * 1e3,
@@ -563,8 +567,8 @@ def run_moe(steps: int, warmup: int) -> dict:
 
 def run_extras(args, local_rank: int) -> dict:
     """The other configurations the metric is stated on, in the same run: batch-32 decode (graph-replayed)
-    and the mixed packed step, each with its own roofline, clocks and end-to-end figure; and the
-    mixture-of-experts layer of the MoE calls."""
+    and the mixed packed step (bf16, and its fp16 variant), each with its own roofline, clocks and end-to-end
+    figure; and the mixture-of-experts layer of the MoE calls."""
     import copy
     out = {}
     a = copy.copy(args)
@@ -575,6 +579,7 @@ def run_extras(args, local_rank: int) -> dict:
                                                 "device_status")}
     out["qwen3_0p6b_b32"]["kernels"] = dict(list(r["kernels"].items())[:4])
     out["qwen2p5_1p5b_mixed"] = run_mixed(min(args.steps, 16), min(args.warmup, 4), local_rank)
+    out["qwen2p5_1p5b_mixed_f16"] = run_mixed(min(args.steps, 16), min(args.warmup, 4), local_rank, dtype="f16")
     out["qwen3_30b_a3b_moe_layer"] = run_moe(min(args.steps, 20), 3)
     return out
 

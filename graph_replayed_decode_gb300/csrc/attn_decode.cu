@@ -31,6 +31,7 @@
 namespace cg = cooperative_groups;
 
 namespace grd {
+ENG_ELEM_NS_BEGIN
 
 static constexpr int kStages = 2;    // K/V blocks in flight per warp
 static constexpr int kMaxSplits = kAttnMaxSplits;  // splits of one (row, KV head)
@@ -709,4 +710,5 @@ int attn_flat_ctas(int d, int rows, int sms) {
   return (per_sm < 2 ? per_sm : 2) * sms;
 }
 
+ENG_ELEM_NS_END
 }  // namespace grd

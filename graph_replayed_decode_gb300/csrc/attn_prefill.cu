@@ -15,6 +15,7 @@
 #include "kernels.h"
 
 namespace grd {
+ENG_ELEM_NS_BEGIN
 
 template <int D>
 __global__ void __launch_bounds__(128) k_attn_prefill(AttnPrefillParams p) {
@@ -226,4 +227,5 @@ cudaError_t launch_attn_prefill(const AttnPrefillParams& p, const LaunchOpts& o,
   return cudaErrorInvalidValue;
 }
 
+ENG_ELEM_NS_END
 }  // namespace grd

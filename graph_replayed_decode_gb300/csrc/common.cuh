@@ -1,12 +1,28 @@
-// common.cuh -- shared device helpers of libeng: bf16 packing, warp reductions and thin inline-PTX
-// wrappers (warp-level bf16 MMA, ldmatrix, cp.async, programmatic dependent launch).
+// common.cuh -- shared device helpers of libeng: 16-bit element packing, warp reductions and thin
+// inline-PTX wrappers (warp-level MMA, ldmatrix, cp.async, programmatic dependent launch).
+//
+// Element type.  Weights, the K/V cache and the operand planes are 16-bit values held in the storage
+// type bf16.  The kernel files whose arithmetic depends on the format (gemm.cu, attn_decode.cu,
+// attn_prefill.cu, norm.cu, pack.cu) are compiled twice: as they stand for bfloat16, and with ENG_F16
+// defined for IEEE binary16 (the fp16 variant of a model), into the nested namespace grd::f16.  In an
+// ENG_F16 translation unit the bits in bf16 storage are binary16 values, and every conversion and MMA
+// below reads and writes them as such; no kernel converts between the formats.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 typedef __nv_bfloat16 bf16;
+
+#ifdef ENG_F16
+#define ENG_ELEM_NS_BEGIN namespace f16 {
+#define ENG_ELEM_NS_END }
+#else
+#define ENG_ELEM_NS_BEGIN
+#define ENG_ELEM_NS_END
+#endif
 
 #define ENG_DEVICE __device__ __forceinline__
 
@@ -20,16 +36,40 @@ ENG_DEVICE void set_status(int* status, int bit) {
   if (status) atomicOr(status, bit);
 }
 
-// ------------------------------------------------------------------ bf16 helpers
-ENG_DEVICE uint32_t pack_bf16x2(float lo, float hi) {
+// ------------------------------------------------------------------ 16-bit element helpers
+// (static: an ENG_F16 translation unit defines them for binary16; each unit keeps its own)
+#ifdef ENG_F16
+static ENG_DEVICE uint32_t pack_bf16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+static ENG_DEVICE float2 unpack_bf16x2(uint32_t u) {
+  __half2 v = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(v);
+}
+
+static ENG_DEVICE float elem_to_float(bf16 x) { return __half2float(*reinterpret_cast<const __half*>(&x)); }
+
+static ENG_DEVICE bf16 float_to_elem(float v) {
+  const __half h = __float2half_rn(v);
+  return *reinterpret_cast<const bf16*>(&h);
+}
+#else
+static ENG_DEVICE uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-ENG_DEVICE float2 unpack_bf16x2(uint32_t u) {
+static ENG_DEVICE float2 unpack_bf16x2(uint32_t u) {
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
   return __bfloat1622float2(v);
 }
+
+static ENG_DEVICE float elem_to_float(bf16 x) { return __bfloat162float(x); }
+
+static ENG_DEVICE bf16 float_to_elem(float v) { return __float2bfloat16_rn(v); }
+#endif
 
 ENG_DEVICE float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
@@ -37,23 +77,23 @@ ENG_DEVICE float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint3
 // lo = bf16(v - hi) (the difference is exact in fp32), so hi + lo keeps about 16 significant bits and a
 // product over the pair (W.hi + W.lo, accumulated in fp32) loses almost nothing to operand rounding.
 // Single-bf16 activations would put every projection's input through a 2^-9 rounding, and over a few
-// dozen layers that alone moves the logits by several hundredths.
-ENG_DEVICE void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  hi = *reinterpret_cast<uint32_t*>(&h);
+// dozen layers that alone moves the logits by several hundredths.  (Binary16 pairs keep about 22 bits
+// where the low half stays a normal number; below 2^-14 it loses bits to the format's narrow range.)
+static ENG_DEVICE void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  const float2 hf = unpack_bf16x2(hi);
   lo = pack_bf16x2(a - hf.x, b - hf.y);
 }
 
 // One value into the operand planes at element index i.
-ENG_DEVICE void put_split(bf16* xh, bf16* xl, size_t i, float v) {
-  const bf16 h = __float2bfloat16_rn(v);
+static ENG_DEVICE void put_split(bf16* xh, bf16* xl, size_t i, float v) {
+  const bf16 h = float_to_elem(v);
   xh[i] = h;
-  xl[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+  xl[i] = float_to_elem(v - elem_to_float(h));
 }
 
 // Two adjacent values (i even) into the operand planes.
-ENG_DEVICE void put_split2(bf16* xh, bf16* xl, size_t i, float a, float b) {
+static ENG_DEVICE void put_split2(bf16* xh, bf16* xl, size_t i, float a, float b) {
   uint32_t h, l;
   split_bf16x2(a, b, h, l);
   *reinterpret_cast<uint32_t*>(xh + i) = h;
@@ -193,9 +233,16 @@ ENG_DEVICE uint64_t umma_desc_sw128(const void* tile) {
   return ((a & 0x3FFFF) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both K-major, M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B of the element type (format code 1 for
+// bf16, 0 for binary16 -- both operands alike), both K-major, M x N.
+#ifdef ENG_F16
+static constexpr uint32_t kUmmaAbFormat = 0u;
+#else
+static constexpr uint32_t kUmmaAbFormat = 1u;
+#endif
+static __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (kUmmaAbFormat << 7) | (kUmmaAbFormat << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A . B^T, issued by one thread.
@@ -244,12 +291,18 @@ ENG_DEVICE void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// ------------------------------------------------------------------ warp MMA (m16n8k16, bf16 in, f32 accumulate)
-// A: 16x16 row-major fragment (4 regs), B: 16x8 column fragment (2 regs), C/D: 16x8 f32 (4 regs).
-ENG_DEVICE void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                         uint32_t b1) {
+// ------------------------------------------------------------------ warp MMA (m16n8k16, 16-bit in, f32 accumulate)
+// A: 16x16 row-major fragment (4 regs), B: 16x8 column fragment (2 regs), C/D: 16x8 f32 (4 regs); A and B
+// of the element type (bf16, or binary16 in an ENG_F16 unit).
+#ifdef ENG_F16
+#define ENG_MMA_TYPES "f16.f16"
+#else
+#define ENG_MMA_TYPES "bf16.bf16"
+#endif
+static ENG_DEVICE void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32." ENG_MMA_TYPES ".f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));

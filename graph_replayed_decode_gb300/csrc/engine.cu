@@ -86,6 +86,7 @@ struct eng {
   eng_config_t c{};
   int device = 0;
   int sms = 0;  // SM count of the device (grid sizing)
+  bool f16 = false;  // IEEE binary16 weights, K/V and operand planes (the grd::f16 kernels)
   cudaStream_t stream = nullptr;
   bool own_stream = false;
   cudaStream_t cap_stream = nullptr;
@@ -228,7 +229,7 @@ static std::string check_config(const eng_config_t& c) {
   if (c.q_heads / c.kv_heads > 8) return "at most 8 query heads per KV head";
   if (c.hidden % 32 || c.intermediate % 32 || (c.q_heads * c.head_dim) % 32) return "reduction widths must be multiples of 32";
   if (c.vocab % 16) return "vocab must be a multiple of 16";
-  if (c.dtype != ENG_DTYPE_BF16) return "only ENG_DTYPE_BF16 weights are supported";
+  if (c.dtype != ENG_DTYPE_BF16 && c.dtype != ENG_DTYPE_F16) return "dtype must be ENG_DTYPE_BF16 or ENG_DTYPE_F16";
   if (c.block_size != 16) return "block_size must be 16";
   if (c.num_blocks < 1 || c.max_reqs < 1 || c.max_tokens < c.max_reqs || c.max_blocks_per_seq < 1)
     return "bad engine capacity (num_blocks, max_reqs <= max_tokens, max_blocks_per_seq)";
@@ -249,18 +250,20 @@ struct WeightMap {
 };
 }  // namespace
 
-// Copies `numel` bf16 values of tensor `t` to device memory at dst.
+// Copies `numel` 16-bit values (the model's element type) of tensor `t` to device memory at dst.
 static int copy_bf16(eng_t* e, const eng_tensor_t* t, bf16* dst, int64_t numel, const char* name) {
   if (!t) return fail(e, ENG_EINVAL, std::string("missing weight ") + name);
   if (t->numel != numel) return fail(e, ENG_EINVAL, std::string("wrong numel for ") + name);
-  if (t->dtype != ENG_DTYPE_BF16) return fail(e, ENG_EINVAL, std::string("expected bf16 for ") + name);
+  if (t->dtype != e->c.dtype)
+    return fail(e, ENG_EINVAL, std::string(e->c.dtype == ENG_DTYPE_F16 ? "expected fp16 for " : "expected bf16 for ") + name);
   if (!t->data) return fail(e, ENG_EINVAL, std::string("null data for ") + name);
   CUDA_OR_FAIL(e, cudaMemcpyAsync(dst, t->data, numel * 2, t->on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
                                   e->stream));
   return ENG_OK;
 }
 
-// Loads a 1-D weight (bf16 or f32) as f32 at dst; tmp is a bf16 scratch of at least numel values.
+// Loads a 1-D weight (f32, or the model's element type) as f32 at dst; tmp is a 16-bit scratch of at least
+// numel values.
 static int load_f32(eng_t* e, const eng_tensor_t* t, float* dst, int64_t numel, bf16* tmp, const char* name) {
   if (!t) return fail(e, ENG_EINVAL, std::string("missing weight ") + name);
   if (t->numel != numel) return fail(e, ENG_EINVAL, std::string("wrong numel for ") + name);
@@ -268,9 +271,10 @@ static int load_f32(eng_t* e, const eng_tensor_t* t, float* dst, int64_t numel, 
   const cudaMemcpyKind k = t->on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
   if (t->dtype == ENG_DTYPE_F32) {
     CUDA_OR_FAIL(e, cudaMemcpyAsync(dst, t->data, numel * 4, k, e->stream));
-  } else if (t->dtype == ENG_DTYPE_BF16) {
+  } else if (t->dtype == e->c.dtype) {
     CUDA_OR_FAIL(e, cudaMemcpyAsync(tmp, t->data, numel * 2, k, e->stream));
-    CUDA_OR_FAIL(e, launch_bf16_to_f32(tmp, dst, numel, e->stream));
+    CUDA_OR_FAIL(e, e->f16 ? f16::launch_bf16_to_f32(tmp, dst, numel, e->stream)
+                           : launch_bf16_to_f32(tmp, dst, numel, e->stream));
   } else {
     return fail(e, ENG_EINVAL, std::string("unsupported dtype for ") + name);
   }
@@ -520,7 +524,7 @@ static int setup_buffers(eng_t* e) {
   // and replayed steps agree bit for bit.
   e->split_blocks = (c.max_blocks_per_seq + kAttnMaxSplits - 1) / kAttnMaxSplits;
   e->max_splits = (c.max_blocks_per_seq + e->split_blocks - 1) / e->split_blocks;
-  e->attn_flat = attn_flat_ctas(d, Rm, e->sms);
+  e->attn_flat = e->f16 ? f16::attn_flat_ctas(d, Rm, e->sms) : attn_flat_ctas(d, Rm, e->sms);
   if (e->attn_flat < 1) return fail(e, ENG_ECUDA, "occupancy query of the decode attention kernel failed");
   if ((int64_t)c.kv_heads * Rm * (c.max_blocks_per_seq + 8) >= (1ll << 30))
     return fail(e, ENG_EINVAL, "kv_heads * max_reqs * max_blocks_per_seq too large for decode attention");
@@ -546,6 +550,7 @@ static int setup_decode_step(eng_t* e) {
   const eng_config_t& c = e->c;
   const char* v = getenv("ENG_DECODE_KERNEL");
   if (v && v[0] == '0') return ENG_OK;
+  if (e->f16) return ENG_OK;  // built for bfloat16 only: fp16 models run every step on the per-layer kernels
   const int d = c.head_dim, G = c.q_heads / c.kv_heads;
   if (c.layers > 50 || G > 8 || c.kv_heads > 255 || (d != 64 && d != 128)) return ENG_OK;
   const int kx = std::max({c.hidden, c.q_heads * d, c.intermediate}) + 8;
@@ -688,7 +693,8 @@ static cudaError_t gemm_launch(eng_t* e, const GemmParams& p, const GemmSite& s,
     tm.xh = *xh;
     tm.xl = *xl;
   }
-  const cudaError_t r = launch_gemm(p, epi, norm_in, o, st, tc ? &tm : nullptr);
+  const cudaError_t r = e->f16 ? f16::launch_gemm(p, epi, norm_in, o, st, tc ? &tm : nullptr)
+                               : launch_gemm(p, epi, norm_in, o, st, tc ? &tm : nullptr);
   prof_end(e, st);
   return r;
 }
@@ -802,7 +808,7 @@ static cudaError_t enqueue_piece(eng_t* e, int T, int piece, cudaStream_t st) {
     ep.status = e->status;
     e->launches++;
     prof_begin(e, st, ENG_K_EMBED_NORM, (int64_t)T * H * (2 + 4 + 4));
-    r = launch_embed(ep, o, st);
+    r = e->f16 ? f16::launch_embed(ep, o, st) : launch_embed(ep, o, st);
     prof_end(e, st);
     if (r != cudaSuccess) return r;
   } else {
@@ -921,7 +927,7 @@ static cudaError_t enqueue_attention(eng_t* e, int l, int R, int P, int n_items,
     ap.status = e->status;
     e->launches++;
     prof_begin(e, st, ENG_K_ATTN_PREFILL, 0);
-    r = launch_attn_prefill(ap, o, st);
+    r = e->f16 ? f16::launch_attn_prefill(ap, o, st) : launch_attn_prefill(ap, o, st);
     prof_end(e, st);
     if (r != cudaSuccess) return r;
   }
@@ -952,7 +958,7 @@ static cudaError_t enqueue_attention(eng_t* e, int l, int R, int P, int n_items,
     set_prefetch(e, dp.pf_ptr, dp.pf_bytes, L.gu, e->g_gu);
     e->launches++;
     prof_begin(e, st, ENG_K_ATTN_DECODE, kv_read + (int64_t)(R - P) * Hq * d * 8);
-    r = launch_attn_decode(dp, o, st);
+    r = e->f16 ? f16::launch_attn_decode(dp, o, st) : launch_attn_decode(dp, o, st);
     prof_end(e, st);
     if (r != cudaSuccess) return r;
   }
@@ -1174,6 +1180,7 @@ int eng_create(const eng_config_t* cfg, const eng_tensor_t* weights, int32_t n_w
     return fail(nullptr, ENG_ECUDA, "no CUDA device: the engine has no CPU path");
   eng_t* e = new eng_t();
   e->c = *cfg;
+  e->f16 = cfg->dtype == ENG_DTYPE_F16;
   {
     // programmatic dependent launch between the step's kernels (ENG_PDL=0 turns it off for comparison)
     const char* v = getenv("ENG_PDL");

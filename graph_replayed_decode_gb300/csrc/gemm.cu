@@ -43,6 +43,7 @@
 namespace cg = cooperative_groups;
 
 namespace grd {
+ENG_ELEM_NS_BEGIN
 
 static constexpr int kPieceTiles = 16;          // k-tiles (x32 columns) per X piece when X does not fit whole
 static constexpr int kPreMax = 8;               // k-tiles per warp loaded into registers before waiting
@@ -980,4 +981,5 @@ bool make_tc_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+ENG_ELEM_NS_END
 }  // namespace grd

@@ -330,4 +330,18 @@ size_t decode_step_smem(int slots_n, int trows, int kx, int d, int G, int H, int
 cudaError_t decode_step_prepare(size_t smem, int* max_ctas_per_sm);
 cudaError_t launch_decode_step(const DecodeStepParams& p, int grid, size_t smem, cudaStream_t s);
 
+// The launchers whose kernels depend on the 16-bit element format, built again for IEEE binary16
+// weights, K/V and operand planes (the fp16 variant of a model; see common.cuh).  Same arguments and
+// behaviour as the bfloat16 launchers above.
+namespace f16 {
+cudaError_t launch_pack(const bf16* src, bf16* dst, int N, int K, int interleave_half, cudaStream_t s);
+cudaError_t launch_bf16_to_f32(const bf16* src, float* dst, int64_t n, cudaStream_t s);
+cudaError_t launch_embed(const EmbedParams& p, const LaunchOpts& o, cudaStream_t s);
+cudaError_t launch_gemm(const GemmParams& p, int epi, bool norm_in, const LaunchOpts& o, cudaStream_t s,
+                        const TcMaps* tc = nullptr);
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, const LaunchOpts& o, cudaStream_t s);
+int attn_flat_ctas(int d, int rows, int sms);
+cudaError_t launch_attn_prefill(const AttnPrefillParams& p, const LaunchOpts& o, cudaStream_t s);
+}  // namespace f16
+
 }  // namespace grd

@@ -10,6 +10,7 @@
 #include "kernels.h"
 
 namespace grd {
+ENG_ELEM_NS_BEGIN
 
 __global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
   // The first kernel of a step waits for the previous step to finish (its last kernel updates the step
@@ -31,7 +32,7 @@ __global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
   }
   float ss = 0.f;
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = __bfloat162float(p.embed[packed_offset(id, c, H)]);
+    const float v = elem_to_float(p.embed[packed_offset(id, c, H)]);
     p.h_out[(size_t)row * H + c] = v;
     put_split(p.xh_out, p.xl_out, (size_t)row * H + c, v * p.norm_w[c]);
     ss += v * v;
@@ -61,4 +62,5 @@ cudaError_t launch_embed(const EmbedParams& p, const LaunchOpts& o, cudaStream_t
   return cudaLaunchKernelEx(&cfg, k_embed, p);
 }
 
+ENG_ELEM_NS_END
 }  // namespace grd

@@ -4,6 +4,7 @@
 #include "kernels.h"
 
 namespace grd {
+ENG_ELEM_NS_BEGIN
 
 // One thread per packed element: gathers the source value of packed position `o`.
 __global__ void k_pack(const bf16* __restrict__ src, bf16* __restrict__ dst, int N, int K, int interleave_half) {
@@ -38,7 +39,7 @@ cudaError_t launch_pack(const bf16* src, bf16* dst, int N, int K, int interleave
 
 __global__ void k_bf16_to_f32(const bf16* __restrict__ src, float* __restrict__ dst, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = __bfloat162float(src[i]);
+    dst[i] = elem_to_float(src[i]);
 }
 
 cudaError_t launch_bf16_to_f32(const bf16* src, float* dst, int64_t n, cudaStream_t s) {
@@ -49,4 +50,5 @@ cudaError_t launch_bf16_to_f32(const bf16* src, float* dst, int64_t n, cudaStrea
   return cudaGetLastError();
 }
 
+ENG_ELEM_NS_END
 }  // namespace grd

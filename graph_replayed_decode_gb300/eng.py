@@ -160,31 +160,38 @@ def _ptr_i32(a: np.ndarray):
 
 
 def make_config(shape, num_blocks: int, max_reqs: int, max_tokens: int, max_blocks_per_seq: int,
-                sampling_filters: bool = False) -> eng_config_t:
-    """eng_config_t from a model shape (any object with the synth.ModelShape fields)."""
+                sampling_filters: bool = False, dtype: str = "bf16") -> eng_config_t:
+    """eng_config_t from a model shape (any object with the synth.ModelShape fields); dtype "bf16" or "f16"
+    names the 16-bit format of the weights and activations."""
+    if dtype not in ("bf16", "f16"):
+        raise ValueError(f"dtype must be 'bf16' or 'f16', not {dtype!r}")
     return eng_config_t(
         layers=shape.layers, hidden=shape.hidden, q_heads=shape.q_heads, kv_heads=shape.kv_heads,
         head_dim=shape.head_dim, intermediate=shape.intermediate, vocab=shape.vocab, rms_eps=shape.rms_eps,
         rope_theta=shape.rope_theta, qk_norm=int(shape.qk_norm), qkv_bias=int(shape.qkv_bias),
-        tie_embeddings=int(shape.tie_embeddings), dtype=ENG_DTYPE_BF16, block_size=16, num_blocks=num_blocks,
+        tie_embeddings=int(shape.tie_embeddings), dtype=ENG_DTYPE_BF16 if dtype == "bf16" else ENG_DTYPE_F16,
+        block_size=16, num_blocks=num_blocks,
         max_reqs=max_reqs, max_tokens=max_tokens, max_blocks_per_seq=max_blocks_per_seq,
         sampling_filters=int(sampling_filters))
 
 
 class TensorList:
-    """eng_tensor_t array over host numpy arrays (bf16 as uint16 bits) that keeps them alive."""
+    """eng_tensor_t array over host numpy arrays (16-bit values as uint16 bits, of the format dtype names:
+    "bf16" or "f16") that keeps them alive."""
 
-    def __init__(self, items: Iterable[tuple[str, np.ndarray]]):
+    def __init__(self, items: Iterable[tuple[str, np.ndarray]], dtype: str = "bf16"):
+        if dtype not in ("bf16", "f16"):
+            raise ValueError(f"dtype must be 'bf16' or 'f16', not {dtype!r}")
         self._keep = []
         recs = []
         for name, arr in items:
             arr = np.ascontiguousarray(arr)
             if arr.dtype == np.uint16:
-                dt = ENG_DTYPE_BF16
+                dt = ENG_DTYPE_BF16 if dtype == "bf16" else ENG_DTYPE_F16
             elif arr.dtype == np.float32:
                 dt = ENG_DTYPE_F32
             else:
-                raise TypeError(f"{name}: weights are bf16 bits (uint16) or float32")
+                raise TypeError(f"{name}: weights are 16-bit bits (uint16) or float32")
             nm = name.encode()
             self._keep += [arr, nm]
             recs.append(eng_tensor_t(nm, arr.ctypes.data, arr.size, dt, 0))

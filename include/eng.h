@@ -51,7 +51,7 @@ extern "C" {
 
 /* ------------------------------------------------------------------ dtypes */
 #define ENG_DTYPE_BF16 0
-#define ENG_DTYPE_F16 1 /* reserved: not accepted yet */
+#define ENG_DTYPE_F16 1 /* IEEE binary16: the fp16 variant of a model */
 #define ENG_DTYPE_F32 2
 
 typedef struct eng eng_t;
@@ -73,7 +73,10 @@ typedef struct {
   int32_t qk_norm;   /* 1: per-head RMSNorm of q and k before RoPE (Qwen3) */
   int32_t qkv_bias;  /* 1: q/k/v projections carry a bias (Qwen2.5) */
   int32_t tie_embeddings; /* 1: the LM head is the embedding matrix */
-  int32_t dtype;          /* ENG_DTYPE_BF16 */
+  int32_t dtype;          /* ENG_DTYPE_BF16 or ENG_DTYPE_F16: the 16-bit format of the weights, the K/V
+                             cache and the activation operand planes (hi/lo pairs of that format).  An
+                             fp16 engine runs every step on the per-layer kernels (the persistent decode
+                             kernel is built for bf16) */
   int32_t block_size, num_blocks, max_reqs, max_tokens, max_blocks_per_seq;
   int32_t sampling_filters; /* 1: steps may ask for top-k / top-p (eng_step_t.top_k, .top_p); every step and
                                every captured graph then also writes the logits and runs the filter kernel */
@@ -91,8 +94,8 @@ typedef struct {
  *   model.layers.{i}.mlp.down_proj.weight [hidden, intermediate]
  *   model.norm.weight [hidden]
  *   lm_head.weight [vocab, hidden] (only when tie_embeddings == 0)
- * Row-major, dtype ENG_DTYPE_BF16 (or ENG_DTYPE_F32 for norm weights and
- * biases).  on_device = 1 if `data` is a device pointer of the engine's GPU.
+ * Row-major, dtype = the config's dtype (or ENG_DTYPE_F32 for norm weights and
+ * biases); ENG_EINVAL for a matrix of the other 16-bit format.  on_device = 1 if `data` is a device pointer of the engine's GPU.
  */
 typedef struct {
   const char* name;

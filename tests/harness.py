@@ -44,8 +44,9 @@ class GpuEngine:
         self.s = s
         self.num_blocks = num_blocks
         self.max_blocks_per_seq = max_blocks_per_seq
-        cfg = self.eng.make_config(s, num_blocks, max_reqs, max_tokens, max_blocks_per_seq, sampling_filters)
-        tl = self.eng.TensorList(weights.items())
+        dtype = getattr(weights, "dtype", "bf16")  # synth weights name their 16-bit format
+        cfg = self.eng.make_config(s, num_blocks, max_reqs, max_tokens, max_blocks_per_seq, sampling_filters, dtype)
+        tl = self.eng.TensorList(weights.items(), dtype)
         self.stream = stream
         self.h = self.eng.eng_create(cfg, tl, None if stream is None else stream.cuda_stream)
         del tl
@@ -67,14 +68,14 @@ class GpuEngine:
         return self.eng.eng_pool_alloc(self.h, n)
 
     def kv_pool(self):
-        """torch int16 view [L, 2, NB+1, Hkv, 16, d] of the engine's KV pool (bf16 bits)."""
+        """torch int16 view [L, 2, NB+1, Hkv, 16, d] of the engine's KV pool (16-bit bits of the model's format)."""
         ptr, nbytes = self.eng.eng_kv_pool(self.h)
         s = self.s
         return device_view(ptr, nbytes, self.torch.int16).view(s.layers, 2, self.num_blocks + 1, s.kv_heads, 16,
                                                               s.head_dim)
 
     def fill_context(self, layer: int, blocks, kv_bits: np.ndarray):
-        """Write synthetic K/V [2, Hkv, ctx, d] (bf16 bits) of positions 0..ctx-1 through a block table."""
+        """Write synthetic K/V [2, Hkv, ctx, d] (16-bit bits) of positions 0..ctx-1 through a block table."""
         torch = self.torch
         ctx = kv_bits.shape[2]
         pool = self.kv_pool()

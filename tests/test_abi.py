@@ -4,6 +4,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 import synth
@@ -85,6 +86,28 @@ def test_config_validation_rejects_bad_shapes_before_touching_a_device():
     with pytest.raises(eng.EngError) as ei:
         eng.eng_create(cfg, eng.TensorList([]), None)
     assert ei.value.code == eng.ENG_EINVAL and "block_size" in str(ei.value)
+    cfg = eng.make_config(s, 16, 4, 64, 4)
+    cfg.dtype = eng.ENG_DTYPE_F32             # matrices are 16-bit: bf16 or fp16
+    with pytest.raises(eng.EngError) as ei:
+        eng.eng_create(cfg, eng.TensorList([]), None)
+    assert ei.value.code == eng.ENG_EINVAL and "dtype" in str(ei.value)
+
+
+def test_binding_marks_the_16_bit_format():
+    """make_config and TensorList carry the model's 16-bit format: bf16 (the default) or fp16."""
+    eng = ensure_built()
+    s = synth.shape("tiny")
+    assert eng.make_config(s, 16, 4, 64, 4).dtype == eng.ENG_DTYPE_BF16
+    assert eng.make_config(s, 16, 4, 64, 4, dtype="f16").dtype == eng.ENG_DTYPE_F16
+    w = synth.make_weights(s, seed=0, dtype="f16")
+    items = [(n, w[n]) for n in ("model.embed_tokens.weight", "model.norm.weight")]
+    tl = eng.TensorList(items + [("x", np.zeros(4, np.float32))], "f16")
+    assert [tl.array[i].dtype for i in range(tl.count)] == [eng.ENG_DTYPE_F16, eng.ENG_DTYPE_F16, eng.ENG_DTYPE_F32]
+    assert eng.TensorList(items).array[0].dtype == eng.ENG_DTYPE_BF16
+    with pytest.raises(ValueError):
+        eng.make_config(s, 16, 4, 64, 4, dtype="f32")
+    with pytest.raises(ValueError):
+        eng.TensorList(items, "fp8")
 
 
 def test_no_cpu_fallback_without_a_device():
