@@ -5,24 +5,25 @@
 // the page's A10), and section "Bottleneck": kernels that split the key/value length across the GPU are
 // the standard fix for this shape of work.  "33. Removing overhead", section "CUDA graphs for a changing
 // batch": a row with length 0 (padding) must produce zeros, never NaN, and a graphed kernel must not
-// take its grid from host-side batch values -- here the grid is (rows, kv_heads, splits) with the split
-// count fixed by the block-table width, and CTAs past a row's real length do no work.
+// take its grid from host-side batch values -- here every grid is fixed by the bucket and the engine
+// (rows x KV heads x a split count fixed by the block-table width, or the flat partition's resident
+// CTAs), and work past a row's real length is skipped.
 //
 // The G = Hq / Hkv (<= 8) query heads of a KV head share every K/V load: head g is row g of a 16-row
-// MMA tile and row g + 8 carries the low half of its operand (q as bf16 hi/lo pairs in S = Q K^T, the
+// MMA tile and row g + 8 carries the low half of its operand (q as 16-bit hi/lo pairs in S = Q K^T, the
 // probabilities as hi/lo pairs in O += P V, common.cuh), so both products keep fp32 operands at no extra
 // MMA.  A warp streams 16-key blocks through two cp.async stages (XOR-swizzled rows), computes S and
-// O += P V with bf16 m16n8k16 MMAs and keeps an online softmax in base 2.  Blocks already in the pool
-// are fetched before the kernel waits for the preceding kernel, only the block that holds this step's
-// new token after.  Two launch shapes:
+// O += P V with m16n8k16 MMAs of the element type and keeps an online softmax in base 2.  Blocks already
+// in the pool are fetched before the kernel waits for the preceding kernel, only the block that holds
+// this step's new token after.  Three launch shapes:
 //   * a few rows (<= 4): a CTA per (row, KV head, split), the splits of a row in one thread-block
 //     cluster, merged on chip in split order;
 //   * more rows, a KV head serving at most two query heads: a fixed grid of CTAs over a flat partition of
 //     all the rows' blocks (k_attn_decode_flat below), so that rows of very different lengths still keep
 //     every SM streaming to the end;
 //   * more rows, larger query groups: a CTA per (row, KV head, split), merged through a global workspace.
-// Both merge partial results in a fixed order, so the result does not depend on which CTA or warp
-// finishes last, and every counter is back at zero when the launch ends (graph replay finds it so).
+// All merge partial results in a fixed order, so the result does not depend on which CTA or warp finishes
+// last, and every counter is back at zero when the launch ends (graph replay finds it so).
 #include <cooperative_groups.h>
 
 #include "common.cuh"
