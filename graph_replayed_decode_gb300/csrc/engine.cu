@@ -519,9 +519,10 @@ static int setup_buffers(eng_t* e) {
   e->sq_stride = std::max(e->g_o.max_groups(), e->g_down.max_groups());
   TRY(dev_alloc(e, &e->sq, (size_t)Tm * e->sq_stride));
 
-  // decode attention: a few rows split each row's blocks into at most 8 splits merged on chip; more rows
-  // take the flat partition over a grid of the CTAs resident at once.  Both are fixed per engine, so eager
-  // and replayed steps agree bit for bit.
+  // decode attention: each row's blocks in at most 8 splits (merged on chip for a few rows, through the
+  // workspace for more rows with query groups larger than two), or the flat partition over a grid of the
+  // CTAs resident at once (more rows, groups of at most two).  All fixed per engine, so eager and replayed
+  // steps agree bit for bit.
   e->split_blocks = (c.max_blocks_per_seq + kAttnMaxSplits - 1) / kAttnMaxSplits;
   e->max_splits = (c.max_blocks_per_seq + e->split_blocks - 1) / e->split_blocks;
   e->attn_flat = e->f16 ? f16::attn_flat_ctas(d, Rm, e->sms) : attn_flat_ctas(d, Rm, e->sms);

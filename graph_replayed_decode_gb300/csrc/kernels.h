@@ -164,7 +164,7 @@ struct AttnDecodeParams {
   float* ws;              // partials [slots][G][d + 2]: rows * Hkv + 4 * flat_ctas pieces of the flat
                           //   partition, or rows * Hkv * max_splits splits
   int* counters;          // [rows][Hkv] finished pieces, zero between launches
-  int flat_ctas;          // grid of the flat partition (more than 4 rows): CTAs resident at once
+  int flat_ctas;          // grid of the flat partition (more than 4 rows, G <= 2): CTAs resident at once
   float scale_log2;       // log2(e) / sqrt(d)
   const void* pf_ptr;     // weights of a later kernel to prefetch into L2
   unsigned long long pf_bytes;
